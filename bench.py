@@ -1,0 +1,577 @@
+"""Benchmark of the GB300 shared-expert SwiGLU MLP library (one JSON line on rank 0).
+
+Step = one pass of the hot path over one batch: the Kimi-K3 shared-expert layer
+at decode, T = 64 tokens, hidden 7168, intermediate 6144, bf16
+(mlp_swiglu_forward: gate_up + SiLU*mul kernel, down-projection kernel).
+Headline: HBM TB/s = algorithmic bytes per step / device time per step, with the
+same number also given as microseconds per layer.  Weights are cycled over
+distinct copies (more bytes than L2), so no step reads its weights from L2.
+
+Extra lines in the same JSON object: the T = 8192 prefill layer (TFLOP/s), the
+TP8-sharded form (partials + shard_sum) and the merged MLA q_a/kv_a projection.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead.
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run each rank runs an independent replica (the layer does not
+need more than one GPU), timed between barriers, max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "shared-expert µs/layer & HBM TB/s at T=64; TFLOP/s at T=8192 (1 GB300)"
+UNIT = "TB/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+# ------------------------------------------------------------------------------------------
+# byte / flop models (algorithmic work per call)
+# ------------------------------------------------------------------------------------------
+
+def mlp_bytes(T, H, I):
+    """Weights once + x read + y written (h stays on chip / in L2 and is not counted)."""
+    return 2 * I * H * 2 + H * I * 2 + T * H * 2 + T * H * 2
+
+
+def gate_up_bytes(T, H, I):
+    """Bytes of the gate_up launch: W_gate_up + x + h written."""
+    return 2 * I * H * 2 + T * H * 2 + T * I * 2
+
+
+def mlp_flops(T, H, I):
+    return 2 * T * (2 * I * H + H * I)
+
+
+def gate_up_flops(T, H, I):
+    return 2 * T * 2 * I * H
+
+
+# ------------------------------------------------------------------------------------------
+# environment helpers
+# ------------------------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS_SUSTAINED, "source": "fallback"}
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ["tc.cu", "common.cuh", "tc.h"]:
+        with open(os.path.join(ROOT, "moe_shared_expert_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key):
+    """ncu DRAM bytes per launch recorded in profiles/traffic.json, if the kernel source
+    still matches the one that was profiled; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons around the timed region."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.path = None
+        self.windows = {}
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clk", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i", str(index),
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def mark(self, name, t0, t1):
+        self.windows[name] = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+
+    def summary(self, name, fallback_name=None):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:9]))
+                except Exception:
+                    continue
+        if not rows:
+            return None
+
+        def pick(win):
+            t0, t1 = self.windows[win]
+            return [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+
+        sel = pick(name) if name in self.windows else []
+        window = name
+        if len(sel) < 2 and fallback_name in self.windows:
+            sel = pick(fallback_name)
+            window = fallback_name
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": rows[-1][2], "reasons": [], "samples": 0, "window": window}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sel for i, v in enumerate(r[4]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "power_w_max": max(r[3] for r in sel) if False else None,
+                "reasons": reasons, "samples": len(sel), "window": window}
+
+
+# ------------------------------------------------------------------------------------------
+# distributed plumbing
+# ------------------------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def done(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------
+
+def dev_bf16(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def weight_copies(wgu0, wd0, n):
+    """Copy 0 is the drawn weight; copies 1.. are row rotations of it (same distribution,
+    distinct bytes and addresses), so consecutive steps stream different memory."""
+    import torch
+    gus, wds = [wgu0], [wd0]
+    for i in range(1, n):
+        gus.append(torch.roll(wgu0, shifts=977 * i, dims=0).contiguous())
+        wds.append(torch.roll(wd0, shifts=331 * i, dims=0).contiguous())
+    return gus, wds
+
+
+def time_loop(fn, K, stream):
+    import torch
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for i in range(K):
+        fn(i)
+    e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e) / 1e3   # seconds
+
+
+def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=None):
+    """Replicated shared-expert layer: returns dict with device time, e2e time and phase times."""
+    import torch
+    import moe_shared_expert_gb300 as mse
+    L = mse.lib()
+    T, H, I = w.T, w.H, w.I
+    x = dev_bf16(W.make_x(w))
+    wgu_b, wd_b = W.make_mlp_weights(w)
+    gus, wds = weight_copies(dev_bf16(wgu_b), dev_bf16(wd_b), layers)
+    del wgu_b, wd_b
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    ws = mse.new_mlp_workspace(T, H, I)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    px, py, pws, wsb = x.data_ptr(), y.data_ptr(), ws.data_ptr(), ws.numel()
+    pgu = [g.data_ptr() for g in gus]
+    pwd = [d.data_ptr() for d in wds]
+    cap = T * H
+    bad = [0]
+
+    def step(i):
+        j = i % layers
+        bad[0] |= L.mlp_swiglu_forward(px, T, H, I, pgu[j], pwd[j], py, cap, pws, wsb, sp)
+
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    dev_s = time_loop(step, K, stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t1 = time.time()
+    if clocks:
+        clocks.mark(f"{w.name}.timed", t0, t1)
+    if bad[0]:
+        raise RuntimeError(f"mlp_swiglu_forward returned an error status ({bad[0]})")
+    st = mse.poll_device_error()
+    if st:
+        raise RuntimeError(f"device error {mse.STATUS.get(st)}")
+
+    # per-kernel durations: CUDA events recorded by the library between its two kernels
+    n_ph = min(phase_steps, K)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ph)]
+    for i in range(n_ph):
+        mse.set_phase_events(*evs[i])
+        step(i)
+    mse.set_phase_events(None, None, None)
+    torch.cuda.synchronize()
+    gate_up_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    down_ms = [e[1].elapsed_time(e[2]) for e in evs]
+
+    # end to end through the public API with host buffers
+    n_e2e = e2e_steps if e2e_steps is not None else min(K, 2000)
+    xh = torch.from_numpy(W.make_x(w).view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+
+    def e2e_step(i):
+        j = i % layers
+        xd.copy_(xh, non_blocking=True)
+        bad[0] |= L.mlp_swiglu_forward(xd.data_ptr(), T, H, I, pgu[j], pwd[j], py, cap, pws, wsb, sp)
+        yh.copy_(y, non_blocking=True)
+
+    for i in range(min(Wm, 10)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e2e_s = time_loop(e2e_step, n_e2e, stream)
+    torch.cuda.synchronize()
+    if bad[0]:
+        raise RuntimeError("error status in e2e loop")
+    del gus, wds
+    torch.cuda.empty_cache()
+    return {"dev_s": dev_s, "K": K, "e2e_s": e2e_s, "e2e_K": n_e2e,
+            "gate_up_ms": statistics.mean(gate_up_ms), "down_ms": statistics.mean(down_ms),
+            "gate_up_ms_median": statistics.median(gate_up_ms), "h2d": T * H * 2, "d2h": T * H * 2}
+
+
+def bench_tp8(w, K, Wm, layers):
+    import torch
+    import moe_shared_expert_gb300 as mse
+    L = mse.lib()
+    T, H, I, tp = w.T, w.H, w.I, w.tp
+    x = dev_bf16(W.make_x(w))
+    wgu_b, wd_b = W.make_mlp_weights(w)
+    gus, wds = weight_copies(dev_bf16(wgu_b), dev_bf16(wd_b), layers)
+    parts = torch.empty((tp, T, H), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    ws = mse.new_mlp_workspace(T, H, I)
+    sp = torch.cuda.current_stream().cuda_stream
+    pgu = [g.data_ptr() for g in gus]
+    pwd = [d.data_ptr() for d in wds]
+    bad = [0]
+
+    def step(i):
+        j = i % layers
+        bad[0] |= L.mlp_swiglu_shard_partial(x.data_ptr(), T, H, I, pgu[j], pwd[j], tp, 0, tp, parts.data_ptr(),
+                                             0, parts.numel(), ws.data_ptr(), ws.numel(), sp)
+        bad[0] |= L.shard_sum(parts.data_ptr(), 0, tp, T, H, out.data_ptr(), out.numel(), sp)
+
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    s = time_loop(step, K, torch.cuda.current_stream())
+    if bad[0]:
+        raise RuntimeError("tp8 error status")
+    del gus, wds
+    torch.cuda.empty_cache()
+    return s / K
+
+
+def bench_mla(w, K, Wm, copies=24):
+    import torch
+    import moe_shared_expert_gb300 as mse
+    L = mse.lib()
+    T, H, q, kv, tp = w.T, w.H, w.q_dim, w.kv_dim, w.tp
+    C = q + kv
+    x = dev_bf16(W.make_x(w))
+    w0 = dev_bf16(W.make_merged_weight(w))
+    ws_ = [w0] + [torch.roll(w0, shifts=13 * i, dims=0).contiguous() for i in range(1, copies)]
+    lo = torch.empty((T, C), dtype=torch.bfloat16, device="cuda")
+    rm = torch.empty((T, C), dtype=torch.bfloat16, device="cuda")
+    wsp = mse.new_merged_workspace(T, H, q, kv)
+    sp = torch.cuda.current_stream().cuda_stream
+    pw = [t.data_ptr() for t in ws_]
+    bad = [0]
+
+    def step(i):
+        bad[0] |= L.merged_proj_forward(x.data_ptr(), T, H, pw[i % copies], q, kv, tp, lo.data_ptr(), rm.data_ptr(),
+                                        T * C, wsp.data_ptr(), wsp.numel(), sp)
+
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    s = time_loop(step, K, torch.cuda.current_stream())
+    if bad[0]:
+        raise RuntimeError("mla error status")
+    return s / K
+
+
+def cpu_oracle_baseline(w, max_rows=None):
+    """The oracle as it stands on the host cores: the full decode step (all T token rows)."""
+    import oracle
+    x = W.make_x(w)
+    wgu, wd = W.make_mlp_weights(w)
+    rows = None if max_rows is None else np.arange(min(max_rows, w.T))
+    n = w.T if rows is None else len(rows)
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.mlp_forward(x, wgu, wd, rows=rows, nthreads=threads)
+    dt = time.perf_counter() - t0
+    frac = n / w.T
+    value = frac * mlp_bytes(w.T, w.H, w.I) / dt / 1e12
+    return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {w.T} token rows of the {w.name} layer (H={w.H}, I={w.I}), fp64, "
+                      f"{dt:.2f} s wall on {threads} threads"}
+
+
+def gpu_arm(args):
+    import torch
+    dist = Dist()
+    torch.cuda.set_device(dist.local)
+    dist.init("nccl")
+    from moe_shared_expert_gb300 import _build
+    if dist.local == 0:
+        _build.build()
+    dist.barrier()
+    import moe_shared_expert_gb300 as mse
+    mse.lib()
+    peaks = load_peaks()
+    clocks = ClockSampler(dist.local) if dist.rank == 0 else None
+
+    w = W.DECODE_T64
+    t_w0 = time.time()
+    r = bench_mlp(w, args.steps, args.warmup, args.layers, dist, clocks=clocks)
+    dev_s = dist.max(r["dev_s"])
+    e2e_s = dist.max(r["e2e_s"])
+    if clocks:
+        clocks.mark("decode.all", t_w0, time.time())
+
+    extra = {}
+    if not args.decode_only:
+        wp = W.PREFILL_T8192
+        t_p0 = time.time()
+        rp = bench_mlp(wp, args.prefill_steps, max(3, min(args.warmup, 5)), 2, dist, clocks=clocks,
+                       phase_steps=min(10, args.prefill_steps), e2e_steps=0)
+        if clocks:
+            clocks.mark("prefill.all", t_p0, time.time())
+        ps = dist.max(rp["dev_s"]) / args.prefill_steps
+        gu_fl = gate_up_flops(wp.T, wp.H, wp.I)
+        ach = gu_fl / (rp["gate_up_ms"] * 1e-3) / 1e12
+        extra["prefill_t8192"] = {
+            "ms_per_layer": ps * 1e3, "tflops": mlp_flops(wp.T, wp.H, wp.I) / ps / 1e12,
+            "frac_of_bf16_peak": mlp_flops(wp.T, wp.H, wp.I) / ps / 1e12 / peaks["bf16_tflops_sustained"],
+            "gate_up_ms": rp["gate_up_ms"], "down_ms": rp["down_ms"],
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": ach / peaks["bf16_tflops"], "traffic": profiled_traffic("std_gate_up_prefill"),
+                         "peak_kind": f"burst bf16 ({peaks['source']})"},
+            "gpu_launches": 2 * args.prefill_steps,
+        }
+        w3 = W.TP8_EMULATED
+        s3 = bench_tp8(w3, args.aux_steps, args.warmup, args.layers)
+        b3 = mlp_bytes(w3.T, w3.H, w3.I)
+        extra["tp8_emulated_t128"] = {"us": s3 * 1e6, "tbps_algorithmic": b3 / s3 / 1e12,
+                                      "frac_of_hbm": b3 / s3 / 1e9 / peaks["hbm_gbs"],
+                                      "partials_roundtrip_bytes": 2 * w3.tp * w3.T * w3.H * 2,
+                                      "gpu_launches_per_step": 3}
+        w4 = W.MLA_MERGED
+        s4 = bench_mla(w4, args.aux_steps, args.warmup)
+        C = w4.q_dim + w4.kv_dim
+        b4 = C * w4.H * 2 + w4.T * w4.H * 2 + w4.T * C * 2
+        extra["mla_merged_tp16_t128"] = {"us": s4 * 1e6, "tbps_algorithmic": b4 / s4 / 1e12,
+                                         "frac_of_hbm": b4 / s4 / 1e9 / peaks["hbm_gbs"],
+                                         "outputs": "logical + rank-major", "weight_copies_cycled": 24}
+    if clocks:
+        clocks.stop()
+
+    if dist.rank != 0:
+        dist.done()
+        return
+    N = dist.world
+    K = args.steps
+    bytes_step = mlp_bytes(w.T, w.H, w.I)
+    ms = dev_s / K * 1e3
+    value = N * bytes_step * K / dev_s / 1e12
+    gu_bytes = gate_up_bytes(w.T, w.H, w.I)
+    ach = gu_bytes / (r["gate_up_ms"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": N, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "us_per_layer": ms * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "weights": "N(0,1/fan_in) bf16, seed 1",
+                   "x": "N(0,1) bf16", "l2": f"inputs larger than L2: {args.layers} distinct weight copies "
+                   f"({args.layers * 264.2:.0f} MB) cycled across steps", "parallelism": f"replicas x{N}"},
+        "clocks": clocks.summary(f"{w.name}.timed", "decode.all") if clocks else None,
+        "e2e": {"value": N * bytes_step * r["e2e_K"] / e2e_s / 1e12 if r["e2e_K"] else None, "unit": UNIT,
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_K"]},
+        "gpu_launches": 2 * K,
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": profiled_traffic("swapab_gate_up_decode"),
+                     "kernel": "swapab_kernel<EPI_SWIGLU> (gate_up + SiLU*mul)",
+                     "kernel_ms": r["gate_up_ms"], "algorithmic_bytes": gu_bytes,
+                     "peak_kind": f"HBM copy ({peaks['source']})"},
+        "step_frac_of_hbm": bytes_step / (dev_s / K) / 1e9 / peaks["hbm_gbs"],
+        "down_kernel_ms": r["down_ms"],
+    }
+    if extra:
+        line["also"] = extra
+    if not args.no_cpu_baseline and N == 1:
+        line["cpu_baseline"] = cpu_oracle_baseline(w)
+    print(json.dumps(line), flush=True)
+    dist.done()
+
+
+# ------------------------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ------------------------------------------------------------------------------------------
+
+def reference_arm(args):
+    dist = Dist()
+    if dist.rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = W.DECODE_T64
+    x = W.make_x(w)
+    wgu, wd = W.make_mlp_weights(w)
+    threads = oracle.default_threads()
+    # calibrate one token row, then size each step's sample so the whole run stays
+    # within a few minutes: r token rows of the layer, or one row of one intermediate
+    # slice (a shard partial) when even one full row per step is too much.
+    t0 = time.perf_counter()
+    oracle.mlp_forward(x, wgu, wd, rows=np.array([0]), nthreads=threads)
+    t_row = time.perf_counter() - t0
+    budget = float(args.ref_budget_s)
+    per_step = budget / max(1, args.steps + args.warmup)
+    if per_step >= t_row:
+        rows = int(min(w.T, max(1, per_step // t_row)))
+        tp = 1
+    else:
+        rows = 1
+        tp = 96                                    # one 64-wide intermediate slice
+    sample_rows = np.arange(rows)
+    frac = rows / w.T / tp
+
+    def step(i):
+        if tp == 1:
+            oracle.mlp_forward(x, wgu, wd, rows=sample_rows, nthreads=threads)
+        else:
+            oracle.shard_partial(x, wgu, wd, tp, i % tp, oracle.BF16, rows=sample_rows, nthreads=threads)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = frac * mlp_bytes(w.T, w.H, w.I) * args.steps / dt / 1e12
+    sample = (f"{rows} of {w.T} token rows" if tp == 1 else f"1 token row x 1/{tp} intermediate slice") + \
+             f" of the {w.name} layer per step, fp64 oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=4, help="distinct weight copies cycled")
+    ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--aux-steps", type=int, default=2000)
+    ap.add_argument("--decode-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,235 @@
+/*
+ * mse.h -- C ABI of the GB300 (sm_103a) shared-expert SwiGLU MLP library.
+ *
+ * The library computes, on one GPU:
+ *   - the Kimi-K3 shared-expert / dense SwiGLU MLP
+ *       y = W_down . ( SiLU(W_gate . x) * (W_up . x) )
+ *     with a merged gate_up weight (gate rows first), hidden 7168 and
+ *     intermediate 6144 in bf16
+ *     ("[Kimi-K3] Add option to shard the shared expert instead of replicating",
+ *      sections "Problem" and "Change");
+ *   - the tensor-parallel sharded form of that MLP: shard r of tp owns the
+ *     intermediate slice [r*s, (r+1)*s), s = I/tp, computes a partial output over
+ *     it for all gathered tokens, and the partials are summed -- the sum half of
+ *     the reduce-scatter; rank r keeps token rows [r*T/tp, (r+1)*T/tp)
+ *     (same page, section "Change"; prhub analysis of vllm PR #50656, sections
+ *      "实现拆解" and "关键源码片段");
+ *   - the merged MLA q_a/kv_a latent projection stored as tensor-parallel
+ *     column shards, whose gathered output is rank-major and is restored to the
+ *     logical [q_a | kv_a] layout
+ *     ("[II] TP-shard Kimi MLA latent projections", sections "Behavior",
+ *      "Technical reason" and "Compatibility").
+ *
+ * Conventions (every entry point):
+ *   - bf16 tensors are uint16_t bit patterns; all tensors are dense row-major.
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The library
+ *     allocates no device memory; scratch comes from the caller's workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Launches are asynchronous on it; nothing synchronises.
+ *   - The return value reports host-side validation and launch errors.  Errors
+ *     raised on the device (a bounded wait that ran out) are reported later by
+ *     mse_poll_device_error().
+ *   - Arguments are validated before any CUDA call, so invalid calls fail the
+ *     same way with or without a GPU.  There is no CPU fallback: on a device
+ *     other than sm_103 the calls return MSE_ERR_UNSUPPORTED_DEVICE.
+ *   - "capacity" arguments are element counts of the caller's buffer; a buffer
+ *     smaller than the geometry needs is rejected as MSE_ERR_GEOMETRY (the
+ *     truncated-geometry rejection of the MLA page, section "Validation").
+ *   - The library is thread-safe; calls on the same stream are ordered.
+ */
+#ifndef MSE_H
+#define MSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define MSE_API __attribute__((visibility("default")))
+#else
+#define MSE_API
+#endif
+
+typedef uint16_t mse_bf16;
+
+typedef enum {
+    MSE_OK = 0,
+    MSE_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, bad enum      */
+    MSE_ERR_NOT_DIVISIBLE = 2,      /* I, H, q or kv not divisible by tp; T by parts  */
+    MSE_ERR_GEOMETRY = 3,           /* capacity too small, rank range outside [0,tp)  */
+    MSE_ERR_WORKSPACE = 4,          /* workspace missing, too small or misaligned     */
+    MSE_ERR_UNSUPPORTED_DEVICE = 5, /* no CUDA device, or not compute capability 10.3 */
+    MSE_ERR_CUDA = 6,               /* a CUDA runtime call failed                      */
+    MSE_ERR_TIMEOUT = 7,            /* a device-side bounded wait ran out              */
+    MSE_ERR_UNSUPPORTED_SHAPE = 8   /* kernel path forced by mse_set_kernel_path()
+                                       cannot serve this shape/alignment               */
+} mse_status;
+
+typedef enum { MSE_BF16 = 0, MSE_F32 = 1 } mse_dtype;
+
+/* Kernel path selection (process-wide; default MSE_PATH_AUTO).
+ *   AUTO:        tensor-core (tcgen05/TMA) kernels where the shape and the
+ *                16-byte alignment allow, else the generic CUDA-core kernels.
+ *   GENERIC:     always the generic CUDA-core kernels (any shape).
+ *   TENSORCORE:  always tcgen05 kernels; calls they cannot serve return
+ *                MSE_ERR_UNSUPPORTED_SHAPE. */
+typedef enum { MSE_PATH_AUTO = 0, MSE_PATH_GENERIC = 1, MSE_PATH_TENSORCORE = 2 } mse_kernel_path;
+
+/* ---------------------------------------------------------------------------
+ * Workspace sizing.  The workspace holds the bf16 intermediate h [T x I] and,
+ * for the tensor-core path, fp32 split-K partial tiles and tile counters.
+ * It must be 256-byte aligned and ZERO-FILLED before its first use; every call
+ * that completes leaves the counter region zero again, so one workspace can be
+ * reused by consecutive calls on one stream.  Calls that run concurrently
+ * (different streams) need different workspaces.  After MSE_ERR_TIMEOUT the
+ * caller must zero the workspace again.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes needed by mlp_swiglu_forward and mlp_swiglu_shard_partial for T tokens
+ * (the same size serves both; tp does not change it).  Returns 0 on invalid
+ * arguments. */
+MSE_API size_t mlp_swiglu_workspace_bytes(int64_t T, int64_t H, int64_t I);
+
+/* Bytes needed by merged_proj_forward.  Returns 0 on invalid arguments. */
+MSE_API size_t merged_proj_workspace_bytes(int64_t T, int64_t H, int64_t q_dim, int64_t kv_dim);
+
+/* ---------------------------------------------------------------------------
+ * Replicated SwiGLU MLP ("[Kimi-K3] Add option to shard the shared expert
+ * instead of replicating", section "Change": gate_up projection, SiluAndMul,
+ * down projection; the replicated path when the flag is off).
+ *
+ *   x          [T x H]    bf16 tokens
+ *   w_gate_up  [2I x H]   bf16; rows [0, I) = W_gate, rows [I, 2I) = W_up
+ *   w_down     [H x I]    bf16 (out x in)
+ *   y          [T x H]    bf16 output, y_capacity >= T*H elements
+ *
+ *   g = x W_gate^T, u = x W_up^T accumulate in fp32 and are not rounded;
+ *   h = bf16_rne(silu(g) * u) is rounded once and kept in the workspace;
+ *   y = bf16_rne(h W_down^T) with fp32 accumulation.
+ * ------------------------------------------------------------------------- */
+MSE_API mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I,
+                              const mse_bf16 *w_gate_up, const mse_bf16 *w_down,
+                              mse_bf16 *y, int64_t y_capacity,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Partial outputs of shards [rank_first, rank_first + rank_count) of a tp-way
+ * shard of the MLP over the intermediate dimension (prhub analysis of vllm
+ * PR #50656, section "关键源码片段": shard r uses gate rows and up rows
+ * [r*s, (r+1)*s) and down columns [r*s, (r+1)*s); the down projection is
+ * RowParallel and partial over the intermediate dimension per the Kimi-K3 PR,
+ * section "Change").  All T tokens are the gathered token set.
+ *
+ *   partials   [rank_count x T x H], partial_dtype MSE_BF16 or MSE_F32;
+ *              partials[i] is the partial of rank rank_first + i, rounded once
+ *              from its fp32 accumulator; partials_capacity >= rank_count*T*H.
+ *
+ * Errors: MSE_ERR_NOT_DIVISIBLE if I % tp or H % tp (the divisibility rule of
+ * the sharding gate, prhub section "实现拆解"); MSE_ERR_GEOMETRY if
+ * rank_first < 0, rank_count < 1 or rank_first + rank_count > tp.
+ * ------------------------------------------------------------------------- */
+MSE_API mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int64_t I,
+                                    const mse_bf16 *w_gate_up, const mse_bf16 *w_down,
+                                    int tp, int rank_first, int rank_count,
+                                    void *partials, mse_dtype partial_dtype,
+                                    int64_t partials_capacity,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Sum of partials: the reduction half of the block-end reduce-scatter
+ * (Kimi-K3 PR, section "Change": it sums across TP and restores the sequence
+ * sharding).  out[t, n] = bf16_rne( sum_{r ascending} partials[r, t, n] ) with
+ * fp32 accumulation.  Rank r's scatter share is the row block
+ * [r*T/n_parts, (r+1)*T/n_parts) of `out` (a view; nothing is copied).
+ *
+ *   partials   [n_parts x T x H] of partial_dtype
+ *   out        [T x H] bf16, out_capacity >= T*H
+ *
+ * Errors: MSE_ERR_NOT_DIVISIBLE if T % n_parts != 0 (token rows cannot be
+ * scattered evenly).
+ * ------------------------------------------------------------------------- */
+MSE_API mse_status shard_sum(const void *partials, mse_dtype partial_dtype, int n_parts,
+                     int64_t T, int64_t H, mse_bf16 *out, int64_t out_capacity, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Merged MLA q_a/kv_a latent projection ("[II] TP-shard Kimi MLA latent
+ * projections", section "Behavior").  C = q_dim + kv_dim.
+ *
+ *   x            [T x H] bf16
+ *   w            [C x H] bf16, logical row order: q_a rows then kv_a rows
+ *   out_logical    nullable, [T x C] bf16 in logical column order [q_a | kv_a]
+ *   out_rank_major nullable, [T x C] bf16 in gathered order: for each rank r
+ *                  ascending, its q_a columns [r*q/tp, (r+1)*q/tp) then its kv_a
+ *                  columns [r*kv/tp, (r+1)*kv/tp)  (the layout a tensor-parallel
+ *                  gather of merged column shards produces)
+ *   At least one output must be non-null; out_capacity >= T*C.
+ *   out = bf16_rne(x w^T) with fp32 accumulation.
+ *
+ * Errors: MSE_ERR_NOT_DIVISIBLE if q_dim % tp or kv_dim % tp (every merged
+ * output size must be divisible by tp, section "Compatibility").
+ * ------------------------------------------------------------------------- */
+MSE_API mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const mse_bf16 *w,
+                               int64_t q_dim, int64_t kv_dim, int tp,
+                               mse_bf16 *out_logical, mse_bf16 *out_rank_major,
+                               int64_t out_capacity,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Rank-major -> logical reorder alone (MLA page, sections "Behavior" and
+ * "Technical reason": the merged-column gather is rank-major and the logical
+ * q_a-then-kv_a ranges are restored explicitly).  A pure permutation of 16-bit
+ * words: gathered column g = r*(qs+ks) + l maps to logical column
+ * r*qs + l (l < qs) or q_dim + r*ks + (l - qs) (l >= qs), qs = q/tp, ks = kv/tp.
+ *
+ *   rank_major, logical: [T x C] bf16, capacity >= T*C each; must not overlap.
+ * ------------------------------------------------------------------------- */
+MSE_API mse_status merged_proj_reorder(const mse_bf16 *rank_major, mse_bf16 *logical, int64_t T,
+                               int64_t q_dim, int64_t kv_dim, int tp, int64_t capacity,
+                               void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Errors raised on the device and process-wide settings.
+ * ------------------------------------------------------------------------- */
+
+/* Synchronises `stream`, then reads and clears the library's device error word
+ * on the current device: MSE_OK, MSE_ERR_TIMEOUT, or MSE_ERR_CUDA if the
+ * synchronisation itself failed. */
+MSE_API mse_status mse_poll_device_error(void *stream);
+
+/* Upper bound, in nanoseconds, of every device-side wait of later launches
+ * (default 2e9 = 2 s).  A wait that runs out sets the device error word, the
+ * kernel drains its in-flight copies, frees its tensor memory and returns. */
+MSE_API void mse_set_wait_limit_ns(uint64_t ns);
+MSE_API uint64_t mse_get_wait_limit_ns(void);
+
+/* Kernel path selection, see mse_kernel_path.  Returns the previous value. */
+MSE_API int mse_set_kernel_path(int path);
+
+/* Failure-detection self test: launches one CTA that waits on a barrier no one
+ * arrives on, bounded by `limit_ns`.  The wait runs out by design; the kernel
+ * records MSE_ERR_TIMEOUT in the device error word and returns, leaving the
+ * context usable.  Read the result with mse_poll_device_error(). */
+MSE_API mse_status mse_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/* Timing hook for profiling harnesses.  While set, every mlp_swiglu_forward call
+ * records ev_begin before its first kernel, ev_mid between the gate_up and the
+ * down kernel, and ev_end after the down kernel, on its stream (cudaEvent_t
+ * handles passed as void*; all three non-null, or all null to clear).  The
+ * records separate the two kernels, so launches made while the hook is set do
+ * not overlap them. Process-wide; not meant for concurrent callers. */
+MSE_API void mse_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end);
+
+/* Human-readable name of a status code (static string). */
+MSE_API const char *mse_status_string(mse_status s);
+
+/* Library version string, e.g. "mse 0.1 sm_103a". */
+MSE_API const char *mse_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSE_H */

@@ -1,0 +1,265 @@
+"""GB300 (sm_103a) Kimi-K3 shared-expert SwiGLU MLP: thin Python binding of ``libmse.so``.
+
+Every step of the computation runs in the CUDA library behind the C ABI of
+``include/mse.h``; this module only marshals torch tensors (device memory and
+streams) into pointers and sizes and turns status codes into exceptions.  There
+is no CPU or PyTorch fallback: if the library is missing, every call raises.
+
+Functions carry the C-ABI names:
+    mlp_swiglu_forward, mlp_swiglu_shard_partial, shard_sum,
+    merged_proj_forward, merged_proj_reorder
+plus the workspace queries, the device-error poll and the settings.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+__all__ = [
+    "MSEError", "lib", "library_path", "mlp_swiglu_forward", "mlp_swiglu_shard_partial", "shard_sum",
+    "merged_proj_forward", "merged_proj_reorder", "mlp_swiglu_workspace_bytes", "merged_proj_workspace_bytes",
+    "poll_device_error", "set_wait_limit_ns", "get_wait_limit_ns", "set_kernel_path", "selftest_wait_timeout",
+    "set_phase_events", "BF16", "F32", "PATH_AUTO", "PATH_GENERIC", "PATH_TENSORCORE", "STATUS",
+]
+
+BF16, F32 = 0, 1
+PATH_AUTO, PATH_GENERIC, PATH_TENSORCORE = 0, 1, 2
+STATUS = {
+    0: "MSE_OK", 1: "MSE_ERR_INVALID_ARG", 2: "MSE_ERR_NOT_DIVISIBLE", 3: "MSE_ERR_GEOMETRY",
+    4: "MSE_ERR_WORKSPACE", 5: "MSE_ERR_UNSUPPORTED_DEVICE", 6: "MSE_ERR_CUDA", 7: "MSE_ERR_TIMEOUT",
+    8: "MSE_ERR_UNSUPPORTED_SHAPE",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+class MSEError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = int(status)
+        self.name = STATUS.get(self.status, f"status {status}")
+        super().__init__(f"{func}: {self.name}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"libmse.so not built ({_build.LIB}); run __graft_entry__.build() first")
+            L = ctypes.CDLL(_build.LIB)
+            P, i64, ci, sz, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64
+            sig = {
+                "mlp_swiglu_workspace_bytes": (sz, [i64, i64, i64]),
+                "merged_proj_workspace_bytes": (sz, [i64, i64, i64, i64]),
+                "mlp_swiglu_forward": (ci, [P, i64, i64, i64, P, P, P, i64, P, sz, P]),
+                "mlp_swiglu_shard_partial": (ci, [P, i64, i64, i64, P, P, ci, ci, ci, P, ci, i64, P, sz, P]),
+                "shard_sum": (ci, [P, ci, ci, i64, i64, P, i64, P]),
+                "merged_proj_forward": (ci, [P, i64, i64, P, i64, i64, ci, P, P, i64, P, sz, P]),
+                "merged_proj_reorder": (ci, [P, P, i64, i64, i64, ci, i64, P]),
+                "mse_poll_device_error": (ci, [P]),
+                "mse_set_wait_limit_ns": (None, [u64]),
+                "mse_get_wait_limit_ns": (u64, []),
+                "mse_set_kernel_path": (ci, [ci]),
+                "mse_selftest_wait_timeout": (ci, [u64, P]),
+                "mse_set_phase_events": (None, [P, P, P]),
+                "mse_status_string": (ctypes.c_char_p, [ci]),
+                "mse_version": (ctypes.c_char_p, []),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(func: str, status: int) -> None:
+    if status != 0:
+        raise MSEError(func, status)
+
+
+def _need(t, name: str, dtypes, ndim: int):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or t.dtype not in dtypes or t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name}: need a contiguous {ndim}-d CUDA tensor of {dtypes}, got "
+                         f"{t.dtype} {tuple(t.shape)} on {t.device}")
+    return t
+
+
+def _bf16s():
+    torch = _torch()
+    return (torch.bfloat16, torch.int16, torch.uint16)
+
+
+def _dtype_code(dtype) -> int:
+    torch = _torch()
+    if dtype in (torch.bfloat16, BF16):
+        return BF16
+    if dtype in (torch.float32, F32):
+        return F32
+    raise ValueError(f"partial dtype must be bfloat16 or float32, got {dtype}")
+
+
+def _workspace(nbytes: int, device):
+    torch = _torch()
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------------------
+
+def mlp_swiglu_workspace_bytes(T: int, H: int, I: int) -> int:
+    return int(lib().mlp_swiglu_workspace_bytes(T, H, I))
+
+
+def merged_proj_workspace_bytes(T: int, H: int, q_dim: int, kv_dim: int) -> int:
+    return int(lib().merged_proj_workspace_bytes(T, H, q_dim, kv_dim))
+
+
+def new_mlp_workspace(T: int, H: int, I: int, device="cuda"):
+    """A zero-filled workspace for mlp_swiglu_forward / mlp_swiglu_shard_partial."""
+    return _workspace(mlp_swiglu_workspace_bytes(T, H, I), device)
+
+
+def new_merged_workspace(T: int, H: int, q_dim: int, kv_dim: int, device="cuda"):
+    return _workspace(merged_proj_workspace_bytes(T, H, q_dim, kv_dim), device)
+
+
+def mlp_swiglu_forward(x, w_gate_up, w_down, y=None, workspace=None, stream=None):
+    """y [T, H] = W_down (silu(W_gate x) * (W_up x)); x [T, H], w_gate_up [2I, H], w_down [H, I]."""
+    torch = _torch()
+    _need(x, "x", _bf16s(), 2)
+    _need(w_gate_up, "w_gate_up", _bf16s(), 2)
+    _need(w_down, "w_down", _bf16s(), 2)
+    T, H = x.shape
+    I = w_down.shape[1]
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", _bf16s(), 2)
+    if workspace is None:
+        workspace = new_mlp_workspace(T, H, I, x.device)
+    st = lib().mlp_swiglu_forward(_ptr(x), T, H, I, _ptr(w_gate_up), _ptr(w_down), _ptr(y), y.numel(),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("mlp_swiglu_forward", st)
+    return y
+
+
+def mlp_swiglu_shard_partial(x, w_gate_up, w_down, tp, rank_first=0, rank_count=None, partial_dtype=None,
+                             partials=None, workspace=None, stream=None):
+    """Partials [rank_count, T, H] of shards rank_first.. of a tp-way intermediate split."""
+    torch = _torch()
+    _need(x, "x", _bf16s(), 2)
+    T, H = x.shape
+    I = w_down.shape[1]
+    rank_count = tp - rank_first if rank_count is None else rank_count
+    code = _dtype_code(torch.bfloat16 if partial_dtype is None else partial_dtype)
+    if partials is None:
+        partials = torch.empty((max(rank_count, 0), T, H), dtype=torch.float32 if code == F32 else torch.bfloat16,
+                               device=x.device)
+    if workspace is None:
+        workspace = new_mlp_workspace(T, H, I, x.device)
+    st = lib().mlp_swiglu_shard_partial(_ptr(x), T, H, I, _ptr(w_gate_up), _ptr(w_down), tp, rank_first,
+                                        rank_count, _ptr(partials), code, partials.numel(), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("mlp_swiglu_shard_partial", st)
+    return partials
+
+
+def shard_sum(partials, out=None, stream=None):
+    """out [T, H] bf16 = sum over the leading axis of partials [n, T, H] (fp32 accumulation)."""
+    torch = _torch()
+    n, T, H = partials.shape
+    code = _dtype_code(partials.dtype)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=partials.device)
+    st = lib().shard_sum(_ptr(partials), code, n, T, H, _ptr(out), out.numel(), _stream(stream))
+    _check("shard_sum", st)
+    return out
+
+
+def merged_proj_forward(x, w, q_dim, kv_dim, tp, logical=True, rank_major=True, out_logical=None,
+                        out_rank_major=None, workspace=None, stream=None):
+    """(logical [T, C], rank_major [T, C]) of x w^T; either may be skipped (None returned)."""
+    torch = _torch()
+    T, H = x.shape
+    C = q_dim + kv_dim
+    if logical and out_logical is None:
+        out_logical = torch.empty((T, C), dtype=torch.bfloat16, device=x.device)
+    if rank_major and out_rank_major is None:
+        out_rank_major = torch.empty((T, C), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = new_merged_workspace(T, H, q_dim, kv_dim, x.device)
+    st = lib().merged_proj_forward(_ptr(x), T, H, _ptr(w), q_dim, kv_dim, tp, _ptr(out_logical),
+                                   _ptr(out_rank_major), T * C, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("merged_proj_forward", st)
+    return out_logical, out_rank_major
+
+
+def merged_proj_reorder(rank_major, q_dim, kv_dim, tp, out=None, stream=None):
+    torch = _torch()
+    T, C = rank_major.shape
+    if out is None:
+        out = torch.empty_like(rank_major)
+    st = lib().merged_proj_reorder(_ptr(rank_major), _ptr(out), T, q_dim, kv_dim, tp, T * C, _stream(stream))
+    _check("merged_proj_reorder", st)
+    return out
+
+
+def poll_device_error(stream=None) -> int:
+    return int(lib().mse_poll_device_error(_stream(stream)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    lib().mse_set_wait_limit_ns(int(ns))
+
+
+def get_wait_limit_ns() -> int:
+    return int(lib().mse_get_wait_limit_ns())
+
+
+def set_kernel_path(path: int) -> int:
+    return int(lib().mse_set_kernel_path(int(path)))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check("mse_selftest_wait_timeout", lib().mse_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def set_phase_events(ev_begin=None, ev_mid=None, ev_end=None) -> None:
+    h = lambda e: None if e is None else e.cuda_event
+    lib().mse_set_phase_events(h(ev_begin), h(ev_mid), h(ev_end))

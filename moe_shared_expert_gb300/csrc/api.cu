@@ -1,0 +1,615 @@
+// C-ABI entry points: argument validation (before any CUDA call), device
+// check, workspace carving, tensor-map encoding and kernel dispatch.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.h"
+
+namespace mse {
+
+__device__ uint32_t g_device_error_word;
+
+namespace {
+
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_path{MSE_PATH_AUTO};
+std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
+
+struct DeviceInfo {
+    bool init = false;
+    bool supported = false;
+    int sm_count = 0;
+    uint32_t *err = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+mse_status current_device(DeviceInfo **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return MSE_ERR_UNSUPPORTED_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return MSE_ERR_CUDA;
+        }
+        d.supported = (major == 10 && minor == 3);
+        d.sm_count = sms;
+        if (d.supported) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) {
+                cudaGetLastError();
+                return MSE_ERR_CUDA;
+            }
+            d.err = static_cast<uint32_t *>(p);
+        }
+        d.init = true;
+    }
+    if (!d.supported) return MSE_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return MSE_OK;
+}
+
+mse_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MSE_OK : MSE_ERR_CUDA; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int round_up16(int64_t v) { return (int)((v + 15) / 16 * 16); }
+
+int pow2_at_least(int v) {
+    int p = 64;   // two accumulator buffers of >= 32 columns each
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// ----------------------------------------------------------------- workspace
+struct MlpWs {
+    size_t h_off = 0, slots_off = 0, cnt_gu_off = 0, cnt_dn_off = 0, total = 0;
+};
+
+constexpr int64_t kSwapAbMaxT = 256;   // token counts served by the swap-AB kernels
+
+MlpWs mlp_ws_layout(int64_t T, int64_t H, int64_t I) {
+    MlpWs w;
+    size_t off = 0;
+    w.h_off = off;
+    off = align_up(off + (size_t)T * (size_t)I * 2, 256);
+    if (T <= kSwapAbMaxT) {
+        const int bn = round_up16(T);
+        w.slots_off = off;
+        off = align_up(off + (size_t)tc::kMaxGrid * 2 * 128 * (size_t)bn * 4, 256);
+        w.cnt_gu_off = off;
+        off = align_up(off + (size_t)((I + 63) / 64) * 4, 256);
+        w.cnt_dn_off = off;
+        off = align_up(off + (size_t)((I + 63) / 64) * (size_t)((H + 127) / 128) * 4, 256);
+    }
+    w.total = off;
+    return w;
+}
+
+struct MergedWs {
+    size_t slots_off = 0, cnt_off = 0, total = 0;
+};
+
+MergedWs merged_ws_layout(int64_t T, int64_t C) {
+    MergedWs w;
+    size_t off = 0;
+    if (T <= kSwapAbMaxT) {
+        const int bn = round_up16(T);
+        w.slots_off = off;
+        off = align_up(off + (size_t)tc::kMaxGrid * 2 * 128 * (size_t)bn * 4, 256);
+        w.cnt_off = off;
+        off = align_up(off + (size_t)((C + 127) / 128) * 4, 256);
+    }
+    w.total = off;
+    return w;
+}
+
+// ----------------------------------------------------------------- tensor maps
+mse_status encoder(EncodeTiledFn *fn) {
+    std::call_once(g_encode_once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+    });
+    if (!g_encode) return MSE_ERR_CUDA;
+    *fn = g_encode;
+    return MSE_OK;
+}
+
+// Encoded descriptors are cached by their full argument list (they are plain host
+// data; the driver call costs more than a lookup).
+struct MapKey {
+    uint64_t base;
+    uint64_t dims[5];
+    uint64_t strides[4];
+    uint32_t box[5];
+    int rank;
+    bool operator==(const MapKey &o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const {
+        const unsigned char *p = reinterpret_cast<const unsigned char *>(&k);
+        uint64_t h = 1469598103934665603ull;
+        for (size_t i = 0; i < sizeof(MapKey); ++i) h = (h ^ p[i]) * 1099511628211ull;
+        return (size_t)h;
+    }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
+constexpr size_t kMapCacheMax = 4096;
+
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first, strides in bytes.
+mse_status make_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
+                    const uint32_t *box) {
+    MapKey key;
+    std::memset(&key, 0, sizeof key);
+    key.base = reinterpret_cast<uint64_t>(base);
+    key.rank = rank;
+    for (int i = 0; i < rank; ++i) { key.dims[i] = dims[i]; key.box[i] = box[i]; }
+    for (int i = 0; i < rank - 1; ++i) key.strides[i] = strides[i];
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_map_cache.find(key);
+        if (it != g_map_cache.end()) { *m = it->second; return MSE_OK; }
+    }
+    EncodeTiledFn fn;
+    mse_status st = encoder(&fn);
+    if (st != MSE_OK) return st;
+    cuuint64_t d[5], s[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+    }
+    for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), d, s, b, e,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return MSE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
+    g_map_cache.emplace(key, *m);
+    return MSE_OK;
+}
+
+// [rows x cols] row-major bf16 (row pitch ld elements), box 64 cols x box_rows rows.
+mse_status map_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+    const uint64_t strides[1] = {(uint64_t)ld * 2};
+    const uint32_t box[2] = {64u, (uint32_t)box_rows};
+    return make_map(m, base, 2, dims, strides, box);
+}
+
+// W_gate_up [2I x H] viewed as (k, j, half): one box = `rows` gate rows followed by
+// the `rows` up rows of the same j.  rows = 16 builds the swap-AB tile from four
+// boxes (each 32-row quarter pairs gate and up rows of 16 consecutive j); rows =
+// 128 gives the 256-row operand of the prefill kernel.
+mse_status map_gate_up_halves(CUtensorMap *m, const void *w, int64_t H, int64_t I, int rows) {
+    const uint64_t dims[3] = {(uint64_t)H, (uint64_t)I, 2};
+    const uint64_t strides[2] = {(uint64_t)H * 2, (uint64_t)I * H * 2};
+    const uint32_t box[3] = {64, (uint32_t)rows, 2};
+    return make_map(m, w, 3, dims, strides, box);
+}
+
+// ----------------------------------------------------------------- launch helpers
+tc::SwapAbParams swapab_base(int64_t T, int total_units) {
+    tc::SwapAbParams p;
+    std::memset(&p, 0, sizeof p);
+    p.bn = round_up16(T);
+    p.stages = tc::swapab_stages_for(p.bn);
+    p.tmem_cols = pow2_at_least(2 * p.bn);
+    p.T = (int)T;
+    p.total_units = total_units;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    return p;
+}
+
+int swapab_grid(const DeviceInfo &d, int total_units) {
+    int g = d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid;
+    return g < total_units ? g : total_units;
+}
+
+tc::StdParams std_base(int64_t T) {
+    tc::StdParams p;
+    std::memset(&p, 0, sizeof p);
+    p.stages = tc::std_stages();
+    p.T = (int)T;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    return p;
+}
+
+int std_grid(const DeviceInfo &d, int64_t n_tiles) {
+    int64_t g = d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid;
+    return (int)(g < n_tiles ? g : n_tiles);
+}
+
+// gate_up + SiluAndMul over intermediate columns [j_begin, j_begin + width) into h [T x I].
+mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t H, int64_t I,
+                      const uint16_t *w_gate_up, int64_t j_begin, int64_t width, uint16_t *h, char *ws,
+                      const MlpWs &L, cudaStream_t s) {
+    CUtensorMap ta, tb;
+    mse_status st;
+    if (T <= kSwapAbMaxT) {
+        const int n_mtiles = (int)(width / 64);
+        const int kbp = (int)(H / 64);
+        tc::SwapAbParams p = swapab_base(T, n_mtiles * kbp);
+        if ((st = map_gate_up_halves(&ta, w_gate_up, H, I, 16)) != MSE_OK) return st;
+        if ((st = map_2d(&tb, x, T, H, H, p.bn)) != MSE_OK) return st;
+        p.n_mtiles = n_mtiles;
+        p.n_groups = 1;
+        p.kb_per_tile = kbp;
+        p.kb_first = 0;
+        p.kb_group_stride = 0;
+        p.a_row_base = (int)j_begin;
+        p.m_valid = 2 * width;
+        p.out = h;
+        p.ldo = I;
+        p.slots = reinterpret_cast<float *>(ws + L.slots_off);
+        p.counters = reinterpret_cast<int *>(ws + L.cnt_gu_off);
+        p.err = d.err;
+        return from_cuda(tc::launch_swapab(tc::EPI_SWIGLU, ta, tb, p, swapab_grid(d, p.total_units), true, s));
+    }
+    tc::StdParams p = std_base(T);
+    if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
+    if ((st = map_gate_up_halves(&tb, w_gate_up, H, I, 128)) != MSE_OK) return st;
+    p.n_mtiles = (int)((T + 127) / 128);
+    p.n_ntiles = (int)((width + 127) / 128);
+    p.n_groups = 1;
+    p.kb_per_tile = (int)(H / 64);
+    p.n_valid = j_begin + width;
+    p.n_base = (int)j_begin;
+    p.out = h;
+    p.ldo = I;
+    p.err = d.err;
+    const int64_t n_tiles = (int64_t)p.n_mtiles * p.n_ntiles;
+    return from_cuda(tc::launch_std(tc::EPI_SWIGLU, ta, tb, p, std_grid(d, n_tiles), true, s));
+}
+
+// out[g] = h[:, slice g] . W_down[:, slice g]^T for groups g, slices of `s_width`
+// intermediate columns starting at column kcol0 + g * s_width.
+mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H, int64_t I, const uint16_t *w_down,
+                   int64_t kcol0, int64_t s_width, int groups, void *out, int epi, char *ws, const MlpWs &L,
+                   cudaStream_t s) {
+    CUtensorMap ta, tb;
+    mse_status st;
+    if (T <= kSwapAbMaxT) {
+        const int n_mtiles = (int)((H + 127) / 128);
+        const int kbp = (int)(s_width / 64);
+        tc::SwapAbParams p = swapab_base(T, groups * n_mtiles * kbp);
+        if ((st = map_2d(&ta, w_down, H, I, I, 128)) != MSE_OK) return st;
+        if ((st = map_2d(&tb, h, T, I, I, p.bn)) != MSE_OK) return st;
+        p.n_mtiles = n_mtiles;
+        p.n_groups = groups;
+        p.kb_per_tile = kbp;
+        p.kb_first = (int)(kcol0 / 64);
+        p.kb_group_stride = kbp;
+        p.m_valid = H;
+        p.out = out;
+        p.ldo = H;
+        p.o_group_stride = T * H;
+        p.slots = reinterpret_cast<float *>(ws + L.slots_off);
+        p.counters = reinterpret_cast<int *>(ws + L.cnt_dn_off);
+        p.err = d.err;
+        return from_cuda(tc::launch_swapab(epi, ta, tb, p, swapab_grid(d, p.total_units), true, s));
+    }
+    tc::StdParams p = std_base(T);
+    if ((st = map_2d(&ta, h, T, I, I, 128)) != MSE_OK) return st;
+    if ((st = map_2d(&tb, w_down, H, I, I, 256)) != MSE_OK) return st;
+    p.n_mtiles = (int)((T + 127) / 128);
+    p.n_ntiles = (int)((H + 255) / 256);
+    p.n_groups = groups;
+    p.kb_per_tile = (int)(s_width / 64);
+    p.kb_first = (int)(kcol0 / 64);
+    p.kb_group_stride = p.kb_per_tile;
+    p.n_valid = H;
+    p.out = out;
+    p.ldo = H;
+    p.o_group_stride = T * H;
+    p.err = d.err;
+    const int64_t n_tiles = (int64_t)groups * p.n_mtiles * p.n_ntiles;
+    return from_cuda(tc::launch_std(epi, ta, tb, p, std_grid(d, n_tiles), true, s));
+}
+
+// ----------------------------------------------------------------- path choice
+enum Path { PATH_GENERIC, PATH_TC };
+
+mse_status choose(bool tc_ok, Path *out) {
+    const int pol = g_path.load();
+    if (pol == MSE_PATH_GENERIC) { *out = PATH_GENERIC; return MSE_OK; }
+    if (pol == MSE_PATH_TENSORCORE) {
+        if (!tc_ok) return MSE_ERR_UNSUPPORTED_SHAPE;
+        *out = PATH_TC;
+        return MSE_OK;
+    }
+    *out = tc_ok ? PATH_TC : PATH_GENERIC;
+    return MSE_OK;
+}
+
+bool mlp_tc_ok(const void *x, int64_t H, int64_t I, int64_t slice, const void *wgu, const void *wd, const void *out,
+               const void *ws) {
+    return H % 64 == 0 && I % 64 == 0 && slice % 64 == 0 && aligned16(x) && aligned16(wgu) && aligned16(wd) &&
+           aligned16(out) && aligned16(ws) && H <= (int64_t)1 << 20 && I <= (int64_t)1 << 20;
+}
+
+void record(std::atomic<void *> &ev, cudaStream_t s) {
+    void *e = ev.load();
+    if (e) cudaEventRecord(static_cast<cudaEvent_t>(e), s);
+}
+
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+}  // namespace mse
+
+using namespace mse;
+
+// =============================================================================
+// exported C ABI
+// =============================================================================
+extern "C" {
+
+size_t mlp_swiglu_workspace_bytes(int64_t T, int64_t H, int64_t I) {
+    if (T <= 0 || H <= 0 || I <= 0) return 0;
+    return mlp_ws_layout(T, H, I).total;
+}
+
+size_t merged_proj_workspace_bytes(int64_t T, int64_t H, int64_t q_dim, int64_t kv_dim) {
+    if (T <= 0 || H <= 0 || q_dim < 0 || kv_dim < 0 || q_dim + kv_dim <= 0) return 0;
+    const size_t n = merged_ws_layout(T, q_dim + kv_dim).total;
+    return n == 0 ? 256 : n;
+}
+
+mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, const mse_bf16 *w_gate_up,
+                              const mse_bf16 *w_down, mse_bf16 *y, int64_t y_capacity, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    if (!x || !w_gate_up || !w_down || !y || T <= 0 || H <= 0 || I <= 0) return MSE_ERR_INVALID_ARG;
+    if (y_capacity < T * H) return MSE_ERR_GEOMETRY;
+    const MlpWs L = mlp_ws_layout(T, H, I);
+    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MSE_ERR_WORKSPACE;
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    Path path;
+    if ((st = choose(mlp_tc_ok(x, H, I, I, w_gate_up, w_down, y, workspace), &path)) != MSE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h_off);
+
+    record(g_ev_begin, s);
+    if (path == PATH_GENERIC) {
+        SimtGemmArgs a = {};
+        a.A = x; a.lda = H; a.B = w_gate_up; a.B2 = w_gate_up + I * H; a.ldb = H;
+        a.M = T; a.N = I; a.K = H; a.groups = 1; a.out = h; a.ldo = I; a.mode = SIMT_SWIGLU;
+        if ((st = from_cuda(launch_simt_gemm(a, s))) != MSE_OK) return st;
+        record(g_ev_mid, s);
+        SimtGemmArgs b = {};
+        b.A = h; b.lda = I; b.B = w_down; b.ldb = I;
+        b.M = T; b.N = H; b.K = I; b.groups = 1; b.out = y; b.ldo = H; b.mode = SIMT_BF16;
+        if ((st = from_cuda(launch_simt_gemm(b, s))) != MSE_OK) return st;
+    } else {
+        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, 0, I, h, ws, L, s)) != MSE_OK) return st;
+        record(g_ev_mid, s);
+        if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s)) != MSE_OK) return st;
+    }
+    record(g_ev_end, s);
+    return MSE_OK;
+}
+
+mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, const mse_bf16 *w_gate_up,
+                                    const mse_bf16 *w_down, int tp, int rank_first, int rank_count, void *partials,
+                                    mse_dtype partial_dtype, int64_t partials_capacity, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    if (!x || !w_gate_up || !w_down || !partials || T <= 0 || H <= 0 || I <= 0 || tp <= 0)
+        return MSE_ERR_INVALID_ARG;
+    if (partial_dtype != MSE_BF16 && partial_dtype != MSE_F32) return MSE_ERR_INVALID_ARG;
+    if (I % tp != 0 || H % tp != 0) return MSE_ERR_NOT_DIVISIBLE;
+    if (rank_first < 0 || rank_count < 1 || (int64_t)rank_first + rank_count > tp) return MSE_ERR_GEOMETRY;
+    if (partials_capacity < (int64_t)rank_count * T * H) return MSE_ERR_GEOMETRY;
+    const MlpWs L = mlp_ws_layout(T, H, I);
+    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MSE_ERR_WORKSPACE;
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    const int64_t sw = I / tp;
+    Path path;
+    if ((st = choose(mlp_tc_ok(x, H, I, sw, w_gate_up, w_down, partials, workspace), &path)) != MSE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h_off);
+    const int64_t j0 = (int64_t)rank_first * sw, width = (int64_t)rank_count * sw;
+
+    if (path == PATH_GENERIC) {
+        // the shards' gate rows [j0, j0 + width) and up rows I + [j0, j0 + width)
+        SimtGemmArgs a = {};
+        a.A = x; a.lda = H; a.B = w_gate_up + j0 * H; a.B2 = w_gate_up + (I + j0) * H; a.ldb = H;
+        a.M = T; a.N = width; a.K = H; a.groups = 1; a.out = h + j0; a.ldo = I; a.mode = SIMT_SWIGLU;
+        if ((st = from_cuda(launch_simt_gemm(a, s))) != MSE_OK) return st;
+        // per shard: its h columns times its W_down columns
+        SimtGemmArgs b = {};
+        b.A = h + j0; b.lda = I; b.a_gstride = sw;
+        b.B = w_down + j0; b.ldb = I; b.b_gstride = sw;
+        b.M = T; b.N = H; b.K = sw; b.groups = rank_count;
+        b.out = partials; b.ldo = H; b.o_gstride = T * H;
+        b.mode = partial_dtype == MSE_F32 ? SIMT_F32 : SIMT_BF16;
+        return from_cuda(launch_simt_gemm(b, s));
+    }
+    if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s)) != MSE_OK) return st;
+    return tc_down(*d, h, T, H, I, w_down, j0, sw, rank_count, partials,
+                   partial_dtype == MSE_F32 ? tc::EPI_F32 : tc::EPI_BF16, ws, L, s);
+}
+
+mse_status shard_sum(const void *partials, mse_dtype partial_dtype, int n_parts, int64_t T, int64_t H,
+                     mse_bf16 *out, int64_t out_capacity, void *stream) {
+    if (!partials || !out || n_parts <= 0 || T <= 0 || H <= 0) return MSE_ERR_INVALID_ARG;
+    if (partial_dtype != MSE_BF16 && partial_dtype != MSE_F32) return MSE_ERR_INVALID_ARG;
+    if (T % n_parts != 0) return MSE_ERR_NOT_DIVISIBLE;
+    if (out_capacity < T * H) return MSE_ERR_GEOMETRY;
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    return from_cuda(launch_shard_sum(partials, partial_dtype == MSE_F32, n_parts, T * H, out, d->sm_count,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const mse_bf16 *w, int64_t q_dim,
+                               int64_t kv_dim, int tp, mse_bf16 *out_logical, mse_bf16 *out_rank_major,
+                               int64_t out_capacity, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!x || !w || (!out_logical && !out_rank_major) || T <= 0 || H <= 0 || q_dim <= 0 || kv_dim <= 0 || tp <= 0)
+        return MSE_ERR_INVALID_ARG;
+    if (q_dim % tp != 0 || kv_dim % tp != 0) return MSE_ERR_NOT_DIVISIBLE;
+    const int64_t C = q_dim + kv_dim;
+    if (out_capacity < T * C) return MSE_ERR_GEOMETRY;
+    const MergedWs L = merged_ws_layout(T, C);
+    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MSE_ERR_WORKSPACE;
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    const bool tc_ok = H % 64 == 0 && aligned16(x) && aligned16(w) && aligned16(workspace);
+    Path path;
+    if ((st = choose(tc_ok, &path)) != MSE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (path == PATH_GENERIC) {
+        SimtGemmArgs a = {};
+        a.A = x; a.lda = H; a.B = w; a.ldb = H; a.M = T; a.N = C; a.K = H; a.groups = 1;
+        a.out = out_logical; a.ldo = C; a.out_rm = out_rank_major; a.q_dim = q_dim; a.kv_dim = kv_dim; a.tp = tp;
+        a.mode = SIMT_MERGED;
+        return from_cuda(launch_simt_gemm(a, s));
+    }
+    CUtensorMap ta, tb;
+    char *ws = static_cast<char *>(workspace);
+    if (T <= kSwapAbMaxT) {
+        const int n_mtiles = (int)((C + 127) / 128), kbp = (int)(H / 64);
+        tc::SwapAbParams p = swapab_base(T, n_mtiles * kbp);
+        if ((st = map_2d(&ta, w, C, H, H, 128)) != MSE_OK) return st;
+        if ((st = map_2d(&tb, x, T, H, H, p.bn)) != MSE_OK) return st;
+        p.n_mtiles = n_mtiles;
+        p.n_groups = 1;
+        p.kb_per_tile = kbp;
+        p.m_valid = C;
+        p.out = out_logical;
+        p.ldo = C;
+        p.out_rm = out_rank_major;
+        p.q_dim = q_dim; p.kv_dim = kv_dim; p.tp = tp;
+        p.slots = reinterpret_cast<float *>(ws + L.slots_off);
+        p.counters = reinterpret_cast<int *>(ws + L.cnt_off);
+        p.err = d->err;
+        return from_cuda(tc::launch_swapab(tc::EPI_MERGED, ta, tb, p, swapab_grid(*d, p.total_units), true, s));
+    }
+    tc::StdParams p = std_base(T);
+    if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
+    if ((st = map_2d(&tb, w, C, H, H, 256)) != MSE_OK) return st;
+    p.n_mtiles = (int)((T + 127) / 128);
+    p.n_ntiles = (int)((C + 255) / 256);
+    p.n_groups = 1;
+    p.kb_per_tile = (int)(H / 64);
+    p.n_valid = C;
+    p.out = out_logical;
+    p.ldo = C;
+    p.out_rm = out_rank_major;
+    p.q_dim = q_dim; p.kv_dim = kv_dim; p.tp = tp;
+    p.err = d->err;
+    return from_cuda(tc::launch_std(tc::EPI_MERGED, ta, tb, p, std_grid(*d, (int64_t)p.n_mtiles * p.n_ntiles), true, s));
+}
+
+mse_status merged_proj_reorder(const mse_bf16 *rank_major, mse_bf16 *logical, int64_t T, int64_t q_dim,
+                               int64_t kv_dim, int tp, int64_t capacity, void *stream) {
+    if (!rank_major || !logical || T <= 0 || q_dim <= 0 || kv_dim <= 0 || tp <= 0) return MSE_ERR_INVALID_ARG;
+    if (q_dim % tp != 0 || kv_dim % tp != 0) return MSE_ERR_NOT_DIVISIBLE;
+    const int64_t C = q_dim + kv_dim;
+    if (capacity < T * C) return MSE_ERR_GEOMETRY;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(rank_major), b = reinterpret_cast<uintptr_t>(logical);
+    const uintptr_t n = (uintptr_t)(T * C * 2);
+    if (a < b + n && b < a + n) return MSE_ERR_INVALID_ARG;   // buffers overlap
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    return from_cuda(launch_reorder(rank_major, logical, T, q_dim, kv_dim, tp, static_cast<cudaStream_t>(stream)));
+}
+
+mse_status mse_poll_device_error(void *stream) {
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MSE_ERR_CUDA;
+    }
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, d->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MSE_ERR_CUDA;
+    if (word != 0) {
+        const uint32_t zero = 0;
+        if (cudaMemcpy(d->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return MSE_ERR_CUDA;
+    }
+    return (word & DEV_ERR_TIMEOUT) ? MSE_ERR_TIMEOUT : MSE_OK;
+}
+
+void mse_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
+uint64_t mse_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
+
+int mse_set_kernel_path(int path) {
+    if (path < MSE_PATH_AUTO || path > MSE_PATH_TENSORCORE) return g_path.load();
+    return g_path.exchange(path);
+}
+
+void mse_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end) {
+    const bool all = ev_begin && ev_mid && ev_end;
+    g_ev_begin.store(all ? ev_begin : nullptr);
+    g_ev_mid.store(all ? ev_mid : nullptr);
+    g_ev_end.store(all ? ev_end : nullptr);
+}
+
+mse_status mse_selftest_wait_timeout(uint64_t limit_ns, void *stream) {
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    return from_cuda(launch_wait_selftest(limit_ns, d->err, static_cast<cudaStream_t>(stream)));
+}
+
+const char *mse_status_string(mse_status s) {
+    switch (s) {
+        case MSE_OK: return "MSE_OK";
+        case MSE_ERR_INVALID_ARG: return "MSE_ERR_INVALID_ARG";
+        case MSE_ERR_NOT_DIVISIBLE: return "MSE_ERR_NOT_DIVISIBLE";
+        case MSE_ERR_GEOMETRY: return "MSE_ERR_GEOMETRY";
+        case MSE_ERR_WORKSPACE: return "MSE_ERR_WORKSPACE";
+        case MSE_ERR_UNSUPPORTED_DEVICE: return "MSE_ERR_UNSUPPORTED_DEVICE";
+        case MSE_ERR_CUDA: return "MSE_ERR_CUDA";
+        case MSE_ERR_TIMEOUT: return "MSE_ERR_TIMEOUT";
+        case MSE_ERR_UNSUPPORTED_SHAPE: return "MSE_ERR_UNSUPPORTED_SHAPE";
+    }
+    return "MSE_ERR_UNKNOWN";
+}
+
+const char *mse_version(void) { return "mse 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,671 @@
+// Tensor-core kernels for sm_103a: TMA-fed, mbarrier-pipelined tcgen05 MMA with
+// fp32 accumulators in tensor memory, warp-specialised:
+//   warp 0      TMA producer (one elected lane)
+//   warp 1      TMEM allocator + MMA issuer (one elected lane)
+//   warps 2..5  epilogue (tcgen05.ld of the warp's 32-lane quarter)
+//
+// swapab_kernel: decode-sized token counts.  The weight rows fill the 128-row
+//   MMA M side and the tokens form N (<= 256), so each CTA streams weight tiles
+//   through a deep TMA ring.  Work is split stream-K over (group, m-tile,
+//   k-block) units so that every SM streams the same number of weight bytes;
+//   a tile cut between CTAs is finished by whichever CTA arrives last on the
+//   tile's counter (fp32 partial tiles in the workspace, summed in a fixed
+//   order, so results do not depend on arrival order).  No CTA ever waits on
+//   another one.
+// std_kernel: prefill-sized token counts.  Persistent CTAs walk 128-token x
+//   256-column tiles over the full reduction with two TMEM accumulators, so the
+//   epilogue of one tile overlaps the MMA of the next.
+#include <atomic>
+
+#include "common.cuh"
+#include "tc.h"
+
+namespace mse {
+namespace tc {
+namespace {
+
+constexpr uint32_t kATileBytes = 128 * 64 * 2;   // 128 rows x 64 bf16
+constexpr uint32_t kFull = 0xffffffffu;
+
+struct Ctrl {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int fin_flag;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(const uint64_t *b) { return smem_u32(b); }
+
+__device__ __forceinline__ int64_t logical_to_gathered(int64_t c, int64_t q_dim, int64_t kv_dim, int tp) {
+    const int64_t qs = q_dim / tp, ks = kv_dim / tp, w = qs + ks;
+    if (c < q_dim) return (c / qs) * w + (c % qs);
+    const int64_t c2 = c - q_dim;
+    return (c2 / ks) * w + qs + (c2 % ks);
+}
+
+__device__ __forceinline__ void load_tmem_chunk(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------------------
+// swap-AB stream-K kernel
+// ---------------------------------------------------------------------------
+
+struct StreamK {
+    int64_t U, G;
+    __device__ __forceinline__ int64_t begin(int64_t c) const { return c * U / G; }
+    __device__ __forceinline__ int64_t owner(int64_t u) const { return ((u + 1) * G - 1) / U; }
+};
+
+// Epilogue of one 16-token chunk of a swap-AB tile.  Thread `lane` of epilogue
+// warp quarter `q` holds accumulator row r = 32q + lane for tokens c*16 .. c*16+15.
+template <int EPI>
+__device__ __forceinline__ void swapab_epilogue_chunk(const SwapAbParams &p, int group, int m, int q, int lane,
+                                                      int c, const float (&v)[16]) {
+    if constexpr (EPI == EPI_SWIGLU) {
+        // Rows of quarter q: lanes 0-15 hold gate rows j, lanes 16-31 the up rows of the
+        // same j (j = j0 + 16q + (lane & 15)).  Lane pairs (l, l+16) swap half of their
+        // tokens so that each computes silu(g) * u for 8 tokens.
+        float send[8], recv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) send[i] = (lane < 16) ? v[8 + i] : v[i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) recv[i] = __shfl_xor_sync(kFull, send[i], 16);
+        const int64_t j = (int64_t)p.a_row_base + (int64_t)m * 64 + q * 16 + (lane & 15);
+        const int t0 = c * 16 + ((lane < 16) ? 0 : 8);
+        uint16_t *h = static_cast<uint16_t *>(p.out);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float g = (lane < 16) ? v[i] : recv[i];
+            const float u = (lane < 16) ? recv[i] : v[8 + i];
+            const int t = t0 + i;
+            if (t < p.T) h[(int64_t)t * p.ldo + j] = f32_to_bf16_bits(silu_f32(g) * u);
+        }
+    } else {
+        const int64_t n = (int64_t)m * 128 + q * 32 + lane;
+        if (n >= p.m_valid) return;
+        if constexpr (EPI == EPI_F32) {
+            float *o = static_cast<float *>(p.out) + group * p.o_group_stride;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = c * 16 + i;
+                if (t < p.T) o[(int64_t)t * p.ldo + n] = v[i];
+            }
+        } else if constexpr (EPI == EPI_BF16) {
+            uint16_t *o = static_cast<uint16_t *>(p.out) + group * p.o_group_stride;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = c * 16 + i;
+                if (t < p.T) o[(int64_t)t * p.ldo + n] = f32_to_bf16_bits(v[i]);
+            }
+        } else {  // EPI_MERGED
+            uint16_t *lo = static_cast<uint16_t *>(p.out);
+            const int64_t gcol = logical_to_gathered(n, p.q_dim, p.kv_dim, p.tp);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = c * 16 + i;
+                if (t < p.T) {
+                    const uint16_t b = f32_to_bf16_bits(v[i]);
+                    if (lo) lo[(int64_t)t * p.ldo + n] = b;
+                    if (p.out_rm) p.out_rm[(int64_t)t * p.ldo + gcol] = b;
+                }
+            }
+        }
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kSwapAbThreads, 1)
+    swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const SwapAbParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const int S = p.stages, bn = p.bn;
+    const uint32_t b_tile_bytes = (uint32_t)bn * 128u;
+    const uint32_t sA = base;
+    const uint32_t sB = base + (uint32_t)S * kATileBytes;
+    Ctrl *ctl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + (uint32_t)S * (kATileBytes + b_tile_bytes));
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const StreamK sk{p.total_units, gridDim.x};
+    const int64_t ub = sk.begin(blockIdx.x), ue = sk.begin(blockIdx.x + 1);
+    const int kbp = p.kb_per_tile;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_addr(&ctl->full[s]), 1);
+            mbar_init(bar_addr(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_addr(&ctl->tfull[b]), 1);
+            mbar_init(bar_addr(&ctl->tempty[b]), 128);
+        }
+        mbar_init(bar_addr(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), (uint32_t)p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile int *abort_flag = &ctl->abort_flag;
+    pdl_launch_dependents();
+
+    int64_t issued = 0;   // producer: k-blocks whose loads were issued
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            const int64_t n_items = ue - ub;
+            auto kglob = [&](int64_t u) {
+                const int64_t tile = u / kbp;
+                const int group = (int)(tile / p.n_mtiles);
+                return p.kb_first + group * p.kb_group_stride + (int)(u % kbp);
+            };
+            auto load_a = [&](int64_t u, int stage) {
+                const int64_t tile = u / kbp;
+                const int m = (int)(tile % p.n_mtiles);
+                const int k = kglob(u) * 64;
+                const uint32_t fb = bar_addr(&ctl->full[stage]);
+                if constexpr (EPI == EPI_SWIGLU) {
+                    // four 32-row quarters: 16 gate rows then the 16 up rows of the same j
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq)
+                        tma_load_3d(sA + stage * kATileBytes + qq * 4096u, &tmA, fb, k, p.a_row_base + m * 64 + qq * 16,
+                                    0, pol_w);
+                } else
+                    tma_load_2d(sA + stage * kATileBytes, &tmA, fb, k, m * 128, pol_w);
+            };
+            auto load_b = [&](int64_t u, int stage) {
+                tma_load_2d(sB + stage * b_tile_bytes, &tmB, bar_addr(&ctl->full[stage]), kglob(u) * 64, 0, pol_x);
+            };
+            // Prologue: weight tiles do not depend on the previous kernel, so they
+            // are requested before waiting for it; token tiles follow the wait.
+            const int64_t pro = n_items < S ? n_items : S;
+            for (int64_t i = 0; i < pro; ++i) {
+                mbar_arrive_expect_tx(bar_addr(&ctl->full[i]), kATileBytes + b_tile_bytes);
+                load_a(ub + i, (int)i);
+            }
+            pdl_wait();
+            for (int64_t i = 0; i < pro; ++i) load_b(ub + i, (int)i);
+            issued = pro;
+            int stage = (int)(pro % S);
+            uint32_t phase = (pro == S) ? 1u : 0u;
+            for (int64_t i = pro; i < n_items; ++i) {
+                if (!mbar_wait_bounded(bar_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns, p.err))
+                    break;
+                mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), kATileBytes + b_tile_bytes);
+                load_a(ub + i, stage);
+                load_b(ub + i, stage);
+                ++issued;
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)bn);
+            int stage = 0;
+            uint32_t phase = 0;
+            int seg = 0;
+            bool ok = true;
+            for (int64_t u = ub; u < ue && ok; ++seg) {
+                const int64_t tile = u / kbp;
+                const int kb0 = (int)(u % kbp);
+                const int64_t rem = ue - u;
+                const int kb1 = (int)((kbp - kb0) < rem ? kbp : kb0 + rem);
+                const int buf = seg & 1;
+                const uint32_t use = (uint32_t)(seg >> 1);
+                if (!mbar_wait_bounded(bar_addr(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, p.wait_limit_ns,
+                                       p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(buf * (p.tmem_cols / 2));
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait_bounded(bar_addr(&ctl->full[stage]), phase, abort_flag, p.wait_limit_ns, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_sw128(sA + stage * kATileBytes);
+                    const uint64_t bd = smem_desc_sw128(sB + stage * b_tile_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                    (kb > kb0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar_addr(&ctl->empty[stage]));
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(bar_addr(&ctl->tfull[buf]));
+                u = tile * kbp + kb1;
+            }
+        }
+    } else {
+        // epilogue warps 2..5
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        pdl_wait();
+        int seg = 0;
+        for (int64_t u = ub; u < ue; ++seg) {
+            const int64_t tile = u / kbp;
+            const int kb0 = (int)(u % kbp);
+            const int64_t rem = ue - u;
+            const int kb1 = (int)((kbp - kb0) < rem ? kbp : kb0 + rem);
+            const int buf = seg & 1;
+            const uint32_t use = (uint32_t)(seg >> 1);
+            const int group = (int)(tile / p.n_mtiles);
+            const int m = (int)(tile % p.n_mtiles);
+            u = tile * kbp + kb1;
+            const bool got = mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
+            if (!named_barrier_and(1, 128, got)) break;   // all epilogue warps take the same branch
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + (uint32_t)(buf * (p.tmem_cols / 2)) + lane_off;
+            const int nchunks = bn / 16;
+            if (kb0 == 0 && kb1 == kbp) {
+                for (int c = 0; c < nchunks; ++c) {
+                    float v[16];
+                    load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
+                    swapab_epilogue_chunk<EPI>(p, group, m, q, lane, c, v);
+                }
+                tc_fence_before();
+                mbar_arrive(bar_addr(&ctl->tempty[buf]));
+                continue;
+            }
+            // Tile shared with other CTAs: park the fp32 partial in this CTA's slot.
+            const int which = (sk.begin(blockIdx.x) / kbp == tile) ? 0 : 1;
+            float *slot = p.slots + ((size_t)blockIdx.x * 2 + which) * (size_t)(128 * bn);
+            for (int c = 0; c < nchunks; ++c) {
+                float v[16];
+                load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
+                float4 *dst = reinterpret_cast<float4 *>(slot + ((size_t)c * 128 + row) * 16);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(&ctl->tempty[buf]));
+            __threadfence();
+            named_barrier_sync(1, 128);
+            const int64_t c_first = sk.owner(tile * kbp), c_last = sk.owner(tile * kbp + kbp - 1);
+            if (threadIdx.x == 64) {
+                const int prev = atomicAdd(p.counters + tile, 1);
+                ctl->fin_flag = (prev == (int)(c_last - c_first)) ? 1 : 0;
+            }
+            named_barrier_sync(1, 128);
+            if (ctl->fin_flag) {
+                __threadfence();
+                for (int c = 0; c < nchunks; ++c) {
+                    float v[16] = {};
+                    for (int64_t cc = c_first; cc <= c_last; ++cc) {
+                        const int w = (sk.begin(cc) / kbp == tile) ? 0 : 1;
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.slots + ((size_t)cc * 2 + w) * (size_t)(128 * bn) + ((size_t)c * 128 + row) * 16);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 a = __ldcg(src + i);
+                            v[4 * i] += a.x; v[4 * i + 1] += a.y; v[4 * i + 2] += a.z; v[4 * i + 3] += a.w;
+                        }
+                    }
+                    swapab_epilogue_chunk<EPI>(p, group, m, q, lane, c, v);
+                }
+                if (threadIdx.x == 64) p.counters[tile] = 0;
+            }
+            named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
+        }
+    }
+
+    // ---- teardown: drain in-flight copies and MMAs, then free tensor memory ----
+    if (warp == 0 && lane == 0) {
+        const int64_t first = issued > S ? issued - S : 0;
+        for (int64_t i = first; i < issued; ++i) {
+            const int st = (int)(i % S);
+            const uint32_t par = (uint32_t)((i / S) & 1);
+            (void)mbar_wait_drain(bar_addr(&ctl->full[st]), par, p.wait_limit_ns);
+        }
+    }
+    if (warp == 1 && lane == 0) {
+        tc_commit(bar_addr(&ctl->drain));
+        (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, p.wait_limit_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+}
+
+// ---------------------------------------------------------------------------
+// persistent standard-orientation kernel
+// ---------------------------------------------------------------------------
+constexpr uint32_t kStdBTileBytes = 256 * 64 * 2;   // 256 rows x 64 bf16
+constexpr int kStdBandM = 16;                       // m-tiles per raster band
+
+struct StdTile { int group, m, n; };
+
+__device__ __forceinline__ StdTile std_tile(const StdParams &p, int64_t id) {
+    const int64_t per_group = (int64_t)p.n_mtiles * p.n_ntiles;
+    StdTile t;
+    t.group = (int)(id / per_group);
+    const int64_t r = id % per_group;
+    const int64_t per_band = (int64_t)kStdBandM * p.n_ntiles;
+    const int band = (int)(r / per_band);
+    const int first_m = band * kStdBandM;
+    const int band_m = min(kStdBandM, p.n_mtiles - first_m);
+    const int64_t in_band = r % per_band;
+    t.m = first_m + (int)(in_band % band_m);
+    t.n = (int)(in_band / band_m);
+    return t;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kStdThreads, 1)
+    std_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const StdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const int S = p.stages;
+    const uint32_t sA = base;
+    const uint32_t sB = base + (uint32_t)S * kATileBytes;
+    Ctrl *ctl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + (uint32_t)S * (kATileBytes + kStdBTileBytes));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t n_tiles = (int64_t)p.n_groups * p.n_mtiles * p.n_ntiles;
+    const int kbp = p.kb_per_tile;
+    constexpr uint32_t kTmemCols = 512;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_addr(&ctl->full[s]), 1);
+            mbar_init(bar_addr(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_addr(&ctl->tfull[b]), 1);
+            mbar_init(bar_addr(&ctl->tempty[b]), 128);
+        }
+        mbar_init(bar_addr(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile int *abort_flag = &ctl->abort_flag;
+    pdl_launch_dependents();
+
+    int64_t issued = 0;
+    if (warp == 0) {
+        if (lane == 0) {
+            pdl_wait();
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int64_t id = blockIdx.x; id < n_tiles && ok; id += gridDim.x) {
+                const StdTile t = std_tile(p, id);
+                for (int kb = 0; kb < kbp; ++kb) {
+                    if (!mbar_wait_bounded(bar_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns,
+                                           p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_addr(&ctl->full[stage]);
+                    mbar_arrive_expect_tx(fb, kATileBytes + kStdBTileBytes);
+                    const int k = (p.kb_first + t.group * p.kb_group_stride + kb) * 64;
+                    tma_load_2d_nohint(sA + stage * kATileBytes, &tmA, fb, k, t.m * 128);
+                    if constexpr (EPI == EPI_SWIGLU)
+                        tma_load_3d_nohint(sB + stage * kStdBTileBytes, &tmB, fb, k, p.n_base + t.n * 128, 0);
+                    else
+                        tma_load_2d_nohint(sB + stage * kStdBTileBytes, &tmB, fb, k, t.n * 256);
+                    ++issued;
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, 256);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int64_t id = blockIdx.x; id < n_tiles && ok; id += gridDim.x, ++it) {
+                const int buf = it & 1;
+                const uint32_t use = (uint32_t)(it >> 1);
+                if (!mbar_wait_bounded(bar_addr(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, p.wait_limit_ns,
+                                       p.err))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(buf * 256);
+                for (int kb = 0; kb < kbp; ++kb) {
+                    if (!mbar_wait_bounded(bar_addr(&ctl->full[stage]), phase, abort_flag, p.wait_limit_ns, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_sw128(sA + stage * kATileBytes);
+                    const uint64_t bd = smem_desc_sw128(sB + stage * kStdBTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar_addr(&ctl->empty[stage]));
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(bar_addr(&ctl->tfull[buf]));
+            }
+        }
+    } else {
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        pdl_wait();
+        int it = 0;
+        for (int64_t id = blockIdx.x; id < n_tiles; id += gridDim.x, ++it) {
+            const StdTile t = std_tile(p, id);
+            const int buf = it & 1;
+            const uint32_t use = (uint32_t)(it >> 1);
+            const bool got = mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
+            if (!named_barrier_and(1, 128, got)) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + (uint32_t)(buf * 256) + lane_off;
+            const int64_t tok = (int64_t)t.m * 128 + row;
+            const bool tok_ok = tok < p.T;
+            if constexpr (EPI == EPI_SWIGLU) {
+                uint16_t *h = static_cast<uint16_t *>(p.out);
+                const int64_t j0 = (int64_t)p.n_base + (int64_t)t.n * 128;
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    float g[16], u[16];
+                    load_tmem_chunk(tacc + (uint32_t)(c * 16), g);
+                    load_tmem_chunk(tacc + (uint32_t)(128 + c * 16), u);
+                    const int64_t j = j0 + c * 16;
+                    if (tok_ok && j < p.n_valid) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[i] = (uint32_t)f32_to_bf16_bits(silu_f32(g[2 * i]) * u[2 * i]) |
+                                   ((uint32_t)f32_to_bf16_bits(silu_f32(g[2 * i + 1]) * u[2 * i + 1]) << 16);
+                        uint4 *dst = reinterpret_cast<uint4 *>(h + tok * p.ldo + j);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 16; ++c) {
+                    float v[16];
+                    load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
+                    const int64_t n = (int64_t)t.n * 256 + c * 16;
+                    if (!tok_ok || n >= p.n_valid) continue;
+                    if constexpr (EPI == EPI_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
+                                                                 t.group * p.o_group_stride + tok * p.ldo + n);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    } else if constexpr (EPI == EPI_BF16) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[i] = (uint32_t)f32_to_bf16_bits(v[2 * i]) | ((uint32_t)f32_to_bf16_bits(v[2 * i + 1]) << 16);
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                                               t.group * p.o_group_stride + tok * p.ldo + n);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    } else {  // EPI_MERGED
+                        uint16_t *lo = static_cast<uint16_t *>(p.out);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int64_t col = n + i;
+                            if (col >= p.n_valid) break;
+                            const uint16_t b = f32_to_bf16_bits(v[i]);
+                            if (lo) lo[tok * p.ldo + col] = b;
+                            if (p.out_rm) p.out_rm[tok * p.ldo + logical_to_gathered(col, p.q_dim, p.kv_dim, p.tp)] = b;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(&ctl->tempty[buf]));
+        }
+    }
+
+    if (warp == 0 && lane == 0) {
+        const int64_t first = issued > S ? issued - S : 0;
+        for (int64_t i = first; i < issued; ++i)
+            (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1), p.wait_limit_ns);
+    }
+    if (warp == 1 && lane == 0) {
+        tc_commit(bar_addr(&ctl->drain));
+        (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, p.wait_limit_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// Opt the kernel into the largest dynamic shared memory once per device.
+template <typename Kern>
+cudaError_t ensure_smem_attr(Kern kern, int slot) {
+    static std::atomic<uint64_t> done[8];   // bit per device, per kernel slot
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done[slot].load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess) done[slot].fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+}  // namespace
+
+size_t swapab_smem_bytes(int bn, int stages) {
+    return (size_t)stages * (kATileBytes + (size_t)bn * 128) + 1024 + sizeof(Ctrl);
+}
+size_t std_smem_bytes(int stages) { return (size_t)stages * (kATileBytes + kStdBTileBytes) + 1024 + sizeof(Ctrl); }
+
+int swapab_stages_for(int bn) {
+    const size_t budget = 227 * 1024 - 1024 - sizeof(Ctrl) - 64;
+    int st = (int)(budget / (kATileBytes + (size_t)bn * 128));
+    return st > kMaxStages ? kMaxStages : st;
+}
+int std_stages() { return 4; }
+
+cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
+                          bool pdl, cudaStream_t s) {
+    const size_t smem = swapab_smem_bytes(p.bn, p.stages);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)kSwapAbThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e;
+    switch (epi) {
+        case EPI_SWIGLU:
+            e = ensure_smem_attr(swapab_kernel<EPI_SWIGLU>, 0);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, swapab_kernel<EPI_SWIGLU>, ta, tb, p);
+        case EPI_BF16:
+            e = ensure_smem_attr(swapab_kernel<EPI_BF16>, 1);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, swapab_kernel<EPI_BF16>, ta, tb, p);
+        case EPI_F32:
+            e = ensure_smem_attr(swapab_kernel<EPI_F32>, 2);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, swapab_kernel<EPI_F32>, ta, tb, p);
+        default:
+            e = ensure_smem_attr(swapab_kernel<EPI_MERGED>, 3);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, swapab_kernel<EPI_MERGED>, ta, tb, p);
+    }
+}
+
+cudaError_t launch_std(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const StdParams &p, int grid, bool pdl,
+                       cudaStream_t s) {
+    const size_t smem = std_smem_bytes(p.stages);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)kStdThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e;
+    switch (epi) {
+        case EPI_SWIGLU:
+            e = ensure_smem_attr(std_kernel<EPI_SWIGLU>, 4);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, std_kernel<EPI_SWIGLU>, ta, tb, p);
+        case EPI_BF16:
+            e = ensure_smem_attr(std_kernel<EPI_BF16>, 5);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, std_kernel<EPI_BF16>, ta, tb, p);
+        case EPI_F32:
+            e = ensure_smem_attr(std_kernel<EPI_F32>, 6);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, std_kernel<EPI_F32>, ta, tb, p);
+        default:
+            e = ensure_smem_attr(std_kernel<EPI_MERGED>, 7);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, std_kernel<EPI_MERGED>, ta, tb, p);
+    }
+}
+
+}  // namespace tc
+}  // namespace mse

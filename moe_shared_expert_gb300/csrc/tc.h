@@ -1,0 +1,76 @@
+// Internal interface of the tensor-core (tcgen05 + TMA) kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mse {
+namespace tc {
+
+enum Epi : int {
+    EPI_SWIGLU = 0,      // h[t, j] = bf16(silu(g) * u)
+    EPI_BF16 = 1,        // out[t, n] = bf16(acc)
+    EPI_F32 = 2,         // out[t, n] = acc (fp32)
+    EPI_MERGED = 3,      // logical and/or rank-major bf16 outputs
+};
+
+// Work of one launch of the swap-AB kernel (weights on the 128-row MMA side,
+// tokens on the N side), decomposed stream-K over (group, m-tile, k-block).
+struct SwapAbParams {
+    int n_mtiles;          // 128-row A tiles per group
+    int n_groups;          // independent outputs (shards); 1 when replicated
+    int kb_per_tile;       // 64-wide k-blocks reduced by one tile
+    int kb_first;          // k-block index of group 0's first block
+    int kb_group_stride;   // k-block offset between groups
+    int total_units;       // n_groups * n_mtiles * kb_per_tile
+    int bn;                // MMA N (tokens, padded to a multiple of 16), <= 256
+    int stages;            // smem pipeline depth
+    int tmem_cols;         // allocated TMEM columns (power of two >= 2*bn)
+    int a_row_base;        // SWIGLU: first intermediate index j of tile 0 (multiple of 64)
+    int T;                 // valid tokens
+    int64_t m_valid;       // valid output features (A rows) for masking
+    void *out; int64_t ldo; int64_t o_group_stride;
+    uint16_t *out_rm; int64_t q_dim, kv_dim; int tp;   // EPI_MERGED
+    float *slots;          // split-K partial tiles: 2 per CTA, 128 x bn fp32 each
+    int *counters;         // one per tile; zero on entry, left zero on exit
+    uint64_t wait_limit_ns;
+    uint32_t *err;
+};
+
+// Persistent standard-orientation kernel (tokens on the 128-row MMA side,
+// weights on N = 256), one tile = 128 tokens x 256 output columns, full K.
+struct StdParams {
+    int n_mtiles;          // token tiles of 128
+    int n_ntiles;          // 256-wide column tiles (SWIGLU: 128 j's of gate + 128 of up)
+    int n_groups;
+    int kb_per_tile;
+    int kb_first;
+    int kb_group_stride;
+    int stages;
+    int T;
+    int64_t n_valid;       // valid output columns (I, H or C)
+    int n_base;            // SWIGLU: first j of column tile 0
+    void *out; int64_t ldo; int64_t o_group_stride;
+    uint16_t *out_rm; int64_t q_dim, kv_dim; int tp;
+    uint64_t wait_limit_ns;
+    uint32_t *err;
+};
+
+constexpr int kSwapAbThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kStdThreads = 192;
+constexpr int kMaxStages = 12;
+constexpr int kMaxGrid = 160;         // cap on persistent / stream-K grids
+
+// Dynamic shared memory of the kernels.
+size_t swapab_smem_bytes(int bn, int stages);
+size_t std_smem_bytes(int stages);
+int swapab_stages_for(int bn);
+int std_stages();
+
+cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
+                          bool pdl, cudaStream_t s);
+cudaError_t launch_std(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const StdParams &p, int grid, bool pdl,
+                       cudaStream_t s);
+
+}  // namespace tc
+}  // namespace mse

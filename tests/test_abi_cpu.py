@@ -1,0 +1,150 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol its
+header declares, and rejects invalid arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_shared_expert_gb300 as mse
+from moe_shared_expert_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mse.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return mse.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"^MSE_API\s+[\w\s\*]*?\**\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_symbols())
+    for n in ["mlp_swiglu_forward", "mlp_swiglu_shard_partial", "shard_sum", "merged_proj_forward",
+              "merged_proj_reorder", "mlp_swiglu_workspace_bytes", "merged_proj_workspace_bytes",
+              "mse_poll_device_error", "mse_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings(L):
+    for code, name in mse.STATUS.items():
+        assert L.mse_status_string(code).decode() == name
+    assert L.mse_version().decode().startswith("mse")
+
+
+def test_workspace_sizes(L):
+    T, H, I = 64, 7168, 6144
+    n = L.mlp_swiglu_workspace_bytes(T, H, I)
+    assert n >= T * I * 2 and n % 256 == 0
+    assert L.mlp_swiglu_workspace_bytes(0, H, I) == 0
+    assert L.mlp_swiglu_workspace_bytes(8192, H, I) >= 8192 * I * 2
+    assert L.merged_proj_workspace_bytes(128, 7168, 1536, 576) > 0
+    assert L.merged_proj_workspace_bytes(128, 7168, -1, 576) == 0
+
+
+# Fake, never-dereferenced addresses: every call below fails validation before any
+# CUDA call.  As a second guard they are not run where a CUDA device is visible.
+FAKE = 0x10000
+
+
+def _gpu_visible():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+no_gpu_only = pytest.mark.skipif(_gpu_visible(), reason="fake-pointer validation checks run only without a GPU")
+GOOD_WS = 1 << 30
+
+
+def code(name):
+    return mse.STATUS_CODE[name]
+
+
+@no_gpu_only
+def test_forward_validation(L):
+    f = L.mlp_swiglu_forward
+    assert f(None, 64, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168, FAKE, GOOD_WS, None) == code("MSE_ERR_INVALID_ARG")
+    assert f(FAKE, 0, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168, FAKE, GOOD_WS, None) == code("MSE_ERR_INVALID_ARG")
+    # truncated output geometry
+    assert f(FAKE, 64, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168 - 1, FAKE, GOOD_WS, None) == code("MSE_ERR_GEOMETRY")
+    # workspace missing / too small / misaligned
+    assert f(FAKE, 64, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168, None, GOOD_WS, None) == code("MSE_ERR_WORKSPACE")
+    assert f(FAKE, 64, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168, FAKE, 1024, None) == code("MSE_ERR_WORKSPACE")
+    assert f(FAKE, 64, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168, FAKE + 8, GOOD_WS, None) == code("MSE_ERR_WORKSPACE")
+
+
+@no_gpu_only
+def test_shard_partial_validation(L):
+    f = L.mlp_swiglu_shard_partial
+    args = lambda tp, rf, rc, cap, dt=0: (FAKE, 128, 7168, 6144, FAKE, FAKE, tp, rf, rc, FAKE, dt, cap, FAKE,
+                                          GOOD_WS, None)
+    full = 8 * 128 * 7168
+    # 6144 % 5 != 0: the sharding gate's divisibility rule
+    assert f(*args(5, 0, 5, full)) == code("MSE_ERR_NOT_DIVISIBLE")
+    # H % tp != 0 (7168 % 3 != 0 although 6144 % 3 == 0)
+    assert f(*args(3, 0, 3, full)) == code("MSE_ERR_NOT_DIVISIBLE")
+    assert f(*args(8, 6, 3, full)) == code("MSE_ERR_GEOMETRY")       # ranks beyond tp
+    assert f(*args(8, -1, 2, full)) == code("MSE_ERR_GEOMETRY")
+    assert f(*args(8, 0, 0, full)) == code("MSE_ERR_GEOMETRY")
+    assert f(*args(8, 0, 8, full - 1)) == code("MSE_ERR_GEOMETRY")   # truncated partial buffer
+    assert f(*args(8, 0, 8, full, 7)) == code("MSE_ERR_INVALID_ARG")  # bad dtype
+    assert f(*args(0, 0, 1, full)) == code("MSE_ERR_INVALID_ARG")
+
+
+@no_gpu_only
+def test_shard_sum_validation(L):
+    f = L.shard_sum
+    assert f(FAKE, 0, 8, 127, 7168, FAKE, 127 * 7168, None) == code("MSE_ERR_NOT_DIVISIBLE")
+    assert f(FAKE, 0, 8, 128, 7168, FAKE, 128 * 7168 - 1, None) == code("MSE_ERR_GEOMETRY")
+    assert f(None, 0, 8, 128, 7168, FAKE, 128 * 7168, None) == code("MSE_ERR_INVALID_ARG")
+    assert f(FAKE, 3, 8, 128, 7168, FAKE, 128 * 7168, None) == code("MSE_ERR_INVALID_ARG")
+
+
+@no_gpu_only
+def test_merged_validation(L):
+    f = L.merged_proj_forward
+    C = 1536 + 576
+    ok_ws = L.merged_proj_workspace_bytes(128, 7168, 1536, 576)
+    # every merged output size must be divisible by tp
+    assert f(FAKE, 128, 7168, FAKE, 1536, 576, 5, FAKE, FAKE, 128 * C, FAKE, ok_ws, None) == code("MSE_ERR_NOT_DIVISIBLE")
+    assert f(FAKE, 128, 7168, FAKE, 1536, 576, 128, FAKE, FAKE, 128 * C, FAKE, ok_ws, None) == code("MSE_ERR_NOT_DIVISIBLE")
+    assert f(FAKE, 128, 7168, FAKE, 1536, 576, 16, FAKE, FAKE, 128 * C - 1, FAKE, ok_ws, None) == code("MSE_ERR_GEOMETRY")
+    assert f(FAKE, 128, 7168, FAKE, 1536, 576, 16, None, None, 128 * C, FAKE, ok_ws, None) == code("MSE_ERR_INVALID_ARG")
+    r = L.merged_proj_reorder
+    assert r(FAKE, FAKE + 1 << 20, 128, 1536, 576, 7, 128 * C, None) == code("MSE_ERR_NOT_DIVISIBLE")
+    assert r(FAKE, FAKE + (1 << 24), 128, 1536, 576, 16, 128 * C - 1, None) == code("MSE_ERR_GEOMETRY")
+    assert r(FAKE, FAKE + 100, 128, 1536, 576, 16, 128 * C, None) == code("MSE_ERR_INVALID_ARG")  # overlap
+
+
+def test_settings_roundtrip(L):
+    old = L.mse_get_wait_limit_ns()
+    L.mse_set_wait_limit_ns(12345)
+    assert L.mse_get_wait_limit_ns() == 12345
+    L.mse_set_wait_limit_ns(old)
+    prev = L.mse_set_kernel_path(mse.PATH_GENERIC)
+    assert L.mse_set_kernel_path(prev) == mse.PATH_GENERIC
+    assert L.mse_set_kernel_path(99) == prev        # invalid value: unchanged
+
+
+def test_product_path_does_not_import_oracle():
+    import sys
+    for mod in ["moe_shared_expert_gb300", "moe_shared_expert_gb300._build"]:
+        src = open(sys.modules[mod].__file__).read()
+        assert "oracle" not in src.replace("# oracle", "")
+    for f in os.listdir(os.path.join(ROOT, "moe_shared_expert_gb300", "csrc")):
+        assert "oracle" not in open(os.path.join(ROOT, "moe_shared_expert_gb300", "csrc", f)).read().lower()

@@ -1,0 +1,314 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on the
+same seeded inputs, for the five workloads and the edge cases of the method.
+
+Criterion: |gpu - oracle| <= 0.02 + 0.02 |oracle| per element for floating
+point; permutations (shard slices, rank-major <-> logical) bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests.helpers import assert_close, bits_f64, kernel_path, to_bits, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+mse = pytest.importorskip("moe_shared_expert_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from moe_shared_expert_gb300 import _build
+    _build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mse.lib()
+    yield
+    assert mse.poll_device_error() == 0
+
+
+_cache = {}
+
+
+def mlp_inputs(w: W.Workload, T=None):
+    key = (w.name, T)
+    if key not in _cache:
+        wgu, wd = W.make_mlp_weights(w)
+        _cache[key] = (W.make_x(w, T), wgu, wd)
+    return _cache[key]
+
+
+def run_forward(x, wgu, wd):
+    dx, dgu, dwd = to_dev(x), to_dev(wgu), to_dev(wd)
+    T, H = x.shape
+    I = wd.shape[1]
+    ws = mse.new_mlp_workspace(T, H, I)
+    y = mse.mlp_swiglu_forward(dx, dgu, dwd, workspace=ws)
+    torch.cuda.synchronize()
+    h = ws[: T * I * 2].view(torch.int16).view(T, I).cpu().numpy().view(np.uint16)
+    return to_bits(y), h
+
+
+# --------------------------------------------------------------------------- config 1
+def test_tiny_sharded_tp4():
+    w = W.TINY_SHARDED
+    x, wgu, wd = mlp_inputs(w)
+    y_ref, _, _ = oracle.mlp_forward(x, wgu, wd)
+    y, _ = run_forward(x, wgu, wd)
+    assert_close(bits_f64(y), bits_f64(y_ref), "replicated")
+    parts = mse.mlp_swiglu_shard_partial(to_dev(x), to_dev(wgu), to_dev(wd), w.tp, partial_dtype=torch.float32)
+    red = mse.shard_sum(parts)
+    torch.cuda.synchronize()
+    ref_parts = [oracle.shard_partial(x, wgu, wd, w.tp, r, oracle.F32)[1] for r in range(w.tp)]
+    for r in range(w.tp):
+        assert_close(parts[r].cpu().numpy(), ref_parts[r], f"partial {r}")
+    ref_red = oracle.shard_sum(np.stack(ref_parts), oracle.F32)
+    red_b = to_bits(red)
+    assert_close(bits_f64(red_b), bits_f64(ref_red), "shard_sum")
+    tpr = w.T // w.tp
+    for r in range(w.tp):   # each rank's scatter share equals the replicated rows
+        sl = slice(r * tpr, (r + 1) * tpr)
+        assert_close(bits_f64(red_b[sl]), bits_f64(y_ref[sl]), f"rank {r} rows")
+
+
+# --------------------------------------------------------------------------- config 2
+@pytest.mark.parametrize("path", [mse.PATH_TENSORCORE, mse.PATH_GENERIC])
+def test_decode_t64(path):
+    w = W.DECODE_T64
+    x, wgu, wd = mlp_inputs(w)
+    y_ref, _, h_ref = oracle.mlp_forward(x, wgu, wd)
+    with kernel_path(path):
+        y, h = run_forward(x, wgu, wd)
+        y2, _ = run_forward(x, wgu, wd)
+    assert_close(bits_f64(h), bits_f64(h_ref), "h")
+    r = assert_close(bits_f64(y), bits_f64(y_ref), "y")
+    assert np.array_equal(y, y2), "not deterministic"
+    print(f"decode T=64 path {path}: max err/tol {r:.3f}")
+
+
+# --------------------------------------------------------------------------- config 3
+def test_tp8_emulated_t128():
+    w = W.TP8_EMULATED
+    x, wgu, wd = mlp_inputs(w)
+    dx, dgu, dwd = to_dev(x), to_dev(wgu), to_dev(wd)
+    ws = mse.new_mlp_workspace(w.T, w.H, w.I)
+    parts = mse.mlp_swiglu_shard_partial(dx, dgu, dwd, w.tp, workspace=ws)
+    red = mse.shard_sum(parts)
+    y = mse.mlp_swiglu_forward(dx, dgu, dwd, workspace=ws)
+    torch.cuda.synchronize()
+    ref_parts = []
+    for r in range(w.tp):
+        _, pr = oracle.shard_partial(x, wgu, wd, w.tp, r, oracle.BF16)
+        ref_parts.append(pr)
+        assert_close(bits_f64(to_bits(parts[r])), bits_f64(pr), f"partial {r}")
+    ref_red = oracle.shard_sum(np.stack(ref_parts), oracle.BF16)
+    assert_close(bits_f64(to_bits(red)), bits_f64(ref_red), "shard_sum")
+    y_ref, _, _ = oracle.mlp_forward(x, wgu, wd)
+    assert_close(bits_f64(to_bits(y)), bits_f64(y_ref), "replicated")
+    # the pages' equivalence: the reduced partials reproduce the replicated output per token
+    assert_close(bits_f64(to_bits(red)), bits_f64(y_ref), "sum of partials vs replicated")
+
+
+def test_shard_subset_matches_all_shards():
+    # rank_first/rank_count select the same partials (the split of the reduction
+    # between CTAs differs, so floating point agrees to tolerance, not bit for bit)
+    w = W.TP8_EMULATED
+    x, wgu, wd = mlp_inputs(w)
+    dx, dgu, dwd = to_dev(x), to_dev(wgu), to_dev(wd)
+    allp = mse.mlp_swiglu_shard_partial(dx, dgu, dwd, w.tp)
+    sub = mse.mlp_swiglu_shard_partial(dx, dgu, dwd, w.tp, rank_first=3, rank_count=2)
+    one = mse.mlp_swiglu_shard_partial(dx, dgu, dwd, w.tp, rank_first=7, rank_count=1)
+    torch.cuda.synchronize()
+    assert_close(bits_f64(to_bits(sub)), bits_f64(to_bits(allp[3:5])), "ranks 3-4")
+    assert_close(bits_f64(to_bits(one)), bits_f64(to_bits(allp[7:8])), "rank 7")
+
+
+def integer_exact_mlp(T, H, I):
+    """Inputs on which every step is exact in fp32 and fp64 whatever the summation
+    order: x in {20, 24, ..., 40}; one-hot gate/up/down rows.  Then g, u in [20, 40],
+    silu(g) rounds to g (e^-20 < 2^-25), h = g*u = 16*m with m <= 100 is a bf16
+    value, and each output is one h value (the rest of its sum is exact zeros)."""
+    rng = np.random.default_rng(T + H + I)
+    xv = 4.0 * rng.integers(5, 11, size=(T, H))
+    x = W.f32_to_bf16_bits(xv.astype(np.float32))
+    wgu = np.zeros((2 * I, H), dtype=np.uint16)
+    j = np.arange(I)
+    wgu[j, j % H] = 0x3F80
+    wgu[I + j, (7 * j + 3) % H] = 0x3F80
+    wd = np.zeros((H, I), dtype=np.uint16)
+    n = np.arange(H)
+    wd[n, (5 * n + 1) % I] = 0x3F80
+    return x, wgu, wd
+
+
+@pytest.mark.parametrize("path", [mse.PATH_TENSORCORE, mse.PATH_GENERIC])
+@pytest.mark.parametrize("T", [16, 300])
+def test_shard_slices_bit_exact(path, T):
+    # the shard index map (gate rows, up rows I + ..., down columns of slice r) checked
+    # bit-exactly through the kernels against the oracle
+    H, I, tp = 384, 192, 3
+    x, wgu, wd = integer_exact_mlp(T, H, I)
+    with kernel_path(path):
+        parts = mse.mlp_swiglu_shard_partial(to_dev(x), to_dev(wgu), to_dev(wd), tp)
+        sub = mse.mlp_swiglu_shard_partial(to_dev(x), to_dev(wgu), to_dev(wd), tp, rank_first=1, rank_count=2)
+        y, _ = run_forward(x, wgu, wd)
+    torch.cuda.synchronize()
+    for r in range(tp):
+        _, pr = oracle.shard_partial(x, wgu, wd, tp, r, oracle.BF16)
+        assert np.array_equal(to_bits(parts[r]), pr), f"partial {r}"
+    assert torch.equal(sub, parts[1:3])
+    y_ref, _, _ = oracle.mlp_forward(x, wgu, wd)
+    assert np.array_equal(y, y_ref)
+    assert np.array_equal(to_bits(mse.shard_sum(parts)), y_ref)
+
+
+# --------------------------------------------------------------------------- config 4
+def test_mla_merged_tp16():
+    w = W.MLA_MERGED
+    x = W.make_x(w)
+    wm = W.make_merged_weight(w)
+    lo, rm = mse.merged_proj_forward(to_dev(x), to_dev(wm), w.q_dim, w.kv_dim, w.tp)
+    back = mse.merged_proj_reorder(rm, w.q_dim, w.kv_dim, w.tp)
+    torch.cuda.synchronize()
+    lo_b, rm_b, back_b = to_bits(lo), to_bits(rm), to_bits(back)
+    ref_lo, ref_rm, _ = oracle.merged_proj(x, wm, w.q_dim, w.kv_dim, w.tp)
+    assert_close(bits_f64(lo_b), bits_f64(ref_lo), "logical")
+    assert_close(bits_f64(rm_b), bits_f64(ref_rm), "rank-major")
+    perm = oracle.rank_major_to_logical(w.q_dim, w.kv_dim, w.tp)
+    assert np.array_equal(rm_b, lo_b[:, perm]), "rank-major is not the gather permutation of logical"
+    assert np.array_equal(back_b, lo_b), "reorder did not restore the logical layout"
+    assert np.array_equal(back_b, oracle.reorder(rm_b, w.q_dim, w.kv_dim, w.tp))
+
+
+def test_mla_permutation_exact_through_projection():
+    # integer-valued x and one-hot weight rows: every output is an exact integer
+    q, kv, tp, H, T = 1536, 576, 16, 7168, 128
+    C = q + kv
+    xi = ((np.arange(T * H).reshape(T, H) * 7) % 201) - 100
+    x = W.f32_to_bf16_bits(xi.astype(np.float32))
+    wm = np.zeros((C, H), dtype=np.uint16)
+    wm[np.arange(C), (np.arange(C) * 3) % H] = 0x3F80      # 1.0
+    lo, rm = mse.merged_proj_forward(to_dev(x), to_dev(wm), q, kv, tp)
+    torch.cuda.synchronize()
+    ref_lo, ref_rm, _ = oracle.merged_proj(x, wm, q, kv, tp)
+    assert np.array_equal(to_bits(lo), ref_lo)
+    assert np.array_equal(to_bits(rm), ref_rm)
+
+
+# --------------------------------------------------------------------------- config 5
+def test_prefill_t8192_sampled_rows():
+    w = W.PREFILL_T8192
+    x, wgu, wd = mlp_inputs(w)
+    y, h = run_forward(x, wgu, wd)
+    rng = np.random.default_rng(123)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 129, 4095, 4096, 8063, 8064, 8190, 8191],
+                                     rng.integers(0, w.T, 29)]))
+    y_ref, _, h_ref = oracle.mlp_forward(x, wgu, wd, rows=rows)
+    assert_close(bits_f64(h[rows]), bits_f64(h_ref), "h rows")
+    r = assert_close(bits_f64(y[rows]), bits_f64(y_ref), "y rows")
+    print(f"prefill sampled rows: max err/tol {r:.3f}")
+
+
+# --------------------------------------------------------------------------- edge cases
+def small_case(T, H, I, seed):
+    x = W.make_custom(seed, 0, (T, H))
+    wgu = W.make_custom(seed, 1, (2 * I, H), 1 / math.sqrt(H))
+    wd = W.make_custom(seed, 2, (H, I), 1 / math.sqrt(I))
+    return x, wgu, wd
+
+
+@pytest.mark.parametrize("T", [1, 7, 16, 17, 100, 200, 256, 257, 300, 383])
+@pytest.mark.parametrize("path", [mse.PATH_TENSORCORE, mse.PATH_GENERIC])
+def test_ragged_tokens(T, path):
+    H, I = 384, 320
+    x, wgu, wd = small_case(T, H, I, 1000 + T)
+    y_ref, _, h_ref = oracle.mlp_forward(x, wgu, wd)
+    with kernel_path(path):
+        y, h = run_forward(x, wgu, wd)
+    assert_close(bits_f64(h), bits_f64(h_ref), f"h T={T}")
+    assert_close(bits_f64(y), bits_f64(y_ref), f"y T={T}")
+
+
+@pytest.mark.parametrize("T,H,I", [(5, 16, 12), (3, 40, 24), (9, 100, 36), (130, 72, 48)])
+def test_unaligned_shapes_take_generic_path(T, H, I):
+    x, wgu, wd = small_case(T, H, I, 7 * T + H)
+    y_ref, _, _ = oracle.mlp_forward(x, wgu, wd)
+    y, _ = run_forward(x, wgu, wd)
+    assert_close(bits_f64(y), bits_f64(y_ref), "y")
+    with kernel_path(mse.PATH_TENSORCORE):
+        with pytest.raises(mse.MSEError) as e:
+            run_forward(x, wgu, wd)
+        assert e.value.name == "MSE_ERR_UNSUPPORTED_SHAPE"
+
+
+@pytest.mark.parametrize("T", [4, 64, 300])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_sharded_edge(T, dtype):
+    H, I, tp = 384, 192, 3          # s = 64
+    x, wgu, wd = small_case(T, H, I, 50 + T)
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    od = oracle.BF16 if dtype == "bf16" else oracle.F32
+    parts = mse.mlp_swiglu_shard_partial(to_dev(x), to_dev(wgu), to_dev(wd), tp, partial_dtype=td)
+    torch.cuda.synchronize()
+    for r in range(tp):
+        _, pr = oracle.shard_partial(x, wgu, wd, tp, r, od)
+        got = to_bits(parts[r]) if dtype == "bf16" else parts[r].cpu().numpy()
+        ref = pr if dtype == "f32" else pr
+        assert_close(bits_f64(got) if dtype == "bf16" else got, bits_f64(ref) if dtype == "bf16" else ref,
+                     f"partial {r}")
+
+
+@pytest.mark.parametrize("T", [1, 33, 300])
+def test_merged_edge(T):
+    q, kv, tp, H = 96, 36, 4, 256
+    x = W.make_custom(77 + T, 0, (T, H))
+    wm = W.make_custom(77 + T, 4, (q + kv, H), 1 / 16)
+    lo, rm = mse.merged_proj_forward(to_dev(x), to_dev(wm), q, kv, tp)
+    only_rm = mse.merged_proj_forward(to_dev(x), to_dev(wm), q, kv, tp, logical=False)[1]
+    torch.cuda.synchronize()
+    ref_lo, ref_rm, _ = oracle.merged_proj(x, wm, q, kv, tp)
+    assert_close(bits_f64(to_bits(lo)), bits_f64(ref_lo), "logical")
+    perm = oracle.rank_major_to_logical(q, kv, tp)
+    assert np.array_equal(to_bits(rm), to_bits(lo)[:, perm])
+    assert np.array_equal(to_bits(only_rm), to_bits(rm))
+
+
+@pytest.mark.parametrize("n,dtype", [(8, "bf16"), (4, "f32"), (3, "bf16")])
+def test_shard_sum_ragged(n, dtype):
+    T, H = 6 * n, 131          # plane not a multiple of 8 -> scalar kernel
+    rng = np.random.default_rng(n)
+    vals = rng.standard_normal((n, T, H)).astype(np.float32)
+    if dtype == "bf16":
+        p = W.f32_to_bf16_bits(vals).reshape(n, T, H)
+        dev = to_dev(p)
+        ref = oracle.shard_sum(p, oracle.BF16)
+    else:
+        dev = torch.from_numpy(vals).cuda()
+        ref = oracle.shard_sum(vals, oracle.F32)
+    out = mse.shard_sum(dev)
+    torch.cuda.synchronize()
+    assert_close(bits_f64(to_bits(out)), bits_f64(ref), "shard_sum")
+
+
+def test_workspace_reuse_across_shapes_and_calls():
+    # one zeroed workspace serves consecutive calls of different sizes
+    H, I = 384, 320
+    ws = mse.new_mlp_workspace(256, H, I)
+    outs = []
+    for T in [256, 40, 256]:
+        x, wgu, wd = small_case(T, H, I, 999)
+        y = mse.mlp_swiglu_forward(to_dev(x), to_dev(wgu), to_dev(wd), workspace=ws)
+        outs.append(to_bits(y))
+    assert np.array_equal(outs[0], outs[2])
+    assert mse.poll_device_error() == 0
+
+
+def test_timeout_selftest_reports_and_context_survives():
+    mse.selftest_wait_timeout(2_000_000)          # 2 ms wait that nothing satisfies
+    assert mse.STATUS[mse.poll_device_error()] == "MSE_ERR_TIMEOUT"
+    assert mse.poll_device_error() == 0            # the error word was cleared
+    a = torch.ones(1024, device="cuda")
+    assert float(a.sum().item()) == 1024.0          # the context is still usable
