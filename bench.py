@@ -284,6 +284,10 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
     # per-kernel durations: CUDA events recorded by the library between its two kernels
     n_ph = min(phase_steps, K)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ph)]
+    for trio in evs:            # torch only times events it has seen recorded; the
+        for e in trio:          # library re-records them between its kernels below
+            e.record(stream)
+    torch.cuda.synchronize()
     for i in range(n_ph):
         mse.set_phase_events(*evs[i])
         step(i)

@@ -79,6 +79,12 @@ typedef enum { MSE_BF16 = 0, MSE_F32 = 1 } mse_dtype;
  *                MSE_ERR_UNSUPPORTED_SHAPE. */
 typedef enum { MSE_PATH_AUTO = 0, MSE_PATH_GENERIC = 1, MSE_PATH_TENSORCORE = 2 } mse_kernel_path;
 
+/* Tensor-core kernel for prefill-sized token counts (T > 256), process-wide.
+ *   AUTO:   CTA-pair kernel (two SMs share one 256 x 256 tile) for T >= 512,
+ *           single-CTA 128 x 256 kernel below.
+ *   SINGLE: always the single-CTA kernel.   PAIR: always the CTA-pair kernel. */
+typedef enum { MSE_PREFILL_AUTO = 0, MSE_PREFILL_SINGLE = 1, MSE_PREFILL_PAIR = 2 } mse_prefill_kernel;
+
 /* ---------------------------------------------------------------------------
  * Workspace sizing.  The workspace holds the bf16 intermediate h [T x I] and,
  * for the tensor-core path, fp32 split-K partial tiles and tile counters.
@@ -208,6 +214,9 @@ MSE_API uint64_t mse_get_wait_limit_ns(void);
 
 /* Kernel path selection, see mse_kernel_path.  Returns the previous value. */
 MSE_API int mse_set_kernel_path(int path);
+
+/* Prefill kernel selection, see mse_prefill_kernel.  Returns the previous value. */
+MSE_API int mse_set_prefill_kernel(int kind);
 
 /* Failure-detection self test: launches one CTA that waits on a barrier no one
  * arrives on, bounded by `limit_ns`.  The wait runs out by design; the kernel

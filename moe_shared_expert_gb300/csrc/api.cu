@@ -17,6 +17,7 @@ namespace {
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_path{MSE_PATH_AUTO};
+std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -244,6 +245,18 @@ tc::StdParams std_base(int64_t T) {
     return p;
 }
 
+bool use_pair(int64_t T) {
+    const int k = g_prefill.load();
+    if (k == MSE_PREFILL_SINGLE) return false;
+    if (k == MSE_PREFILL_PAIR) return true;
+    return T >= 512;
+}
+
+int pair_clusters(const DeviceInfo &d, int64_t n_tiles) {
+    int64_t c = (d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid) / 2;
+    return (int)(c < n_tiles ? c : n_tiles);
+}
+
 int std_grid(const DeviceInfo &d, int64_t n_tiles) {
     int64_t g = d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid;
     return (int)(g < n_tiles ? g : n_tiles);
@@ -276,6 +289,25 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         return from_cuda(tc::launch_swapab(tc::EPI_SWIGLU, ta, tb, p, swapab_grid(d, p.total_units), true, s));
     }
     tc::StdParams p = std_base(T);
+    if (use_pair(T)) {
+        p.stages = tc::pair_stages();
+        if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
+        if ((st = map_2d(&tb, w_gate_up, 2 * I, H, H, 128)) != MSE_OK) return st;
+        p.n_mtiles = (int)((T + 255) / 256);
+        p.n_ntiles = (int)((width + 127) / 128);
+        p.n_groups = 1;
+        p.kb_per_tile = (int)(H / 64);
+        p.n_valid = j_begin + width;
+        p.n_base = (int)j_begin;
+        p.b_base = (int)j_begin;
+        p.b_n_stride = 128;
+        p.b_rank_stride = (int)I;     // CTA 0 loads the gate rows, CTA 1 the up rows
+        p.out = h;
+        p.ldo = I;
+        p.err = d.err;
+        return from_cuda(tc::launch_pair(tc::EPI_SWIGLU, ta, tb, p,
+                                         pair_clusters(d, (int64_t)p.n_mtiles * p.n_ntiles), true, s));
+    }
     if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
     if ((st = map_gate_up_halves(&tb, w_gate_up, H, I, 128)) != MSE_OK) return st;
     p.n_mtiles = (int)((T + 127) / 128);
@@ -319,6 +351,27 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
         return from_cuda(tc::launch_swapab(epi, ta, tb, p, swapab_grid(d, p.total_units), true, s));
     }
     tc::StdParams p = std_base(T);
+    if (use_pair(T)) {
+        p.stages = tc::pair_stages();
+        if ((st = map_2d(&ta, h, T, I, I, 128)) != MSE_OK) return st;
+        if ((st = map_2d(&tb, w_down, H, I, I, 128)) != MSE_OK) return st;
+        p.n_mtiles = (int)((T + 255) / 256);
+        p.n_ntiles = (int)((H + 255) / 256);
+        p.n_groups = groups;
+        p.kb_per_tile = (int)(s_width / 64);
+        p.kb_first = (int)(kcol0 / 64);
+        p.kb_group_stride = p.kb_per_tile;
+        p.n_valid = H;
+        p.b_base = 0;
+        p.b_n_stride = 256;
+        p.b_rank_stride = 128;
+        p.out = out;
+        p.ldo = H;
+        p.o_group_stride = T * H;
+        p.err = d.err;
+        return from_cuda(tc::launch_pair(epi, ta, tb, p,
+                                         pair_clusters(d, (int64_t)groups * p.n_mtiles * p.n_ntiles), true, s));
+    }
     if ((st = map_2d(&ta, h, T, I, I, 128)) != MSE_OK) return st;
     if ((st = map_2d(&tb, w_down, H, I, I, 256)) != MSE_OK) return st;
     p.n_mtiles = (int)((T + 127) / 128);
@@ -526,6 +579,26 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
         return from_cuda(tc::launch_swapab(tc::EPI_MERGED, ta, tb, p, swapab_grid(*d, p.total_units), true, s));
     }
     tc::StdParams p = std_base(T);
+    if (use_pair(T)) {
+        p.stages = tc::pair_stages();
+        if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
+        if ((st = map_2d(&tb, w, C, H, H, 128)) != MSE_OK) return st;
+        p.n_mtiles = (int)((T + 255) / 256);
+        p.n_ntiles = (int)((C + 255) / 256);
+        p.n_groups = 1;
+        p.kb_per_tile = (int)(H / 64);
+        p.n_valid = C;
+        p.b_base = 0;
+        p.b_n_stride = 256;
+        p.b_rank_stride = 128;
+        p.out = out_logical;
+        p.ldo = C;
+        p.out_rm = out_rank_major;
+        p.q_dim = q_dim; p.kv_dim = kv_dim; p.tp = tp;
+        p.err = d->err;
+        return from_cuda(tc::launch_pair(tc::EPI_MERGED, ta, tb, p,
+                                         pair_clusters(*d, (int64_t)p.n_mtiles * p.n_ntiles), true, s));
+    }
     if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
     if ((st = map_2d(&tb, w, C, H, H, 256)) != MSE_OK) return st;
     p.n_mtiles = (int)((T + 127) / 128);
@@ -579,6 +652,11 @@ uint64_t mse_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
 int mse_set_kernel_path(int path) {
     if (path < MSE_PATH_AUTO || path > MSE_PATH_TENSORCORE) return g_path.load();
     return g_path.exchange(path);
+}
+
+int mse_set_prefill_kernel(int kind) {
+    if (kind < MSE_PREFILL_AUTO || kind > MSE_PREFILL_PAIR) return g_prefill.load();
+    return g_prefill.exchange(kind);
 }
 
 void mse_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end) {

@@ -571,10 +571,240 @@ __global__ void __launch_bounds__(kStdThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+
+// ---------------------------------------------------------------------------
+// CTA-pair persistent kernel (cta_group::2): tile = 256 tokens x 256 columns.
+// Each CTA of a cluster pair loads its own 128 token rows (A) and its own half of
+// the 256 B rows, and holds the accumulator rows of its tokens in its own TMEM;
+// the even CTA issues the MMAs for both.  Per SM this halves the operand bytes
+// per FLOP against the single-CTA 128 x 256 tile.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kPairBTileBytes = 128 * 64 * 2;
+constexpr int kPairBandM = 8;
+
+template <int EPI>
+__global__ void __launch_bounds__(kStdThreads, 1)
+    pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const StdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const int S = p.stages;
+    const uint32_t sA = base;
+    const uint32_t sB = base + (uint32_t)S * kATileBytes;
+    Ctrl *ctl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + (uint32_t)S * (kATileBytes + kPairBTileBytes));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int64_t cluster = blockIdx.x / 2, n_clusters = gridDim.x / 2;
+    const int64_t n_tiles = (int64_t)p.n_groups * p.n_mtiles * p.n_ntiles;
+    const int kbp = p.kb_per_tile;
+    constexpr uint32_t kTmemCols = 512;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_addr(&ctl->full[s]), 1);
+            mbar_init(bar_addr(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_addr(&ctl->tfull[b]), 1);
+            mbar_init(bar_addr(&ctl->tempty[b]), 8);   // 4 epilogue warps x 2 CTAs
+        }
+        mbar_init(bar_addr(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();        // the peer's barriers are initialised before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile int *abort_flag = &ctl->abort_flag;
+    pdl_launch_dependents();
+
+    auto tile_of = [&](int64_t id) {
+        StdTile t;
+        const int64_t per_group = (int64_t)p.n_mtiles * p.n_ntiles;
+        t.group = (int)(id / per_group);
+        const int64_t r = id % per_group;
+        const int64_t per_band = (int64_t)kPairBandM * p.n_ntiles;
+        const int band = (int)(r / per_band);
+        const int first_m = band * kPairBandM;
+        const int band_m = min(kPairBandM, p.n_mtiles - first_m);
+        const int64_t in_band = r % per_band;
+        t.m = first_m + (int)(in_band % band_m);
+        t.n = (int)(in_band / band_m);
+        return t;
+    };
+
+    int64_t issued = 0;
+    if (warp == 0) {
+        if (lane == 0) {
+            pdl_wait();
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int64_t id = cluster; id < n_tiles && ok; id += n_clusters) {
+                const StdTile t = tile_of(id);
+                for (int kb = 0; kb < kbp; ++kb) {
+                    if (!mbar_wait_bounded(bar_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns,
+                                           p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = map_to_rank(bar_addr(&ctl->full[stage]), 0);
+                    if (leader) mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), 2u * (kATileBytes + kPairBTileBytes));
+                    const int k = (p.kb_first + t.group * p.kb_group_stride + kb) * 64;
+                    tma_load_2d_pair(sA + stage * kATileBytes, &tmA, fb, k, t.m * 256 + (int)rank * 128);
+                    tma_load_2d_pair(sB + stage * kPairBTileBytes, &tmB, fb, k,
+                                     p.b_base + t.n * p.b_n_stride + (int)rank * p.b_rank_stride);
+                    ++issued;
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            const uint32_t idesc = idesc_bf16_f32(256, 256);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int64_t id = cluster; id < n_tiles && ok; id += n_clusters, ++it) {
+                const int buf = it & 1;
+                const uint32_t use = (uint32_t)(it >> 1);
+                if (!mbar_wait_bounded(bar_addr(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, p.wait_limit_ns,
+                                       p.err))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(buf * 256);
+                for (int kb = 0; kb < kbp; ++kb) {
+                    if (!mbar_wait_bounded(bar_addr(&ctl->full[stage]), phase, abort_flag, p.wait_limit_ns, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_sw128(sA + stage * kATileBytes);
+                    const uint64_t bd = smem_desc_sw128(sB + stage * kPairBTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16_pair(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                         (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit_pair_multicast(bar_addr(&ctl->empty[stage]), (uint16_t)0x3);
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(bar_addr(&ctl->tfull[buf]), (uint16_t)0x3);
+            }
+        }
+    } else {
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        pdl_wait();
+        int it = 0;
+        for (int64_t id = cluster; id < n_tiles; id += n_clusters, ++it) {
+            const StdTile t = tile_of(id);
+            const int buf = it & 1;
+            const uint32_t use = (uint32_t)(it >> 1);
+            const bool got = mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
+            if (!named_barrier_and(1, 128, got)) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + (uint32_t)(buf * 256) + lane_off;
+            const int64_t tok = (int64_t)t.m * 256 + rank * 128 + row;
+            const bool tok_ok = tok < p.T;
+            if constexpr (EPI == EPI_SWIGLU) {
+                uint16_t *h = static_cast<uint16_t *>(p.out);
+                const int64_t j0 = (int64_t)p.n_base + (int64_t)t.n * 128;
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    float g[16], u[16];
+                    load_tmem_chunk(tacc + (uint32_t)(c * 16), g);
+                    load_tmem_chunk(tacc + (uint32_t)(128 + c * 16), u);
+                    const int64_t j = j0 + c * 16;
+                    if (tok_ok && j < p.n_valid) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[i] = (uint32_t)f32_to_bf16_bits(silu_f32(g[2 * i]) * u[2 * i]) |
+                                   ((uint32_t)f32_to_bf16_bits(silu_f32(g[2 * i + 1]) * u[2 * i + 1]) << 16);
+                        uint4 *dst = reinterpret_cast<uint4 *>(h + tok * p.ldo + j);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 16; ++c) {
+                    float v[16];
+                    load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
+                    const int64_t n = (int64_t)t.n * 256 + c * 16;
+                    if (!tok_ok || n >= p.n_valid) continue;
+                    if constexpr (EPI == EPI_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
+                                                                 t.group * p.o_group_stride + tok * p.ldo + n);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    } else if constexpr (EPI == EPI_BF16) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[i] = (uint32_t)f32_to_bf16_bits(v[2 * i]) | ((uint32_t)f32_to_bf16_bits(v[2 * i + 1]) << 16);
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                                               t.group * p.o_group_stride + tok * p.ldo + n);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    } else {  // EPI_MERGED
+                        uint16_t *lo = static_cast<uint16_t *>(p.out);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int64_t col = n + i;
+                            if (col >= p.n_valid) break;
+                            const uint16_t b = f32_to_bf16_bits(v[i]);
+                            if (lo) lo[tok * p.ldo + col] = b;
+                            if (p.out_rm) p.out_rm[tok * p.ldo + logical_to_gathered(col, p.q_dim, p.kv_dim, p.tp)] = b;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(bar_addr(&ctl->tempty[buf]), 0));
+        }
+    }
+
+    // ---- teardown ----
+    if (warp == 0 && lane == 0) {
+        // every issued stage is released by the leader's MMA commit once its bytes
+        // (from both CTAs) have landed and been consumed
+        const int64_t first = issued > S ? issued - S : 0;
+        for (int64_t i = first; i < issued; ++i) {
+            const bool done = mbar_wait_drain(bar_addr(&ctl->empty[i % S]), (uint32_t)((i / S) & 1), p.wait_limit_ns);
+            if (!done) __nanosleep(200000);   // abort path: let in-flight copies land
+        }
+    }
+    if (warp == 1 && lane == 0 && leader) {
+        tc_commit_pair_multicast(bar_addr(&ctl->drain), (uint16_t)0x1);
+        (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, p.wait_limit_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
 // Opt the kernel into the largest dynamic shared memory once per device.
 template <typename Kern>
 cudaError_t ensure_smem_attr(Kern kern, int slot) {
-    static std::atomic<uint64_t> done[8];   // bit per device, per kernel slot
+    static std::atomic<uint64_t> done[16];   // bit per device, per kernel slot
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -664,6 +894,65 @@ cudaError_t launch_std(int epi, const CUtensorMap &ta, const CUtensorMap &tb, co
             e = ensure_smem_attr(std_kernel<EPI_MERGED>, 7);
             if (e != cudaSuccess) return e;
             return cudaLaunchKernelEx(&cfg, std_kernel<EPI_MERGED>, ta, tb, p);
+    }
+}
+
+
+size_t pair_smem_bytes(int stages) { return (size_t)stages * (kATileBytes + kPairBTileBytes) + 1024 + sizeof(Ctrl); }
+int pair_stages() { return 6; }
+
+cudaError_t launch_pair(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const StdParams &p, int clusters,
+                        bool pdl, cudaStream_t s) {
+    const size_t smem = pair_smem_bytes(p.stages);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    cfg.blockDim = dim3((unsigned)kStdThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    cudaError_t e;
+    // one wave: no more clusters than can be resident at once
+    {
+        static std::atomic<int> max_clusters[64];
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        int mc = max_clusters[dev & 63].load();
+        if (mc == 0) {
+            if ((e = ensure_smem_attr(pair_kernel<EPI_BF16>, 9)) != cudaSuccess) return e;
+            cudaLaunchConfig_t q = cfg;
+            q.numAttrs = 1;
+            q.gridDim = dim3(2);
+            if ((e = cudaOccupancyMaxActiveClusters(&mc, pair_kernel<EPI_BF16>, &q)) != cudaSuccess) return e;
+            if (mc < 1) mc = 1;
+            max_clusters[dev & 63].store(mc);
+        }
+        if (clusters > mc) cfg.gridDim = dim3((unsigned)(2 * mc));
+    }
+    switch (epi) {
+        case EPI_SWIGLU:
+            e = ensure_smem_attr(pair_kernel<EPI_SWIGLU>, 8);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, pair_kernel<EPI_SWIGLU>, ta, tb, p);
+        case EPI_BF16:
+            e = ensure_smem_attr(pair_kernel<EPI_BF16>, 9);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, pair_kernel<EPI_BF16>, ta, tb, p);
+        case EPI_F32:
+            e = ensure_smem_attr(pair_kernel<EPI_F32>, 10);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, pair_kernel<EPI_F32>, ta, tb, p);
+        default:
+            e = ensure_smem_attr(pair_kernel<EPI_MERGED>, 11);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, pair_kernel<EPI_MERGED>, ta, tb, p);
     }
 }
 

@@ -52,6 +52,8 @@ struct StdParams {
     int n_base;            // SWIGLU: first j of column tile 0
     void *out; int64_t ldo; int64_t o_group_stride;
     uint16_t *out_rm; int64_t q_dim, kv_dim; int tp;
+    // CTA-pair kernel only: B row coordinate = b_base + n * b_n_stride + rank * b_rank_stride
+    int b_base, b_n_stride, b_rank_stride;
     uint64_t wait_limit_ns;
     uint32_t *err;
 };
@@ -64,6 +66,8 @@ constexpr int kMaxGrid = 160;         // cap on persistent / stream-K grids
 // Dynamic shared memory of the kernels.
 size_t swapab_smem_bytes(int bn, int stages);
 size_t std_smem_bytes(int stages);
+size_t pair_smem_bytes(int stages);
+int pair_stages();
 int swapab_stages_for(int bn);
 int std_stages();
 
@@ -71,6 +75,9 @@ cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb,
                           bool pdl, cudaStream_t s);
 cudaError_t launch_std(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const StdParams &p, int grid, bool pdl,
                        cudaStream_t s);
+// CTA-pair kernel: 256 tokens x 256 columns per tile, grid = 2 x clusters.
+cudaError_t launch_pair(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const StdParams &p, int clusters,
+                        bool pdl, cudaStream_t s);
 
 }  // namespace tc
 }  // namespace mse

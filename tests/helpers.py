@@ -47,3 +47,13 @@ def kernel_path(path: int):
         yield
     finally:
         mse.set_kernel_path(old)
+
+
+@contextlib.contextmanager
+def prefill_kernel(kind: int):
+    import moe_shared_expert_gb300 as mse
+    old = mse.set_prefill_kernel(kind)
+    try:
+        yield
+    finally:
+        mse.set_prefill_kernel(old)

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import workloads as W
-from tests.helpers import assert_close, bits_f64, kernel_path, to_bits, to_dev
+from tests.helpers import assert_close, bits_f64, kernel_path, prefill_kernel, to_bits, to_dev
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -145,7 +145,7 @@ def integer_exact_mlp(T, H, I):
 
 
 @pytest.mark.parametrize("path", [mse.PATH_TENSORCORE, mse.PATH_GENERIC])
-@pytest.mark.parametrize("T", [16, 300])
+@pytest.mark.parametrize("T", [18, 300])
 def test_shard_slices_bit_exact(path, T):
     # the shard index map (gate rows, up rows I + ..., down columns of slice r) checked
     # bit-exactly through the kernels against the oracle
@@ -199,10 +199,12 @@ def test_mla_permutation_exact_through_projection():
 
 
 # --------------------------------------------------------------------------- config 5
-def test_prefill_t8192_sampled_rows():
+@pytest.mark.parametrize("kind", [mse.PREFILL_PAIR, mse.PREFILL_SINGLE])
+def test_prefill_t8192_sampled_rows(kind):
     w = W.PREFILL_T8192
     x, wgu, wd = mlp_inputs(w)
-    y, h = run_forward(x, wgu, wd)
+    with prefill_kernel(kind):
+        y, h = run_forward(x, wgu, wd)
     rng = np.random.default_rng(123)
     rows = np.unique(np.concatenate([[0, 1, 127, 128, 129, 4095, 4096, 8063, 8064, 8190, 8191],
                                      rng.integers(0, w.T, 29)]))
@@ -230,6 +232,36 @@ def test_ragged_tokens(T, path):
         y, h = run_forward(x, wgu, wd)
     assert_close(bits_f64(h), bits_f64(h_ref), f"h T={T}")
     assert_close(bits_f64(y), bits_f64(y_ref), f"y T={T}")
+
+
+@pytest.mark.parametrize("T", [257, 300, 512, 700, 1000])
+@pytest.mark.parametrize("kind", [mse.PREFILL_SINGLE, mse.PREFILL_PAIR])
+def test_prefill_kernels_ragged(T, kind):
+    H, I = 384, 320
+    x, wgu, wd = small_case(T, H, I, 3000 + T)
+    y_ref, _, h_ref = oracle.mlp_forward(x, wgu, wd)
+    with kernel_path(mse.PATH_TENSORCORE), prefill_kernel(kind):
+        y, h = run_forward(x, wgu, wd)
+    assert_close(bits_f64(h), bits_f64(h_ref), f"h T={T}")
+    assert_close(bits_f64(y), bits_f64(y_ref), f"y T={T}")
+
+
+@pytest.mark.parametrize("kind", [mse.PREFILL_SINGLE, mse.PREFILL_PAIR])
+def test_prefill_kernels_shards_and_merged(kind):
+    T, H, I, tp = 600, 384, 192, 3
+    x, wgu, wd = small_case(T, H, I, 4242)
+    with kernel_path(mse.PATH_TENSORCORE), prefill_kernel(kind):
+        parts = mse.mlp_swiglu_shard_partial(to_dev(x), to_dev(wgu), to_dev(wd), tp, partial_dtype=torch.float32)
+        q, kv, tpm = 96, 36, 4
+        wm = W.make_custom(4243, 4, (q + kv, H), 1 / 16)
+        lo, rm = mse.merged_proj_forward(to_dev(x), to_dev(wm), q, kv, tpm)
+    torch.cuda.synchronize()
+    for r in range(tp):
+        _, pr = oracle.shard_partial(x, wgu, wd, tp, r, oracle.F32)
+        assert_close(parts[r].cpu().numpy(), pr, f"partial {r}")
+    ref_lo, ref_rm, _ = oracle.merged_proj(x, wm, q, kv, tpm)
+    assert_close(bits_f64(to_bits(lo)), bits_f64(ref_lo), "merged logical")
+    assert np.array_equal(to_bits(rm), to_bits(lo)[:, oracle.rank_major_to_logical(q, kv, tpm)])
 
 
 @pytest.mark.parametrize("T,H,I", [(5, 16, 12), (3, 40, 24), (9, 100, 36), (130, 72, 48)])
