@@ -218,6 +218,26 @@ MSE_API int mse_set_kernel_path(int path);
 /* Prefill kernel selection, see mse_prefill_kernel.  Returns the previous value. */
 MSE_API int mse_set_prefill_kernel(int kind);
 
+/* Tuning of the decode-size (swap-AB) kernels, process-wide, for later launches.
+ *   MSE_TUNE_ISSUE_GROUP  consecutive 64-wide k-blocks per pipeline stage, i.e. each weight row
+ *                         is fetched in runs of 128 x value contiguous bytes (1..4, default 2)
+ *   MSE_TUNE_STAGES       shared-memory pipeline depth (0 = as many as fit, default)
+ *   MSE_TUNE_CACHE_HINTS  1 = weights evict-first / tokens evict-last in L2 (default), 0 = none
+ *   MSE_TUNE_GRID         CTAs of the stream-K grid (0 = CTAs per SM x SMs, default)
+ *   MSE_TUNE_CTAS_PER_SM  resident CTAs per SM of the stream-K grid (1 default, or 2)
+ *   MSE_TUNE_SPIN_WAIT    1 = pipeline waits poll (mbarrier.test_wait) instead of suspending
+ * Returns the previous value, or -1 for an unknown key or out-of-range value.
+ * Results do not depend on these settings beyond floating-point summation order. */
+typedef enum {
+    MSE_TUNE_ISSUE_GROUP = 1,
+    MSE_TUNE_STAGES = 2,
+    MSE_TUNE_CACHE_HINTS = 3,
+    MSE_TUNE_GRID = 4,
+    MSE_TUNE_CTAS_PER_SM = 5,
+    MSE_TUNE_SPIN_WAIT = 6
+} mse_tune_key;
+MSE_API int mse_set_tuning(int key, int value);
+
 /* Failure-detection self test: launches one CTA that waits on a barrier no one
  * arrives on, bounded by `limit_ns`.  The wait runs out by design; the kernel
  * records MSE_ERR_TIMEOUT in the device error word and returns, leaving the

@@ -22,13 +22,14 @@ __all__ = [
     "MSEError", "lib", "library_path", "mlp_swiglu_forward", "mlp_swiglu_shard_partial", "shard_sum",
     "merged_proj_forward", "merged_proj_reorder", "mlp_swiglu_workspace_bytes", "merged_proj_workspace_bytes",
     "poll_device_error", "set_wait_limit_ns", "get_wait_limit_ns", "set_kernel_path", "selftest_wait_timeout",
-    "set_phase_events", "set_prefill_kernel", "BF16", "F32", "PATH_AUTO", "PATH_GENERIC", "PATH_TENSORCORE",
+    "set_phase_events", "set_prefill_kernel", "set_tuning", "BF16", "F32", "PATH_AUTO", "PATH_GENERIC", "PATH_TENSORCORE",
     "PREFILL_AUTO", "PREFILL_SINGLE", "PREFILL_PAIR", "STATUS",
 ]
 
 BF16, F32 = 0, 1
 PATH_AUTO, PATH_GENERIC, PATH_TENSORCORE = 0, 1, 2
 PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR = 0, 1, 2
+TUNE_ISSUE_GROUP, TUNE_STAGES, TUNE_CACHE_HINTS, TUNE_GRID, TUNE_CTAS_PER_SM, TUNE_SPIN_WAIT = 1, 2, 3, 4, 5, 6
 STATUS = {
     0: "MSE_OK", 1: "MSE_ERR_INVALID_ARG", 2: "MSE_ERR_NOT_DIVISIBLE", 3: "MSE_ERR_GEOMETRY",
     4: "MSE_ERR_WORKSPACE", 5: "MSE_ERR_UNSUPPORTED_DEVICE", 6: "MSE_ERR_CUDA", 7: "MSE_ERR_TIMEOUT",
@@ -73,6 +74,7 @@ def lib() -> ctypes.CDLL:
                 "mse_get_wait_limit_ns": (u64, []),
                 "mse_set_kernel_path": (ci, [ci]),
                 "mse_set_prefill_kernel": (ci, [ci]),
+                "mse_set_tuning": (ci, [ci, ci]),
                 "mse_selftest_wait_timeout": (ci, [u64, P]),
                 "mse_set_phase_events": (None, [P, P, P]),
                 "mse_status_string": (ctypes.c_char_p, [ci]),
@@ -257,6 +259,10 @@ def get_wait_limit_ns() -> int:
 
 def set_kernel_path(path: int) -> int:
     return int(lib().mse_set_kernel_path(int(path)))
+
+
+def set_tuning(key: int, value: int) -> int:
+    return int(lib().mse_set_tuning(int(key), int(value)))
 
 
 def set_prefill_kernel(kind: int) -> int:

@@ -18,6 +18,8 @@ namespace {
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_path{MSE_PATH_AUTO};
 std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
+std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
+    g_tune_ctas_per_sm{1}, g_tune_spin_wait{0};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -208,9 +210,8 @@ mse_status map_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, 
 }
 
 // W_gate_up [2I x H] viewed as (k, j, half): one box = `rows` gate rows followed by
-// the `rows` up rows of the same j.  rows = 16 builds the swap-AB tile from four
-// boxes (each 32-row quarter pairs gate and up rows of 16 consecutive j); rows =
-// 128 gives the 256-row operand of the prefill kernel.
+// the `rows` up rows of the same j (rows = 128: the 256-row operand of the
+// single-CTA prefill kernel).
 mse_status map_gate_up_halves(CUtensorMap *m, const void *w, int64_t H, int64_t I, int rows) {
     const uint64_t dims[3] = {(uint64_t)H, (uint64_t)I, 2};
     const uint64_t strides[2] = {(uint64_t)H * 2, (uint64_t)I * H * 2};
@@ -223,7 +224,13 @@ tc::SwapAbParams swapab_base(int64_t T, int total_units) {
     tc::SwapAbParams p;
     std::memset(&p, 0, sizeof p);
     p.bn = round_up16(T);
-    p.stages = tc::swapab_stages_for(p.bn);
+    p.kbs = g_tune_issue_group.load();
+    int max_stages = tc::swapab_stages_for(p.bn, g_tune_ctas_per_sm.load(), p.kbs);
+    while (max_stages < 2 && p.kbs > 1) max_stages = tc::swapab_stages_for(p.bn, g_tune_ctas_per_sm.load(), --p.kbs);
+    const int want = g_tune_stages.load();
+    p.stages = (want >= 2 && want < max_stages) ? want : max_stages;
+    p.cache_hints = g_tune_cache_hints.load();
+    p.spin_wait = g_tune_spin_wait.load();
     p.tmem_cols = pow2_at_least(2 * p.bn);
     p.T = (int)T;
     p.total_units = total_units;
@@ -232,7 +239,10 @@ tc::SwapAbParams swapab_base(int64_t T, int total_units) {
 }
 
 int swapab_grid(const DeviceInfo &d, int total_units) {
-    int g = d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid;
+    const int per_sm = g_tune_ctas_per_sm.load() >= 2 ? 2 : 1;
+    int g = d.sm_count * per_sm < tc::kMaxGrid ? d.sm_count * per_sm : tc::kMaxGrid;
+    const int want = g_tune_grid.load();
+    if (want > 0 && want < g) g = want;
     return g < total_units ? g : total_units;
 }
 
@@ -253,12 +263,12 @@ bool use_pair(int64_t T) {
 }
 
 int pair_clusters(const DeviceInfo &d, int64_t n_tiles) {
-    int64_t c = (d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid) / 2;
+    int64_t c = (d.sm_count < tc::kMaxPersistentGrid ? d.sm_count : tc::kMaxPersistentGrid) / 2;
     return (int)(c < n_tiles ? c : n_tiles);
 }
 
 int std_grid(const DeviceInfo &d, int64_t n_tiles) {
-    int64_t g = d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid;
+    int64_t g = d.sm_count < tc::kMaxPersistentGrid ? d.sm_count : tc::kMaxPersistentGrid;
     return (int)(g < n_tiles ? g : n_tiles);
 }
 
@@ -272,7 +282,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         const int n_mtiles = (int)(width / 64);
         const int kbp = (int)(H / 64);
         tc::SwapAbParams p = swapab_base(T, n_mtiles * kbp);
-        if ((st = map_gate_up_halves(&ta, w_gate_up, H, I, 16)) != MSE_OK) return st;
+        if ((st = map_2d(&ta, w_gate_up, 2 * I, H, H, 64)) != MSE_OK) return st;
         if ((st = map_2d(&tb, x, T, H, H, p.bn)) != MSE_OK) return st;
         p.n_mtiles = n_mtiles;
         p.n_groups = 1;
@@ -280,6 +290,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         p.kb_first = 0;
         p.kb_group_stride = 0;
         p.a_row_base = (int)j_begin;
+        p.a_up_offset = (int)I;
         p.m_valid = 2 * width;
         p.out = h;
         p.ldo = I;
@@ -657,6 +668,22 @@ int mse_set_kernel_path(int path) {
 int mse_set_prefill_kernel(int kind) {
     if (kind < MSE_PREFILL_AUTO || kind > MSE_PREFILL_PAIR) return g_prefill.load();
     return g_prefill.exchange(kind);
+}
+
+int mse_set_tuning(int key, int value) {
+    std::atomic<int> *slot = nullptr;
+    bool ok = false;
+    switch (key) {
+        case MSE_TUNE_ISSUE_GROUP: slot = &g_tune_issue_group; ok = value >= 1 && value <= 4; break;
+        case MSE_TUNE_STAGES: slot = &g_tune_stages; ok = value == 0 || (value >= 2 && value <= tc::kMaxStages); break;
+        case MSE_TUNE_CACHE_HINTS: slot = &g_tune_cache_hints; ok = value == 0 || value == 1; break;
+        case MSE_TUNE_GRID: slot = &g_tune_grid; ok = value >= 0 && value <= tc::kMaxGrid; break;
+        case MSE_TUNE_CTAS_PER_SM: slot = &g_tune_ctas_per_sm; ok = value == 1 || value == 2; break;
+        case MSE_TUNE_SPIN_WAIT: slot = &g_tune_spin_wait; ok = value == 0 || value == 1; break;
+        default: return -1;
+    }
+    if (!ok) return -1;
+    return slot->exchange(value);
 }
 
 void mse_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end) {

@@ -73,16 +73,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-suspending probe of a phase (returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of `parity` to complete.  Gives up when the
 // CTA-wide abort flag is raised by another role, or after `limit_ns`; in the
 // latter case it raises the abort flag and the device error word.  Returns
 // false when it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                                  uint64_t limit_ns, uint32_t *err) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                                  uint64_t limit_ns, uint32_t *err, bool spin = false) {
+    if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (abort_flag && *abort_flag) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             if (abort_flag) *abort_flag = 1;
@@ -134,6 +147,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, 
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
         : "memory");
 }
+
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16), completion on an mbarrier
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+// order this thread's generic-proxy global accesses with later async-proxy (bulk copy) accesses
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;

@@ -6,7 +6,9 @@
 //
 // swapab_kernel: decode-sized token counts.  The weight rows fill the 128-row
 //   MMA M side and the tokens form N (<= 256), so each CTA streams weight tiles
-//   through a deep TMA ring.  Work is split stream-K over (group, m-tile,
+//   through a deep TMA ring, requesting several consecutive k-blocks back to back
+//   so that DRAM sees runs of >= 512 contiguous bytes per weight row.  Work is
+//   split stream-K over (group, m-tile,
 //   k-block) units so that every SM streams the same number of weight bytes;
 //   a tile cut between CTAs is finished by whichever CTA arrives last on the
 //   tile's counter (fp32 partial tiles in the workspace, summed in a fixed
@@ -15,6 +17,7 @@
 // std_kernel: prefill-sized token counts.  Persistent CTAs walk 128-token x
 //   256-column tiles over the full reduction with two TMEM accumulators, so the
 //   epilogue of one tile overlaps the MMA of the next.
+// pair_kernel: the same with a CTA pair (cta_group::2) per 256 x 256 tile.
 #include <atomic>
 
 #include "common.cuh"
@@ -25,7 +28,6 @@ namespace tc {
 namespace {
 
 constexpr uint32_t kATileBytes = 128 * 64 * 2;   // 128 rows x 64 bf16
-constexpr uint32_t kFull = 0xffffffffu;
 
 struct Ctrl {
     uint64_t full[kMaxStages];
@@ -33,9 +35,12 @@ struct Ctrl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t fixbar;         // swap-AB finisher: bulk copies of partial tiles into shared memory
     uint32_t tmem_base;
     int abort_flag;
     int fin_flag;
+    float xbuf[4][16][32];   // swap-AB SwiGLU epilogue: g/u exchange between lane quarters
+    int seg_slot[128];       // swap-AB split-K finisher: slot index of each part of the tile
 };
 
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t *b) { return smem_u32(b); }
@@ -67,28 +72,31 @@ struct StreamK {
 
 // Epilogue of one 16-token chunk of a swap-AB tile.  Thread `lane` of epilogue
 // warp quarter `q` holds accumulator row r = 32q + lane for tokens c*16 .. c*16+15.
+// All 128 epilogue threads call it together (it contains named barriers).
 template <int EPI>
-__device__ __forceinline__ void swapab_epilogue_chunk(const SwapAbParams &p, int group, int m, int q, int lane,
-                                                      int c, const float (&v)[16]) {
+__device__ __forceinline__ void swapab_epilogue_chunk(const SwapAbParams &p, Ctrl *ctl, int group, int m, int q,
+                                                      int lane, int c, const float (&v)[16]) {
     if constexpr (EPI == EPI_SWIGLU) {
-        // Rows of quarter q: lanes 0-15 hold gate rows j, lanes 16-31 the up rows of the
-        // same j (j = j0 + 16q + (lane & 15)).  Lane pairs (l, l+16) swap half of their
-        // tokens so that each computes silu(g) * u for 8 tokens.
-        float send[8], recv[8];
+        // Rows 0-63 are gate rows j = j0 + r, rows 64-127 the up rows of the same j, so
+        // quarter q (gate) pairs with quarter q ^ 2 (up).  The gate warp computes tokens
+        // 0-7 of the chunk and the up warp tokens 8-15, each reading its partner's half
+        // from shared memory.
 #pragma unroll
-        for (int i = 0; i < 8; ++i) send[i] = (lane < 16) ? v[8 + i] : v[i];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) recv[i] = __shfl_xor_sync(kFull, send[i], 16);
-        const int64_t j = (int64_t)p.a_row_base + (int64_t)m * 64 + q * 16 + (lane & 15);
-        const int t0 = c * 16 + ((lane < 16) ? 0 : 8);
+        for (int i = 0; i < 16; ++i) ctl->xbuf[q][i][lane] = v[i];
+        named_barrier_sync(1, 128);
+        const bool is_gate = q < 2;
+        const int pq = q ^ 2;
+        const int64_t j = (int64_t)p.a_row_base + (int64_t)m * 64 + 32 * (q & 1) + lane;
+        const int t0 = c * 16 + (is_gate ? 0 : 8);
         uint16_t *h = static_cast<uint16_t *>(p.out);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float g = (lane < 16) ? v[i] : recv[i];
-            const float u = (lane < 16) ? recv[i] : v[8 + i];
+            const float g = is_gate ? v[i] : ctl->xbuf[pq][8 + i][lane];
+            const float u = is_gate ? ctl->xbuf[pq][i][lane] : v[8 + i];
             const int t = t0 + i;
             if (t < p.T) h[(int64_t)t * p.ldo + j] = f32_to_bf16_bits(silu_f32(g) * u);
         }
+        named_barrier_sync(1, 128);   // xbuf is rewritten by the next chunk
     } else {
         const int64_t n = (int64_t)m * 128 + q * 32 + lane;
         if (n >= p.m_valid) return;
@@ -130,10 +138,14 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const int S = p.stages, bn = p.bn;
-    const uint32_t b_tile_bytes = (uint32_t)bn * 128u;
-    const uint32_t sA = base;
-    const uint32_t sB = base + (uint32_t)S * kATileBytes;
-    Ctrl *ctl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + (uint32_t)S * (kATileBytes + b_tile_bytes));
+    const int KBS = p.kbs;                                     // k-blocks per pipeline stage
+    const uint32_t b_tile_bytes = (uint32_t)bn * 128u;         // one k-block of tokens
+    const uint32_t a_stage_bytes = (uint32_t)KBS * kATileBytes;
+    const uint32_t stage_bytes = a_stage_bytes + (uint32_t)KBS * b_tile_bytes;
+    // stage s: [KBS weight tiles of 128 x 64][KBS token tiles of bn x 64]
+    auto sA = [&](int st) { return base + (uint32_t)st * stage_bytes; };
+    auto sB = [&](int st) { return base + (uint32_t)st * stage_bytes + a_stage_bytes; };
+    Ctrl *ctl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + (uint32_t)S * stage_bytes);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const StreamK sk{p.total_units, gridDim.x};
@@ -150,6 +162,7 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
             mbar_init(bar_addr(&ctl->tempty[b]), 128);
         }
         mbar_init(bar_addr(&ctl->drain), 1);
+        mbar_init(bar_addr(&ctl->fixbar), 1);
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
@@ -168,53 +181,112 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
     volatile int *abort_flag = &ctl->abort_flag;
     pdl_launch_dependents();
 
-    int64_t issued = 0;   // producer: k-blocks whose loads were issued
+    // The CTA's units [ub, ue) form segments (one per tile touched); each segment is cut
+    // into stages of up to KBS consecutive k-blocks.  Producer and MMA walk the same
+    // sequence with incremental counters (no divisions inside the loops).
+    struct Walk {
+        int64_t u, ue;
+        int kbp, n_mtiles;
+        int kb, kb_end, m, group;     // current stage starts at k-block kb of tile (group, m)
+        int seg;                      // segment index within this CTA
+        __device__ void init(int64_t ub_, int64_t ue_, int kbp_, int n_mtiles_) {
+            u = ub_; ue = ue_; kbp = kbp_; n_mtiles = n_mtiles_; seg = 0;
+            const int64_t tile = ub_ / kbp_;
+            kb = (int)(ub_ - tile * kbp_);
+            group = (int)(tile / n_mtiles_);
+            m = (int)(tile - (int64_t)group * n_mtiles_);
+            set_end();
+        }
+        __device__ void set_end() {
+            const int64_t rem = ue - u;
+            kb_end = (kbp - kb) < rem ? kbp : kb + (int)rem;
+        }
+        __device__ bool done() const { return u >= ue; }
+        // k-blocks of the current stage
+        __device__ int count(int kbs) const { return (kb_end - kb) < kbs ? (kb_end - kb) : kbs; }
+        // advance past a stage of n k-blocks; returns true when that stage ended its segment
+        __device__ bool advance(int n) {
+            kb += n;
+            u += n;
+            if (kb < kb_end) return false;
+            kb = 0;
+            ++seg;
+            if (++m == n_mtiles) { m = 0; ++group; }
+            set_end();
+            return true;
+        }
+    };
+
+    int issued = 0;   // producer: stages whose loads were issued
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
-            const int64_t n_items = ue - ub;
-            auto kglob = [&](int64_t u) {
-                const int64_t tile = u / kbp;
-                const int group = (int)(tile / p.n_mtiles);
-                return p.kb_first + group * p.kb_group_stride + (int)(u % kbp);
+            const bool hints = p.cache_hints != 0;
+            auto kglob = [&](const Walk &w, int i) { return p.kb_first + w.group * p.kb_group_stride + w.kb + i; };
+            auto load_a = [&](const Walk &w, int n, int st) {
+                const uint32_t fb = bar_addr(&ctl->full[st]);
+                for (int i = 0; i < n; ++i) {
+                    const int k = kglob(w, i) * 64;
+                    const uint32_t dst = sA(st) + (uint32_t)i * kATileBytes;
+                    if constexpr (EPI == EPI_SWIGLU) {
+                        // rows 0-63: gate rows j0..j0+63; rows 64-127: the up rows of the same j
+                        const int j0 = p.a_row_base + w.m * 64;
+                        if (hints) {
+                            tma_load_2d(dst, &tmA, fb, k, j0, pol_w);
+                            tma_load_2d(dst + 8192u, &tmA, fb, k, p.a_up_offset + j0, pol_w);
+                        } else {
+                            tma_load_2d_nohint(dst, &tmA, fb, k, j0);
+                            tma_load_2d_nohint(dst + 8192u, &tmA, fb, k, p.a_up_offset + j0);
+                        }
+                    } else {
+                        if (hints) tma_load_2d(dst, &tmA, fb, k, w.m * 128, pol_w);
+                        else tma_load_2d_nohint(dst, &tmA, fb, k, w.m * 128);
+                    }
+                }
             };
-            auto load_a = [&](int64_t u, int stage) {
-                const int64_t tile = u / kbp;
-                const int m = (int)(tile % p.n_mtiles);
-                const int k = kglob(u) * 64;
-                const uint32_t fb = bar_addr(&ctl->full[stage]);
-                if constexpr (EPI == EPI_SWIGLU) {
-                    // four 32-row quarters: 16 gate rows then the 16 up rows of the same j
-#pragma unroll
-                    for (int qq = 0; qq < 4; ++qq)
-                        tma_load_3d(sA + stage * kATileBytes + qq * 4096u, &tmA, fb, k, p.a_row_base + m * 64 + qq * 16,
-                                    0, pol_w);
-                } else
-                    tma_load_2d(sA + stage * kATileBytes, &tmA, fb, k, m * 128, pol_w);
+            auto load_b = [&](const Walk &w, int n, int st) {
+                const uint32_t fb = bar_addr(&ctl->full[st]);
+                for (int i = 0; i < n; ++i) {
+                    const int k = kglob(w, i) * 64;
+                    const uint32_t dst = sB(st) + (uint32_t)i * b_tile_bytes;
+                    if (hints) tma_load_2d(dst, &tmB, fb, k, 0, pol_x);
+                    else tma_load_2d_nohint(dst, &tmB, fb, k, 0);
+                }
             };
-            auto load_b = [&](int64_t u, int stage) {
-                tma_load_2d(sB + stage * b_tile_bytes, &tmB, bar_addr(&ctl->full[stage]), kglob(u) * 64, 0, pol_x);
-            };
-            // Prologue: weight tiles do not depend on the previous kernel, so they
-            // are requested before waiting for it; token tiles follow the wait.
-            const int64_t pro = n_items < S ? n_items : S;
-            for (int64_t i = 0; i < pro; ++i) {
-                mbar_arrive_expect_tx(bar_addr(&ctl->full[i]), kATileBytes + b_tile_bytes);
-                load_a(ub + i, (int)i);
+            Walk w;
+            w.init(ub, ue, kbp, p.n_mtiles);
+            // Prologue: weight tiles do not depend on the previous kernel, so they are
+            // requested before waiting for it; the token tiles follow the wait.
+            {
+                Walk a = w;
+                int st = 0;
+                for (; st < S && !a.done(); ++st) {
+                    const int n = a.count(KBS);
+                    mbar_arrive_expect_tx(bar_addr(&ctl->full[st]), (uint32_t)n * (kATileBytes + b_tile_bytes));
+                    load_a(a, n, st);
+                    a.advance(n);
+                }
+                pdl_wait();
+                for (int t = 0; t < st; ++t) {
+                    const int n = w.count(KBS);
+                    load_b(w, n, t);
+                    w.advance(n);
+                }
+                issued = st;
             }
-            pdl_wait();
-            for (int64_t i = 0; i < pro; ++i) load_b(ub + i, (int)i);
-            issued = pro;
-            int stage = (int)(pro % S);
-            uint32_t phase = (pro == S) ? 1u : 0u;
-            for (int64_t i = pro; i < n_items; ++i) {
-                if (!mbar_wait_bounded(bar_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns, p.err))
+            int stage = issued == S ? 0 : issued;
+            uint32_t phase = issued == S ? 1u : 0u;
+            while (!w.done()) {
+                if (!mbar_wait_bounded(bar_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns, p.err,
+                                       p.spin_wait != 0))
                     break;
-                mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), kATileBytes + b_tile_bytes);
-                load_a(ub + i, stage);
-                load_b(ub + i, stage);
+                const int n = w.count(KBS);
+                mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), (uint32_t)n * (kATileBytes + b_tile_bytes));
+                load_a(w, n, stage);
+                load_b(w, n, stage);
+                w.advance(n);
                 ++issued;
                 if (++stage == S) { stage = 0; phase ^= 1u; }
             }
@@ -224,15 +296,12 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
             const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)bn);
             int stage = 0;
             uint32_t phase = 0;
-            int seg = 0;
+            Walk w;
+            w.init(ub, ue, kbp, p.n_mtiles);
             bool ok = true;
-            for (int64_t u = ub; u < ue && ok; ++seg) {
-                const int64_t tile = u / kbp;
-                const int kb0 = (int)(u % kbp);
-                const int64_t rem = ue - u;
-                const int kb1 = (int)((kbp - kb0) < rem ? kbp : kb0 + rem);
-                const int buf = seg & 1;
-                const uint32_t use = (uint32_t)(seg >> 1);
+            while (!w.done() && ok) {
+                const int buf = w.seg & 1;
+                const uint32_t use = (uint32_t)(w.seg >> 1);
                 if (!mbar_wait_bounded(bar_addr(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, p.wait_limit_ns,
                                        p.err)) {
                     ok = false;
@@ -240,24 +309,30 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * (p.tmem_cols / 2));
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_bounded(bar_addr(&ctl->full[stage]), phase, abort_flag, p.wait_limit_ns, p.err)) {
+                bool first = true, seg_end = false;
+                while (!seg_end) {
+                    if (!mbar_wait_bounded(bar_addr(&ctl->full[stage]), phase, abort_flag, p.wait_limit_ns, p.err,
+                                           p.spin_wait != 0)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = smem_desc_sw128(sA + stage * kATileBytes);
-                    const uint64_t bd = smem_desc_sw128(sB + stage * b_tile_bytes);
+                    const int n = w.count(KBS);
+                    for (int i = 0; i < n; ++i) {
+                        const uint64_t ad = smem_desc_sw128(sA(stage) + (uint32_t)i * kATileBytes);
+                        const uint64_t bd = smem_desc_sw128(sB(stage) + (uint32_t)i * b_tile_bytes);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
-                                    (kb > kb0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            tc_mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, first ? 0u : 1u);
+                            first = false;
+                        }
+                    }
                     tc_commit(bar_addr(&ctl->empty[stage]));
                     if (++stage == S) { stage = 0; phase ^= 1u; }
+                    seg_end = w.advance(n);
                 }
                 if (!ok) break;
                 tc_commit(bar_addr(&ctl->tfull[buf]));
-                u = tile * kbp + kb1;
             }
         }
     } else {
@@ -267,6 +342,7 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         pdl_wait();
         int seg = 0;
+        uint32_t fix_round = 0;   // completed phases of fixbar
         for (int64_t u = ub; u < ue; ++seg) {
             const int64_t tile = u / kbp;
             const int kb0 = (int)(u % kbp);
@@ -286,7 +362,7 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
                 for (int c = 0; c < nchunks; ++c) {
                     float v[16];
                     load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
-                    swapab_epilogue_chunk<EPI>(p, group, m, q, lane, c, v);
+                    swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
                 }
                 tc_fence_before();
                 mbar_arrive(bar_addr(&ctl->tempty[buf]));
@@ -305,28 +381,96 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
             tc_fence_before();
             mbar_arrive(bar_addr(&ctl->tempty[buf]));
             __threadfence();
+            fence_proxy_async_global();   // a finisher may fetch this slot with a bulk copy
             named_barrier_sync(1, 128);
             const int64_t c_first = sk.owner(tile * kbp), c_last = sk.owner(tile * kbp + kbp - 1);
+            const int nseg = (int)(c_last - c_first + 1);
             if (threadIdx.x == 64) {
                 const int prev = atomicAdd(p.counters + tile, 1);
-                ctl->fin_flag = (prev == (int)(c_last - c_first)) ? 1 : 0;
+                ctl->fin_flag = (prev == nseg - 1) ? 1 : 0;
             }
             named_barrier_sync(1, 128);
             if (ctl->fin_flag) {
                 __threadfence();
-                for (int c = 0; c < nchunks; ++c) {
-                    float v[16] = {};
-                    for (int64_t cc = c_first; cc <= c_last; ++cc) {
-                        const int w = (sk.begin(cc) / kbp == tile) ? 0 : 1;
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            p.slots + ((size_t)cc * 2 + w) * (size_t)(128 * bn) + ((size_t)c * 128 + row) * 16);
+                // slot of each part: CTA cc's first segment uses slot 2cc, its last one 2cc+1
+                for (int k = threadIdx.x - 64; k < nseg && k < 128; k += 128) {
+                    const int64_t cc = c_first + k;
+                    ctl->seg_slot[k] = (int)(cc * 2 + ((sk.begin(cc) >= tile * kbp) ? 0 : 1));
+                }
+                named_barrier_sync(1, 128);
+                const size_t slot_floats = (size_t)128 * bn;
+                const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
+                const int per_round = (int)(((size_t)S * stage_bytes) / slot_bytes);
+                if (u == ue && per_round >= 2 && nseg <= 128) {
+                    // Last segment of this CTA: the pipeline's shared memory is idle, so the
+                    // parts are bulk-copied into it (buffer 0 keeps the running sum) and summed
+                    // there in ascending part order, one round trip per round.
+                    fence_proxy_async_global();
+                    const float *buf0 = reinterpret_cast<const float *>(smem_raw + (base - raw));
+                    bool fix_ok = true;
+                    int k0 = 0;
+                    while (k0 < nseg) {
+                        const int first_buf = k0 == 0 ? 0 : 1;
+                        const int nload = min(nseg - k0, per_round - first_buf);
+                        if (threadIdx.x == 64) {
+                            mbar_arrive_expect_tx(bar_addr(&ctl->fixbar), (uint32_t)nload * slot_bytes);
+                            for (int i = 0; i < nload; ++i)
+                                bulk_load(base + (uint32_t)(first_buf + i) * slot_bytes,
+                                          p.slots + (size_t)ctl->seg_slot[k0 + i] * slot_floats, slot_bytes,
+                                          bar_addr(&ctl->fixbar));
+                        }
+                        const bool got_fix = mbar_wait_bounded(bar_addr(&ctl->fixbar), fix_round & 1u, abort_flag,
+                                                               p.wait_limit_ns, p.err);
+                        ++fix_round;
+                        if (!named_barrier_and(1, 128, got_fix)) { fix_ok = false; break; }
+                        // buffer 0 += buffers first_buf.. (own row only: no cross-thread hazards)
+                        const int nsum = first_buf + nload;
+                        if (nsum > 1 || k0 == 0) {
+                            for (int c = 0; c < nchunks; ++c) {
+                                const size_t off = ((size_t)c * 128 + row) * 16;
+                                float4 *dst = reinterpret_cast<float4 *>(const_cast<float *>(buf0) + off);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float4 a = __ldcg(src + i);
-                            v[4 * i] += a.x; v[4 * i + 1] += a.y; v[4 * i + 2] += a.z; v[4 * i + 3] += a.w;
+                                for (int i = 0; i < 4; ++i) {
+                                    float4 a = k0 == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : dst[i];
+                                    for (int b = (k0 == 0 ? 0 : 1); b < nsum; ++b) {
+                                        const float4 t = reinterpret_cast<const float4 *>(buf0 + (size_t)b * slot_floats + off)[i];
+                                        a.x += t.x; a.y += t.y; a.z += t.z; a.w += t.w;
+                                    }
+                                    dst[i] = a;
+                                }
+                            }
+                        }
+                        k0 += nload;
+                        named_barrier_sync(1, 128);   // buffers 1.. are refilled by the next round
+                    }
+                    if (fix_ok) {
+                        for (int c = 0; c < nchunks; ++c) {
+                            const float4 *src = reinterpret_cast<const float4 *>(buf0 + ((size_t)c * 128 + row) * 16);
+                            float v[16];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float4 a = src[i];
+                                v[4 * i] = a.x; v[4 * i + 1] = a.y; v[4 * i + 2] = a.z; v[4 * i + 3] = a.w;
+                            }
+                            swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
                         }
                     }
-                    swapab_epilogue_chunk<EPI>(p, group, m, q, lane, c, v);
+                } else {
+                    for (int c = 0; c < nchunks; ++c) {
+                        float v[16] = {};
+                        const size_t off = ((size_t)c * 128 + row) * 16;
+                        for (int k = 0; k < nseg; ++k) {
+                            const int sl = k < 128 ? ctl->seg_slot[k]
+                                                   : (int)((c_first + k) * 2 + ((sk.begin(c_first + k) >= tile * kbp) ? 0 : 1));
+                            const float4 *src = reinterpret_cast<const float4 *>(p.slots + (size_t)sl * slot_floats + off);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float4 a = __ldcg(src + i);
+                                v[4 * i] += a.x; v[4 * i + 1] += a.y; v[4 * i + 2] += a.z; v[4 * i + 3] += a.w;
+                            }
+                        }
+                        swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
+                    }
                 }
                 if (threadIdx.x == 64) p.counters[tile] = 0;
             }
@@ -336,12 +480,9 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
 
     // ---- teardown: drain in-flight copies and MMAs, then free tensor memory ----
     if (warp == 0 && lane == 0) {
-        const int64_t first = issued > S ? issued - S : 0;
-        for (int64_t i = first; i < issued; ++i) {
-            const int st = (int)(i % S);
-            const uint32_t par = (uint32_t)((i / S) & 1);
-            (void)mbar_wait_drain(bar_addr(&ctl->full[st]), par, p.wait_limit_ns);
-        }
+        const int first = issued > S ? issued - S : 0;
+        for (int i = first; i < issued; ++i)
+            (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1), p.wait_limit_ns);
     }
     if (warp == 1 && lane == 0) {
         tc_commit(bar_addr(&ctl->drain));
@@ -817,21 +958,22 @@ cudaError_t ensure_smem_attr(Kern kern, int slot) {
 
 }  // namespace
 
-size_t swapab_smem_bytes(int bn, int stages) {
-    return (size_t)stages * (kATileBytes + (size_t)bn * 128) + 1024 + sizeof(Ctrl);
+size_t swapab_smem_bytes(int bn, int stages, int kbs) {
+    return (size_t)stages * kbs * (kATileBytes + (size_t)bn * 128) + 1024 + sizeof(Ctrl);
 }
 size_t std_smem_bytes(int stages) { return (size_t)stages * (kATileBytes + kStdBTileBytes) + 1024 + sizeof(Ctrl); }
 
-int swapab_stages_for(int bn) {
-    const size_t budget = 227 * 1024 - 1024 - sizeof(Ctrl) - 64;
-    int st = (int)(budget / (kATileBytes + (size_t)bn * 128));
+int swapab_stages_for(int bn, int ctas_per_sm, int kbs) {
+    const size_t per_cta = ctas_per_sm >= 2 ? 113 * 1024 : 227 * 1024;
+    const size_t budget = per_cta - 1024 - sizeof(Ctrl) - 64;
+    int st = (int)(budget / ((size_t)kbs * (kATileBytes + (size_t)bn * 128)));
     return st > kMaxStages ? kMaxStages : st;
 }
 int std_stages() { return 4; }
 
 cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
                           bool pdl, cudaStream_t s) {
-    const size_t smem = swapab_smem_bytes(p.bn, p.stages);
+    const size_t smem = swapab_smem_bytes(p.bn, p.stages, p.kbs);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)kSwapAbThreads);

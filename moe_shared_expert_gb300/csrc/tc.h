@@ -27,6 +27,11 @@ struct SwapAbParams {
     int stages;            // smem pipeline depth
     int tmem_cols;         // allocated TMEM columns (power of two >= 2*bn)
     int a_row_base;        // SWIGLU: first intermediate index j of tile 0 (multiple of 64)
+    int a_up_offset;       // SWIGLU: row offset of the up half in W_gate_up (= I)
+    int kbs;               // consecutive k-blocks per pipeline stage (each weight row is fetched
+                           // kbs x 128 contiguous bytes at a time; DRAM row-buffer locality)
+    int cache_hints;       // 1: weights evict_first, tokens evict_last in L2; 0: no hints
+    int spin_wait;         // 1: pipeline waits poll without suspending the thread
     int T;                 // valid tokens
     int64_t m_valid;       // valid output features (A rows) for masking
     void *out; int64_t ldo; int64_t o_group_stride;
@@ -61,14 +66,15 @@ struct StdParams {
 constexpr int kSwapAbThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kStdThreads = 192;
 constexpr int kMaxStages = 12;
-constexpr int kMaxGrid = 160;         // cap on persistent / stream-K grids
+constexpr int kMaxGrid = 320;         // cap on stream-K grids (up to 2 CTAs per SM)
+constexpr int kMaxPersistentGrid = 160; // cap on the persistent prefill grids
 
 // Dynamic shared memory of the kernels.
-size_t swapab_smem_bytes(int bn, int stages);
+size_t swapab_smem_bytes(int bn, int stages, int kbs);
 size_t std_smem_bytes(int stages);
 size_t pair_smem_bytes(int stages);
 int pair_stages();
-int swapab_stages_for(int bn);
+int swapab_stages_for(int bn, int ctas_per_sm, int kbs);
 int std_stages();
 
 cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
