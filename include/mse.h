@@ -198,6 +198,36 @@ MSE_API mse_status merged_proj_reorder(const mse_bf16 *rank_major, mse_bf16 *log
                                void *stream);
 
 /* ---------------------------------------------------------------------------
+ * mlp_swiglu_forward for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a deployment convenience of this library.
+ *
+ * Some callers hold only their input and output buffers and have no way to
+ * obtain scratch memory: custom-operator interfaces of inference runtimes that
+ * pass tensors but no workspace, or code that must not call the CUDA allocator
+ * at all (cudaMalloc can synchronise the device and fail under memory pressure).
+ * This entry point computes exactly what mlp_swiglu_forward computes, with the
+ * same arguments minus the workspace: its scratch (h, split-K partial tiles,
+ * tile counters) is a fixed 12 MiB file-scope device array inside the library,
+ * which every device that loads the library holds until the process exits.
+ *
+ *  - Limit: mlp_swiglu_workspace_bytes(T, H, I) <= 12 MiB, e.g. T <= 64 tokens
+ *    at hidden 7168 / intermediate 6144.  Larger calls return MSE_ERR_WORKSPACE
+ *    and launch nothing.
+ *  - It calls no cudaMalloc, cudaFree or allocating library routine.
+ *  - The first call on a device performs a one-time set-up on that device
+ *    (it looks up the array's device address with cudaGetSymbolAddress); make
+ *    that first call before any stream capture.
+ *  - Every call on a device shares the one array, and the array keeps the last
+ *    call's contents (each call clears the tile counters it needs on `stream`).
+ *    Calls whose executions overlap on the GPU (different streams, or several
+ *    host threads without ordering) race on the array and give wrong results;
+ *    order them on one stream.
+ * ------------------------------------------------------------------------- */
+MSE_API mse_status mlp_swiglu_forward_static_scratch(const mse_bf16 *x, int64_t T, int64_t H, int64_t I,
+                                                     const mse_bf16 *w_gate_up, const mse_bf16 *w_down,
+                                                     mse_bf16 *y, int64_t y_capacity, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Errors raised on the device and process-wide settings.
  * ------------------------------------------------------------------------- */
 
@@ -223,8 +253,7 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         is fetched in runs of 128 x value contiguous bytes (1..4, default 2)
  *   MSE_TUNE_STAGES       shared-memory pipeline depth (0 = as many as fit, default)
  *   MSE_TUNE_CACHE_HINTS  1 = weights evict-first / tokens evict-last in L2 (default), 0 = none
- *   MSE_TUNE_GRID         CTAs of the stream-K grid (0 = CTAs per SM x SMs, default)
- *   MSE_TUNE_CTAS_PER_SM  resident CTAs per SM of the stream-K grid (1 default, or 2)
+ *   MSE_TUNE_GRID         CTAs of the stream-K grid (0 = one per SM, default; at most 160)
  *   MSE_TUNE_SPIN_WAIT    1 = pipeline waits poll (mbarrier.test_wait) instead of suspending
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
@@ -233,7 +262,6 @@ typedef enum {
     MSE_TUNE_STAGES = 2,
     MSE_TUNE_CACHE_HINTS = 3,
     MSE_TUNE_GRID = 4,
-    MSE_TUNE_CTAS_PER_SM = 5,
     MSE_TUNE_SPIN_WAIT = 6
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);

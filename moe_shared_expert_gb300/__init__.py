@@ -29,7 +29,7 @@ __all__ = [
 BF16, F32 = 0, 1
 PATH_AUTO, PATH_GENERIC, PATH_TENSORCORE = 0, 1, 2
 PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR = 0, 1, 2
-TUNE_ISSUE_GROUP, TUNE_STAGES, TUNE_CACHE_HINTS, TUNE_GRID, TUNE_CTAS_PER_SM, TUNE_SPIN_WAIT = 1, 2, 3, 4, 5, 6
+TUNE_ISSUE_GROUP, TUNE_STAGES, TUNE_CACHE_HINTS, TUNE_GRID, TUNE_SPIN_WAIT = 1, 2, 3, 4, 6
 STATUS = {
     0: "MSE_OK", 1: "MSE_ERR_INVALID_ARG", 2: "MSE_ERR_NOT_DIVISIBLE", 3: "MSE_ERR_GEOMETRY",
     4: "MSE_ERR_WORKSPACE", 5: "MSE_ERR_UNSUPPORTED_DEVICE", 6: "MSE_ERR_CUDA", 7: "MSE_ERR_TIMEOUT",
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
                 "shard_sum": (ci, [P, ci, ci, i64, i64, P, i64, P]),
                 "merged_proj_forward": (ci, [P, i64, i64, P, i64, i64, ci, P, P, i64, P, sz, P]),
                 "merged_proj_reorder": (ci, [P, P, i64, i64, i64, ci, i64, P]),
+                "mlp_swiglu_forward_static_scratch": (ci, [P, i64, i64, i64, P, P, P, i64, P]),
                 "mse_poll_device_error": (ci, [P]),
                 "mse_set_wait_limit_ns": (None, [u64]),
                 "mse_get_wait_limit_ns": (u64, []),

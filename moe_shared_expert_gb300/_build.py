@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmse.so")
-SOURCES = ["api.cu", "tc.cu", "simt.cu", "elementwise.cu"]
+SOURCES = ["api.cu", "tc.cu", "simt.cu", "elementwise.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

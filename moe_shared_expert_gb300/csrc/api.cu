@@ -19,7 +19,7 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_path{MSE_PATH_AUTO};
 std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
-    g_tune_ctas_per_sm{1}, g_tune_spin_wait{0};
+    g_tune_spin_wait{0};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -225,8 +225,8 @@ tc::SwapAbParams swapab_base(int64_t T, int total_units) {
     std::memset(&p, 0, sizeof p);
     p.bn = round_up16(T);
     p.kbs = g_tune_issue_group.load();
-    int max_stages = tc::swapab_stages_for(p.bn, g_tune_ctas_per_sm.load(), p.kbs);
-    while (max_stages < 2 && p.kbs > 1) max_stages = tc::swapab_stages_for(p.bn, g_tune_ctas_per_sm.load(), --p.kbs);
+    int max_stages = tc::swapab_stages_for(p.bn, p.kbs);
+    while (max_stages < 2 && p.kbs > 1) max_stages = tc::swapab_stages_for(p.bn, --p.kbs);
     const int want = g_tune_stages.load();
     p.stages = (want >= 2 && want < max_stages) ? want : max_stages;
     p.cache_hints = g_tune_cache_hints.load();
@@ -239,8 +239,7 @@ tc::SwapAbParams swapab_base(int64_t T, int total_units) {
 }
 
 int swapab_grid(const DeviceInfo &d, int total_units) {
-    const int per_sm = g_tune_ctas_per_sm.load() >= 2 ? 2 : 1;
-    int g = d.sm_count * per_sm < tc::kMaxGrid ? d.sm_count * per_sm : tc::kMaxGrid;
+    int g = d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid;
     const int want = g_tune_grid.load();
     if (want > 0 && want < g) g = want;
     return g < total_units ? g : total_units;
@@ -429,6 +428,19 @@ void record(std::atomic<void *> &ev, cudaStream_t s) {
 }  // namespace
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+// Byte range of the split-K tile counters inside an mlp workspace (they must be zero
+// before a call); bytes = 0 when the layout has none.
+void mlp_workspace_counter_range(int64_t T, int64_t H, int64_t I, size_t *off, size_t *bytes) {
+    const MlpWs L = mlp_ws_layout(T, H, I);
+    if (L.cnt_gu_off == 0) {
+        *off = 0;
+        *bytes = 0;
+        return;
+    }
+    *off = L.cnt_gu_off;
+    *bytes = L.total - L.cnt_gu_off;
+}
 
 }  // namespace mse
 
@@ -678,7 +690,6 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_STAGES: slot = &g_tune_stages; ok = value == 0 || (value >= 2 && value <= tc::kMaxStages); break;
         case MSE_TUNE_CACHE_HINTS: slot = &g_tune_cache_hints; ok = value == 0 || value == 1; break;
         case MSE_TUNE_GRID: slot = &g_tune_grid; ok = value >= 0 && value <= tc::kMaxGrid; break;
-        case MSE_TUNE_CTAS_PER_SM: slot = &g_tune_ctas_per_sm; ok = value == 1 || value == 2; break;
         case MSE_TUNE_SPIN_WAIT: slot = &g_tune_spin_wait; ok = value == 0 || value == 1; break;
         default: return -1;
     }

@@ -963,9 +963,8 @@ size_t swapab_smem_bytes(int bn, int stages, int kbs) {
 }
 size_t std_smem_bytes(int stages) { return (size_t)stages * (kATileBytes + kStdBTileBytes) + 1024 + sizeof(Ctrl); }
 
-int swapab_stages_for(int bn, int ctas_per_sm, int kbs) {
-    const size_t per_cta = ctas_per_sm >= 2 ? 113 * 1024 : 227 * 1024;
-    const size_t budget = per_cta - 1024 - sizeof(Ctrl) - 64;
+int swapab_stages_for(int bn, int kbs) {
+    const size_t budget = 227 * 1024 - 1024 - sizeof(Ctrl) - 64;
     int st = (int)(budget / ((size_t)kbs * (kATileBytes + (size_t)bn * 128)));
     return st > kMaxStages ? kMaxStages : st;
 }

@@ -66,7 +66,7 @@ struct StdParams {
 constexpr int kSwapAbThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kStdThreads = 192;
 constexpr int kMaxStages = 12;
-constexpr int kMaxGrid = 320;         // cap on stream-K grids (up to 2 CTAs per SM)
+constexpr int kMaxGrid = 160;         // cap on stream-K grids (one CTA per SM)
 constexpr int kMaxPersistentGrid = 160; // cap on the persistent prefill grids
 
 // Dynamic shared memory of the kernels.
@@ -74,7 +74,7 @@ size_t swapab_smem_bytes(int bn, int stages, int kbs);
 size_t std_smem_bytes(int stages);
 size_t pair_smem_bytes(int stages);
 int pair_stages();
-int swapab_stages_for(int bn, int ctas_per_sm, int kbs);
+int swapab_stages_for(int bn, int kbs);
 int std_stages();
 
 cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
