@@ -18,6 +18,7 @@ need more than one GPU), timed between barriers, max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -418,16 +419,21 @@ def gpu_arm(args):
     clocks = ClockSampler(dist.local) if dist.rank == 0 else None
 
     w = W.DECODE_T64
-    t_w0 = time.time()
-    r = bench_mlp(w, args.steps, args.warmup, args.layers, dist, clocks=clocks)
-    dev_s = dist.max(r["dev_s"])
-    e2e_s = dist.max(r["e2e_s"])
-    if clocks:
-        clocks.mark("decode.all", t_w0, time.time())
-
     extra = {}
-    if not args.decode_only:
+    if args.only == "prefill":
+        r = None
+    else:
+        t_w0 = time.time()
+        r = bench_mlp(w, args.steps, args.warmup, args.layers, dist, clocks=clocks)
+        dev_s = dist.max(r["dev_s"])
+        e2e_s = dist.max(r["e2e_s"])
+        if clocks:
+            clocks.mark("decode.all", t_w0, time.time())
+
+    if args.only != "decode":
         wp = W.PREFILL_T8192
+        if args.prefill_tokens != wp.T:
+            wp = dataclasses.replace(wp, T=args.prefill_tokens, name=f"prefill_t{args.prefill_tokens}")
         t_p0 = time.time()
         rp = bench_mlp(wp, args.prefill_steps, max(3, min(args.warmup, 5)), 2, dist, clocks=clocks,
                        phase_steps=min(10, args.prefill_steps), e2e_steps=0)
@@ -436,7 +442,7 @@ def gpu_arm(args):
         ps = dist.max(rp["dev_s"]) / args.prefill_steps
         gu_fl = gate_up_flops(wp.T, wp.H, wp.I)
         ach = gu_fl / (rp["gate_up_ms"] * 1e-3) / 1e12
-        extra["prefill_t8192"] = {
+        extra[wp.name] = {
             "ms_per_layer": ps * 1e3, "tflops": mlp_flops(wp.T, wp.H, wp.I) / ps / 1e12,
             "frac_of_bf16_peak": mlp_flops(wp.T, wp.H, wp.I) / ps / 1e12 / peaks["bf16_tflops_sustained"],
             "gate_up_ms": rp["gate_up_ms"], "down_ms": rp["down_ms"],
@@ -445,6 +451,7 @@ def gpu_arm(args):
                          "peak_kind": f"burst bf16 ({peaks['source']})"},
             "gpu_launches": 2 * args.prefill_steps,
         }
+    if args.only == "all":
         w3 = W.TP8_EMULATED
         s3 = bench_tp8(w3, args.aux_steps, args.warmup, args.layers)
         b3 = mlp_bytes(w3.T, w3.H, w3.I)
@@ -463,6 +470,16 @@ def gpu_arm(args):
         clocks.stop()
 
     if dist.rank != 0:
+        dist.done()
+        return
+    if r is None:   # prefill only: report the prefill measurement as the line
+        pf = extra[wp.name]
+        line = {"metric": METRIC, "value": pf["tflops"], "unit": "TFLOP/s", "n_gpus": dist.world,
+                "steps": args.prefill_steps, "warmup": args.warmup, "ms_per_step": pf["ms_per_layer"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": wp.name, "T": wp.T, "H": wp.H, "I": wp.I},
+                "roofline": pf["roofline"], "gpu_launches": pf["gpu_launches"]}
+        print(json.dumps(line), flush=True)
         dist.done()
         return
     N = dist.world
@@ -565,12 +582,16 @@ def main():
     ap.add_argument("--layers", type=int, default=4, help="distinct weight copies cycled")
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--aux-steps", type=int, default=2000)
-    ap.add_argument("--decode-only", action="store_true")
+    ap.add_argument("--decode-only", action="store_true", help="same as --only decode")
+    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill"])
+    ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.decode_only:
+        args.only = "decode"
     if args.impl == "reference":
         reference_arm(args)
     else:

@@ -245,7 +245,17 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
 // ---------------------------------------------------------------------------
 // math used by the epilogues
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+// silu(g) = g / (1 + e^-g) with the hardware exponential and the fast division
+// intrinsic (about 2 ulp; h is rounded to bf16 afterwards).  For g < -88 the
+// denominator overflows and the quotient is -0, the correct limit.
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// atomic add at GPU scope with acquire-release semantics; returns the old value
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
 
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
     __nv_bfloat16 b = __float2bfloat16_rn(v);

@@ -76,6 +76,9 @@ struct StreamK {
 template <int EPI>
 __device__ __forceinline__ void swapab_epilogue_chunk(const SwapAbParams &p, Ctrl *ctl, int group, int m, int q,
                                                       int lane, int c, const float (&v)[16]) {
+    // Results are computed for every token before any store (branch-free, so the
+    // independent chains interleave); the stores are unpredicated when the whole
+    // chunk is inside T.
     if constexpr (EPI == EPI_SWIGLU) {
         // Rows 0-63 are gate rows j = j0 + r, rows 64-127 the up rows of the same j, so
         // quarter q (gate) pairs with quarter q ^ 2 (up).  The gate warp computes tokens
@@ -88,43 +91,113 @@ __device__ __forceinline__ void swapab_epilogue_chunk(const SwapAbParams &p, Ctr
         const int pq = q ^ 2;
         const int64_t j = (int64_t)p.a_row_base + (int64_t)m * 64 + 32 * (q & 1) + lane;
         const int t0 = c * 16 + (is_gate ? 0 : 8);
-        uint16_t *h = static_cast<uint16_t *>(p.out);
+        uint16_t hv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float g = is_gate ? v[i] : ctl->xbuf[pq][8 + i][lane];
             const float u = is_gate ? ctl->xbuf[pq][i][lane] : v[8 + i];
-            const int t = t0 + i;
-            if (t < p.T) h[(int64_t)t * p.ldo + j] = f32_to_bf16_bits(silu_f32(g) * u);
+            hv[i] = f32_to_bf16_bits(silu_f32(g) * u);
         }
         named_barrier_sync(1, 128);   // xbuf is rewritten by the next chunk
+        uint16_t *h = static_cast<uint16_t *>(p.out) + (int64_t)t0 * p.ldo + j;
+        if (t0 + 8 <= p.T) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[(int64_t)i * p.ldo] = hv[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (t0 + i < p.T) h[(int64_t)i * p.ldo] = hv[i];
+        }
     } else {
         const int64_t n = (int64_t)m * 128 + q * 32 + lane;
         if (n >= p.m_valid) return;
+        const int t0 = c * 16;
+        const int nt = min(16, p.T - t0);
         if constexpr (EPI == EPI_F32) {
-            float *o = static_cast<float *>(p.out) + group * p.o_group_stride;
+            float *o = static_cast<float *>(p.out) + group * p.o_group_stride + (int64_t)t0 * p.ldo + n;
+            if (nt == 16) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = c * 16 + i;
-                if (t < p.T) o[(int64_t)t * p.ldo + n] = v[i];
+                for (int i = 0; i < 16; ++i) o[(int64_t)i * p.ldo] = v[i];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (i < nt) o[(int64_t)i * p.ldo] = v[i];
             }
+        } else {
+            uint16_t b[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) b[i] = f32_to_bf16_bits(v[i]);
+            if constexpr (EPI == EPI_BF16) {
+                uint16_t *o = static_cast<uint16_t *>(p.out) + group * p.o_group_stride + (int64_t)t0 * p.ldo + n;
+                if (nt == 16) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[(int64_t)i * p.ldo] = b[i];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i < nt) o[(int64_t)i * p.ldo] = b[i];
+                }
+            } else {  // EPI_MERGED
+                uint16_t *lo = static_cast<uint16_t *>(p.out);
+                const int64_t gcol = logical_to_gathered(n, p.q_dim, p.kv_dim, p.tp);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (i < nt) {
+                        if (lo) lo[(int64_t)(t0 + i) * p.ldo + n] = b[i];
+                        if (p.out_rm) p.out_rm[(int64_t)(t0 + i) * p.ldo + gcol] = b[i];
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Epilogue of a whole swap-AB tile held in shared memory as fp32 [token][row]
+// (row = accumulator row, 128 per token).  All 128 epilogue threads (tid 0..127)
+// work element-wise: a fixed row per thread, tokens strided, so shared reads are
+// conflict-free and the 32 lanes of a warp store 32 consecutive outputs.
+template <int EPI>
+__device__ __forceinline__ void swapab_epilogue_smem(const SwapAbParams &p, const float *tilebuf, int group, int m,
+                                                     int tid) {
+    if constexpr (EPI == EPI_SWIGLU) {
+        // rows 0-63: g of j = j0 + r; rows 64-127: u of the same j
+        const int jr = tid & 63;
+        uint16_t *h = static_cast<uint16_t *>(p.out) + (int64_t)p.a_row_base + (int64_t)m * 64 + jr;
+        int t = tid >> 6;
+        for (; t + 6 < p.T; t += 8) {   // 4 tokens per step, computed before storing
+            uint16_t hv[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                hv[r] = f32_to_bf16_bits(silu_f32(tilebuf[(t + 2 * r) * 128 + jr]) * tilebuf[(t + 2 * r) * 128 + 64 + jr]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) h[(int64_t)(t + 2 * r) * p.ldo] = hv[r];
+        }
+        for (; t < p.T; t += 2)
+            h[(int64_t)t * p.ldo] = f32_to_bf16_bits(silu_f32(tilebuf[t * 128 + jr]) * tilebuf[t * 128 + 64 + jr]);
+    } else {
+        const int64_t n = (int64_t)m * 128 + tid;
+        if (n >= p.m_valid) return;
+        if constexpr (EPI == EPI_F32) {
+            float *o = static_cast<float *>(p.out) + group * p.o_group_stride + n;
+            for (int t = 0; t < p.T; ++t) o[(int64_t)t * p.ldo] = tilebuf[t * 128 + tid];
         } else if constexpr (EPI == EPI_BF16) {
-            uint16_t *o = static_cast<uint16_t *>(p.out) + group * p.o_group_stride;
+            uint16_t *o = static_cast<uint16_t *>(p.out) + group * p.o_group_stride + n;
+            int t = 0;
+            for (; t + 3 < p.T; t += 4) {
+                uint16_t b[4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = c * 16 + i;
-                if (t < p.T) o[(int64_t)t * p.ldo + n] = f32_to_bf16_bits(v[i]);
+                for (int r = 0; r < 4; ++r) b[r] = f32_to_bf16_bits(tilebuf[(t + r) * 128 + tid]);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) o[(int64_t)(t + r) * p.ldo] = b[r];
             }
-        } else {  // EPI_MERGED
+            for (; t < p.T; ++t) o[(int64_t)t * p.ldo] = f32_to_bf16_bits(tilebuf[t * 128 + tid]);
+        } else {
             uint16_t *lo = static_cast<uint16_t *>(p.out);
             const int64_t gcol = logical_to_gathered(n, p.q_dim, p.kv_dim, p.tp);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = c * 16 + i;
-                if (t < p.T) {
-                    const uint16_t b = f32_to_bf16_bits(v[i]);
-                    if (lo) lo[(int64_t)t * p.ldo + n] = b;
-                    if (p.out_rm) p.out_rm[(int64_t)t * p.ldo + gcol] = b;
-                }
+            for (int t = 0; t < p.T; ++t) {
+                const uint16_t b = f32_to_bf16_bits(tilebuf[t * 128 + tid]);
+                if (lo) lo[(int64_t)t * p.ldo + n] = b;
+                if (p.out_rm) p.out_rm[(int64_t)t * p.ldo + gcol] = b;
             }
         }
     }
@@ -368,30 +441,30 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
                 mbar_arrive(bar_addr(&ctl->tempty[buf]));
                 continue;
             }
-            // Tile shared with other CTAs: park the fp32 partial in this CTA's slot.
+            // Tile shared with other CTAs: park the fp32 partial in this CTA's slot, laid
+            // out [token column][accumulator row] (each warp store is a 128-byte run).
             const int which = (sk.begin(blockIdx.x) / kbp == tile) ? 0 : 1;
             float *slot = p.slots + ((size_t)blockIdx.x * 2 + which) * (size_t)(128 * bn);
             for (int c = 0; c < nchunks; ++c) {
                 float v[16];
                 load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
-                float4 *dst = reinterpret_cast<float4 *>(slot + ((size_t)c * 128 + row) * 16);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                for (int i = 0; i < 16; ++i) __stcg(slot + (size_t)(c * 16 + i) * 128 + row, v[i]);
             }
             tc_fence_before();
             mbar_arrive(bar_addr(&ctl->tempty[buf]));
-            __threadfence();
             fence_proxy_async_global();   // a finisher may fetch this slot with a bulk copy
             named_barrier_sync(1, 128);
             const int64_t c_first = sk.owner(tile * kbp), c_last = sk.owner(tile * kbp + kbp - 1);
             const int nseg = (int)(c_last - c_first + 1);
             if (threadIdx.x == 64) {
-                const int prev = atomicAdd(p.counters + tile, 1);
+                // release: the barrier above orders every epilogue thread's slot stores
+                // before this atomic; acquire: the finisher then sees all other parts
+                const int prev = atomic_add_acq_rel_gpu(p.counters + tile, 1);
                 ctl->fin_flag = (prev == nseg - 1) ? 1 : 0;
             }
             named_barrier_sync(1, 128);
             if (ctl->fin_flag) {
-                __threadfence();
                 // slot of each part: CTA cc's first segment uses slot 2cc, its last one 2cc+1
                 for (int k = threadIdx.x - 64; k < nseg && k < 128; k += 128) {
                     const int64_t cc = c_first + k;
@@ -401,12 +474,13 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
                 const size_t slot_floats = (size_t)128 * bn;
                 const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
                 const int per_round = (int)(((size_t)S * stage_bytes) / slot_bytes);
+                const int tid = threadIdx.x - 64;
                 if (u == ue && per_round >= 2 && nseg <= 128) {
                     // Last segment of this CTA: the pipeline's shared memory is idle, so the
                     // parts are bulk-copied into it (buffer 0 keeps the running sum) and summed
-                    // there in ascending part order, one round trip per round.
+                    // element-wise in ascending part order starting from 0, as the fallback does.
                     fence_proxy_async_global();
-                    const float *buf0 = reinterpret_cast<const float *>(smem_raw + (base - raw));
+                    float *buf0 = reinterpret_cast<float *>(smem_raw + (base - raw));
                     bool fix_ok = true;
                     int k0 = 0;
                     while (k0 < nseg) {
@@ -423,51 +497,45 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
                                                                p.wait_limit_ns, p.err);
                         ++fix_round;
                         if (!named_barrier_and(1, 128, got_fix)) { fix_ok = false; break; }
-                        // buffer 0 += buffers first_buf.. (own row only: no cross-thread hazards)
                         const int nsum = first_buf + nload;
-                        if (nsum > 1 || k0 == 0) {
-                            for (int c = 0; c < nchunks; ++c) {
-                                const size_t off = ((size_t)c * 128 + row) * 16;
-                                float4 *dst = reinterpret_cast<float4 *>(const_cast<float *>(buf0) + off);
+                        float4 *b0 = reinterpret_cast<float4 *>(buf0);
+                        const int n4 = (int)(slot_floats / 4);   // a multiple of 512
+                        for (int e = tid; e < n4; e += 512) {    // 4 independent float4 per thread per step
+                            float4 a[4];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    float4 a = k0 == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : dst[i];
-                                    for (int b = (k0 == 0 ? 0 : 1); b < nsum; ++b) {
-                                        const float4 t = reinterpret_cast<const float4 *>(buf0 + (size_t)b * slot_floats + off)[i];
-                                        a.x += t.x; a.y += t.y; a.z += t.z; a.w += t.w;
-                                    }
-                                    dst[i] = a;
+                            for (int r = 0; r < 4; ++r) {
+                                a[r] = b0[e + r * 128];
+                                if (k0 == 0) a[r] = make_float4(0.f + a[r].x, 0.f + a[r].y, 0.f + a[r].z, 0.f + a[r].w);
+                            }
+                            for (int bb = 1; bb < nsum; ++bb) {
+                                const float4 *src = reinterpret_cast<const float4 *>(buf0 + (size_t)bb * slot_floats);
+                                float4 t4[4];
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) t4[r] = src[e + r * 128];
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) {
+                                    a[r].x += t4[r].x; a[r].y += t4[r].y; a[r].z += t4[r].z; a[r].w += t4[r].w;
                                 }
                             }
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) b0[e + r * 128] = a[r];
                         }
                         k0 += nload;
                         named_barrier_sync(1, 128);   // buffers 1.. are refilled by the next round
                     }
-                    if (fix_ok) {
-                        for (int c = 0; c < nchunks; ++c) {
-                            const float4 *src = reinterpret_cast<const float4 *>(buf0 + ((size_t)c * 128 + row) * 16);
-                            float v[16];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float4 a = src[i];
-                                v[4 * i] = a.x; v[4 * i + 1] = a.y; v[4 * i + 2] = a.z; v[4 * i + 3] = a.w;
-                            }
-                            swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
-                        }
-                    }
+                    if (fix_ok) swapab_epilogue_smem<EPI>(p, buf0, group, m, tid);
                 } else {
                     for (int c = 0; c < nchunks; ++c) {
                         float v[16] = {};
-                        const size_t off = ((size_t)c * 128 + row) * 16;
                         for (int k = 0; k < nseg; ++k) {
                             const int sl = k < 128 ? ctl->seg_slot[k]
                                                    : (int)((c_first + k) * 2 + ((sk.begin(c_first + k) >= tile * kbp) ? 0 : 1));
-                            const float4 *src = reinterpret_cast<const float4 *>(p.slots + (size_t)sl * slot_floats + off);
+                            const float *src = p.slots + (size_t)sl * slot_floats + (size_t)(c * 16) * 128 + row;
+                            float t16[16];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float4 a = __ldcg(src + i);
-                                v[4 * i] += a.x; v[4 * i + 1] += a.y; v[4 * i + 2] += a.z; v[4 * i + 3] += a.w;
-                            }
+                            for (int i = 0; i < 16; ++i) t16[i] = __ldcg(src + (size_t)i * 128);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] += t16[i];
                         }
                         swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
                     }
