@@ -19,7 +19,7 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_path{MSE_PATH_AUTO};
 std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
-    g_tune_spin_wait{0};
+    g_tune_spin_wait{0}, g_tune_one_launch{1};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -86,8 +86,13 @@ int pow2_at_least(int v) {
 }
 
 // ----------------------------------------------------------------- workspace
+// h | split-K slots of the gate_up pass | split-K slots of the down pass | counters of
+// the gate_up tiles | counters of the down tiles | h-tile flags | exit and h-tile counts.  The
+// region from the first counter to the end must be zero before a call and is left
+// zero by every call that completes.
 struct MlpWs {
-    size_t h_off = 0, slots_off = 0, cnt_gu_off = 0, cnt_dn_off = 0, total = 0;
+    size_t h_off = 0, slots_off = 0, slots_dn_off = 0, cnt_gu_off = 0, cnt_dn_off = 0, flags_off = 0, exit_off = 0,
+           total = 0;
 };
 
 constexpr int64_t kSwapAbMaxT = 256;   // token counts served by the swap-AB kernels
@@ -99,12 +104,19 @@ MlpWs mlp_ws_layout(int64_t T, int64_t H, int64_t I) {
     off = align_up(off + (size_t)T * (size_t)I * 2, 256);
     if (T <= kSwapAbMaxT) {
         const int bn = round_up16(T);
+        const size_t slot_region = (size_t)tc::kMaxGrid * 2 * 128 * (size_t)bn * 4;
         w.slots_off = off;
-        off = align_up(off + (size_t)tc::kMaxGrid * 2 * 128 * (size_t)bn * 4, 256);
+        off = align_up(off + slot_region, 256);
+        w.slots_dn_off = off;
+        off = align_up(off + slot_region, 256);
         w.cnt_gu_off = off;
         off = align_up(off + (size_t)((I + 63) / 64) * 4, 256);
         w.cnt_dn_off = off;
         off = align_up(off + (size_t)((I + 63) / 64) * (size_t)((H + 127) / 128) * 4, 256);
+        w.flags_off = off;
+        off = align_up(off + (size_t)((I + 63) / 64) * 4, 256);
+        w.exit_off = off;   // exit counter, then the count of published h tiles
+        off = align_up(off + 8, 256);
     }
     w.total = off;
     return w;
@@ -355,7 +367,7 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
         p.out = out;
         p.ldo = H;
         p.o_group_stride = T * H;
-        p.slots = reinterpret_cast<float *>(ws + L.slots_off);
+        p.slots = reinterpret_cast<float *>(ws + L.slots_dn_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_dn_off);
         p.err = d.err;
         return from_cuda(tc::launch_swapab(epi, ta, tb, p, swapab_grid(d, p.total_units), true, s));
@@ -398,6 +410,63 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
     const int64_t n_tiles = (int64_t)groups * p.n_mtiles * p.n_ntiles;
     return from_cuda(tc::launch_std(epi, ta, tb, p, std_grid(d, n_tiles), true, s));
 }
+
+// The decode-size layer in one launch: gate_up + SiluAndMul over intermediate columns
+// [j0, j0 + width) into h, then `groups` down projections of `s_width` columns each
+// (group g reads h columns j0 + g * s_width ..) into out[g].
+mse_status tc_mlp_one_launch(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t H, int64_t I,
+                             const uint16_t *w_gate_up, const uint16_t *w_down, int64_t j0, int64_t width,
+                             int64_t s_width, int groups, void *out, int epi1, char *ws, const MlpWs &L,
+                             cudaStream_t s) {
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h_off);
+    CUtensorMap ta0, tb0, ta1, tb1;
+    mse_status st;
+    const int n0 = (int)(width / 64), kbp0 = (int)(H / 64);
+    const int n1 = (int)((H + 127) / 128), kbp1 = (int)(s_width / 64);
+    tc::SwapAbMlpParams fp;
+    std::memset(&fp, 0, sizeof fp);
+    tc::SwapAbParams &p0 = fp.ph[0];
+    tc::SwapAbParams &p1 = fp.ph[1];
+    p0 = swapab_base(T, n0 * kbp0);
+    p1 = swapab_base(T, groups * n1 * kbp1);
+    if ((st = map_2d(&ta0, w_gate_up, 2 * I, H, H, 64)) != MSE_OK) return st;
+    if ((st = map_2d(&tb0, x, T, H, H, p0.bn)) != MSE_OK) return st;
+    if ((st = map_2d(&ta1, w_down, H, I, I, 128)) != MSE_OK) return st;
+    if ((st = map_2d(&tb1, h, T, I, I, p1.bn)) != MSE_OK) return st;
+    p0.n_mtiles = n0;
+    p0.n_groups = 1;
+    p0.kb_per_tile = kbp0;
+    p0.a_row_base = (int)j0;
+    p0.a_up_offset = (int)I;
+    p0.m_valid = 2 * width;
+    p0.out = h;
+    p0.ldo = I;
+    p0.slots = reinterpret_cast<float *>(ws + L.slots_off);
+    p0.counters = reinterpret_cast<int *>(ws + L.cnt_gu_off);
+    p0.err = d.err;
+    p1.n_mtiles = n1;
+    p1.n_groups = groups;
+    p1.kb_per_tile = kbp1;
+    p1.kb_first = (int)(j0 / 64);
+    p1.kb_group_stride = kbp1;
+    p1.m_valid = H;
+    p1.out = out;
+    p1.ldo = H;
+    p1.o_group_stride = T * H;
+    p1.slots = reinterpret_cast<float *>(ws + L.slots_dn_off);
+    p1.counters = reinterpret_cast<int *>(ws + L.cnt_dn_off);
+    p1.err = d.err;
+    fp.hflags = reinterpret_cast<int *>(ws + L.flags_off);
+    fp.hcount = reinterpret_cast<int *>(ws + L.exit_off) + 1;
+    fp.exit_count = reinterpret_cast<int *>(ws + L.exit_off);
+    // every CTA needs units in both phases: a split tile counts one part per CTA in
+    // the range of its owners
+    const int units = p0.total_units < p1.total_units ? p0.total_units : p1.total_units;
+    const int grid = swapab_grid(d, units);
+    return from_cuda(tc::launch_swapab_mlp(epi1, ta0, tb0, ta1, tb1, fp, grid, true, s));
+}
+
+bool one_launch_enabled(int64_t T) { return T <= kSwapAbMaxT && g_tune_one_launch.load() != 0; }
 
 // ----------------------------------------------------------------- path choice
 enum Path { PATH_GENERIC, PATH_TC };
@@ -491,9 +560,16 @@ mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I
         b.M = T; b.N = H; b.K = I; b.groups = 1; b.out = y; b.ldo = H; b.mode = SIMT_BF16;
         if ((st = from_cuda(launch_simt_gemm(b, s))) != MSE_OK) return st;
     } else {
-        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, 0, I, h, ws, L, s)) != MSE_OK) return st;
-        record(g_ev_mid, s);
-        if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s)) != MSE_OK) return st;
+        if (one_launch_enabled(T)) {
+            if ((st = tc_mlp_one_launch(*d, x, T, H, I, w_gate_up, w_down, 0, I, I, 1, y, tc::EPI_BF16, ws, L, s)) !=
+                MSE_OK)
+                return st;
+            record(g_ev_mid, s);   // one launch: no boundary between the passes
+        } else {
+            if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, 0, I, h, ws, L, s)) != MSE_OK) return st;
+            record(g_ev_mid, s);
+            if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s)) != MSE_OK) return st;
+        }
     }
     record(g_ev_end, s);
     return MSE_OK;
@@ -538,9 +614,12 @@ mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int
         b.mode = partial_dtype == MSE_F32 ? SIMT_F32 : SIMT_BF16;
         return from_cuda(launch_simt_gemm(b, s));
     }
+    const int epi = partial_dtype == MSE_F32 ? tc::EPI_F32 : tc::EPI_BF16;
+    if (one_launch_enabled(T))
+        return tc_mlp_one_launch(*d, x, T, H, I, w_gate_up, w_down, j0, width, sw, rank_count, partials, epi, ws, L,
+                                 s);
     if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s)) != MSE_OK) return st;
-    return tc_down(*d, h, T, H, I, w_down, j0, sw, rank_count, partials,
-                   partial_dtype == MSE_F32 ? tc::EPI_F32 : tc::EPI_BF16, ws, L, s);
+    return tc_down(*d, h, T, H, I, w_down, j0, sw, rank_count, partials, epi, ws, L, s);
 }
 
 mse_status shard_sum(const void *partials, mse_dtype partial_dtype, int n_parts, int64_t T, int64_t H,
@@ -691,6 +770,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_CACHE_HINTS: slot = &g_tune_cache_hints; ok = value == 0 || value == 1; break;
         case MSE_TUNE_GRID: slot = &g_tune_grid; ok = value >= 0 && value <= tc::kMaxGrid; break;
         case MSE_TUNE_SPIN_WAIT: slot = &g_tune_spin_wait; ok = value == 0 || value == 1; break;
+        case MSE_TUNE_ONE_LAUNCH: slot = &g_tune_one_launch; ok = value == 0 || value == 1; break;
         default: return -1;
     }
     if (!ok) return -1;

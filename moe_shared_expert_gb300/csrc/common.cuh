@@ -257,6 +257,27 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
     return old;
 }
 
+// GPU-scope relaxed load, acquire-release fence, release reduction
+__device__ __forceinline__ int ld_relaxed_gpu(const int *addr) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void red_add_release_gpu(int *addr, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+// GPU-scope acquire load / release store of a flag word
+__device__ __forceinline__ int ld_acquire_gpu(const int *addr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int *addr, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
     __nv_bfloat16 b = __float2bfloat16_rn(v);
     return *reinterpret_cast<uint16_t *>(&b);

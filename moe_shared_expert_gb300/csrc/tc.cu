@@ -203,28 +203,490 @@ __device__ __forceinline__ void swapab_epilogue_smem(const SwapAbParams &p, cons
     }
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kSwapAbThreads, 1)
-    swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const SwapAbParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    const int S = p.stages, bn = p.bn;
-    const int KBS = p.kbs;                                     // k-blocks per pipeline stage
-    const uint32_t b_tile_bytes = (uint32_t)bn * 128u;         // one k-block of tokens
-    const uint32_t a_stage_bytes = (uint32_t)KBS * kATileBytes;
-    const uint32_t stage_bytes = a_stage_bytes + (uint32_t)KBS * b_tile_bytes;
-    // stage s: [KBS weight tiles of 128 x 64][KBS token tiles of bn x 64]
-    auto sA = [&](int st) { return base + (uint32_t)st * stage_bytes; };
-    auto sB = [&](int st) { return base + (uint32_t)st * stage_bytes + a_stage_bytes; };
-    Ctrl *ctl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + (uint32_t)S * stage_bytes);
+// Teardown waits for copies and MMAs that were issued and will complete; they get at
+// least 100 ms even when the wait limit of the pipeline is set shorter.
+__device__ __forceinline__ uint64_t drain_limit_ns(uint64_t limit) {
+    return limit > 100000000ull ? limit : 100000000ull;
+}
 
+// Position in the shared-memory ring (stage index and the parity of its current use).
+struct RingPos {
+    int stage = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int S) {
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+    }
+};
+
+// Shared-memory layout of the swap-AB ring: stage s holds [kbs weight tiles of
+// 128 x 64][kbs token tiles of bn x 64], 1024-byte aligned (128-byte swizzle atoms).
+struct SwapAbSmem {
+    uint32_t base, stage_bytes, a_stage_bytes, b_tile_bytes;
+    __device__ __forceinline__ SwapAbSmem(uint32_t base_, int bn, int kbs) {
+        base = base_;
+        b_tile_bytes = (uint32_t)bn * 128u;
+        a_stage_bytes = (uint32_t)kbs * kATileBytes;
+        stage_bytes = a_stage_bytes + (uint32_t)kbs * b_tile_bytes;
+    }
+    __device__ __forceinline__ uint32_t a(int st) const { return base + (uint32_t)st * stage_bytes; }
+    __device__ __forceinline__ uint32_t b(int st) const { return a(st) + a_stage_bytes; }
+};
+
+// The CTA's units [ub, ue) of one phase form segments (one per tile touched); each
+// segment is cut into stages of up to kbs consecutive k-blocks.  Producer and MMA
+// walk the same sequence with incremental counters (no divisions inside the loops).
+struct Walk {
+    int64_t u, ue;
+    int kbp, n_mtiles;
+    int kb, kb_end, m, group;   // the current stage starts at k-block kb of tile (group, m)
+    int seg;                    // segments completed in this phase
+    __device__ void init(int64_t ub_, int64_t ue_, int kbp_, int n_mtiles_) {
+        u = ub_; ue = ue_; kbp = kbp_; n_mtiles = n_mtiles_; seg = 0;
+        const int64_t tile = ub_ / kbp_;
+        kb = (int)(ub_ - tile * kbp_);
+        group = (int)(tile / n_mtiles_);
+        m = (int)(tile - (int64_t)group * n_mtiles_);
+        set_end();
+    }
+    __device__ void set_end() {
+        const int64_t rem = ue - u;
+        kb_end = (kbp - kb) < rem ? kbp : kb + (int)rem;
+    }
+    __device__ bool done() const { return u >= ue; }
+    __device__ int count(int kbs) const { return (kb_end - kb) < kbs ? (kb_end - kb) : kbs; }
+    // advance past a stage of n k-blocks; true when that stage ended its segment
+    __device__ bool advance(int n) {
+        kb += n;
+        u += n;
+        if (kb < kb_end) return false;
+        kb = 0;
+        ++seg;
+        if (++m == n_mtiles) { m = 0; ++group; }
+        set_end();
+        return true;
+    }
+};
+
+__device__ __forceinline__ Walk cta_walk(const SwapAbParams &p) {
+    const StreamK sk{p.total_units, gridDim.x};
+    Walk w;
+    w.init(sk.begin(blockIdx.x), sk.begin(blockIdx.x + 1), p.kb_per_tile, p.n_mtiles);
+    return w;
+}
+
+// ---- producer (one elected thread of warp 0) ----
+// pdl_prologue: the weight tiles of the first stages are requested before waiting for
+//   the previous kernel of the stream, the token tiles after that wait (first phase).
+// hflags: the token operand is the intermediate h written earlier in this launch; a
+//   stage's token tiles are requested once every gate_up tile they read has been
+//   published there, while weight tiles keep filling the free stages meanwhile.
+// `issued` counts stages whose loads were requested.  Returns false after an abort.
+template <int EPI>
+__device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB, Ctrl *ctl,
+                               const SwapAbSmem &sm, RingPos &r, int &issued, bool pdl_prologue, const int *hflags,
+                               const int *hcount, int n_htiles, volatile int *abort_flag) {
+    const int S = p.stages, KBS = p.kbs;
+    const uint32_t kb_tx = kATileBytes + sm.b_tile_bytes;
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_x = l2_policy_evict_last();
+    const bool hints = p.cache_hints != 0;
+    auto kglob = [&](const Walk &w, int i) { return p.kb_first + w.group * p.kb_group_stride + w.kb + i; };
+    auto load_a = [&](const Walk &w, int n, int st) {
+        const uint32_t fb = bar_addr(&ctl->full[st]);
+        for (int i = 0; i < n; ++i) {
+            const int k = kglob(w, i) * 64;
+            const uint32_t dst = sm.a(st) + (uint32_t)i * kATileBytes;
+            if constexpr (EPI == EPI_SWIGLU) {
+                // rows 0-63: gate rows j0..j0+63; rows 64-127: the up rows of the same j
+                const int j0 = p.a_row_base + w.m * 64;
+                if (hints) {
+                    tma_load_2d(dst, tmA, fb, k, j0, pol_w);
+                    tma_load_2d(dst + 8192u, tmA, fb, k, p.a_up_offset + j0, pol_w);
+                } else {
+                    tma_load_2d_nohint(dst, tmA, fb, k, j0);
+                    tma_load_2d_nohint(dst + 8192u, tmA, fb, k, p.a_up_offset + j0);
+                }
+            } else {
+                if (hints) tma_load_2d(dst, tmA, fb, k, w.m * 128, pol_w);
+                else tma_load_2d_nohint(dst, tmA, fb, k, w.m * 128);
+            }
+        }
+    };
+    auto load_b = [&](const Walk &w, int n, int st) {
+        const uint32_t fb = bar_addr(&ctl->full[st]);
+        for (int i = 0; i < n; ++i) {
+            const int k = kglob(w, i) * 64;
+            const uint32_t dst = sm.b(st) + (uint32_t)i * sm.b_tile_bytes;
+            if (hints) tma_load_2d(dst, tmB, fb, k, 0, pol_x);
+            else tma_load_2d_nohint(dst, tmB, fb, k, 0);
+        }
+    };
+    Walk w = cta_walk(p);
+    if (pdl_prologue) {
+        // the ring is fresh: stages 0.. in their first use
+        Walk a = w;
+        int st = 0;
+        for (; st < S && !a.done(); ++st) {
+            const int n = a.count(KBS);
+            mbar_arrive_expect_tx(bar_addr(&ctl->full[st]), (uint32_t)n * kb_tx);
+            load_a(a, n, st);
+            a.advance(n);
+        }
+        pdl_wait();
+        for (int t = 0; t < st; ++t) {
+            const int n = w.count(KBS);
+            load_b(w, n, t);
+            w.advance(n);
+        }
+        issued += st;
+        r.stage = st == S ? 0 : st;
+        r.phase = st == S ? 1u : 0u;
+    }
+    if (!hflags) {
+        while (!w.done()) {
+            if (!mbar_wait_bounded(bar_addr(&ctl->empty[r.stage]), r.phase ^ 1u, abort_flag, p.wait_limit_ns, p.err,
+                                   p.spin_wait != 0))
+                return false;
+            const int n = w.count(KBS);
+            mbar_arrive_expect_tx(bar_addr(&ctl->full[r.stage]), (uint32_t)n * kb_tx);
+            load_a(w, n, r.stage);
+            load_b(w, n, r.stage);
+            w.advance(n);
+            ++issued;
+            r.next(S);
+        }
+        return true;
+    }
+    // Two cursors over the same stages: `w` requests weight tiles into free stages, `wb`
+    // follows with the token tiles once their h columns are published.  After an abort
+    // the pending token tiles are still requested (without waiting) so that every
+    // issued stage completes and the teardown drain ends.
+    // Flags are polled with relaxed loads (all of a stage's at once) and one fence once
+    // they are seen set; after the count of published tiles reaches n_htiles no flag is
+    // read again.
+    Walk wb = w;
+    RingPos rb = r;
+    int pending = 0;
+    bool aborted = false, all_ready = false;
+    uint64_t idle_since = 0;
+    while (true) {
+        bool progress = false;
+        if (!aborted && !w.done() && mbar_test_wait(bar_addr(&ctl->empty[r.stage]), r.phase ^ 1u)) {
+            const int n = w.count(KBS);
+            mbar_arrive_expect_tx(bar_addr(&ctl->full[r.stage]), (uint32_t)n * kb_tx);
+            load_a(w, n, r.stage);
+            w.advance(n);
+            ++issued;
+            r.next(S);
+            ++pending;
+            progress = true;
+        }
+        if (pending > 0) {
+            const int n = wb.count(KBS);
+            bool ready = true;
+            if (!aborted && !all_ready) {
+                if (ld_relaxed_gpu(hcount) >= n_htiles) {
+                    all_ready = true;
+                } else {
+                    int f[kMaxKbs];
+#pragma unroll
+                    for (int i = 0; i < kMaxKbs; ++i) f[i] = i < n ? ld_relaxed_gpu(hflags + kglob(wb, i)) : 1;
+#pragma unroll
+                    for (int i = 0; i < kMaxKbs; ++i) ready = ready && f[i] != 0;
+                }
+                if (ready) fence_acq_rel_gpu();   // acquire the publishers' h stores
+            }
+            if (ready) {
+                fence_proxy_async_global();   // h was written through the generic proxy
+                load_b(wb, n, rb.stage);
+                wb.advance(n);
+                rb.next(S);
+                --pending;
+                progress = true;
+            }
+        } else if (w.done() || aborted) {
+            break;
+        }
+        if (progress) {
+            idle_since = 0;
+            continue;
+        }
+        if (*abort_flag) {
+            aborted = true;
+            continue;
+        }
+        const uint64_t now = global_timer_ns();
+        if (idle_since == 0) {
+            idle_since = now;
+        } else if (now - idle_since > p.wait_limit_ns) {
+            *abort_flag = 1;
+            raise_device_error(p.err, DEV_ERR_TIMEOUT);
+            aborted = true;
+        }
+    }
+    return !aborted;
+}
+
+// ---- MMA issuer (one elected thread of warp 1) ----
+// Segment `gseg` (counted over all phases) accumulates in TMEM buffer gseg & 1.
+__device__ bool swapab_mma(const SwapAbParams &p, Ctrl *ctl, const SwapAbSmem &sm, RingPos &r, int &gseg,
+                           uint32_t tmem_base, volatile int *abort_flag) {
+    const int S = p.stages, KBS = p.kbs;
+    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)p.bn);
+    Walk w = cta_walk(p);
+    while (!w.done()) {
+        const int buf = gseg & 1;
+        const uint32_t use = (uint32_t)(gseg >> 1);
+        if (!mbar_wait_bounded(bar_addr(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, p.wait_limit_ns, p.err))
+            return false;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * (p.tmem_cols / 2));
+        bool first = true, seg_end = false;
+        while (!seg_end) {
+            if (!mbar_wait_bounded(bar_addr(&ctl->full[r.stage]), r.phase, abort_flag, p.wait_limit_ns, p.err,
+                                   p.spin_wait != 0))
+                return false;
+            tc_fence_after();
+            const int n = w.count(KBS);
+            for (int i = 0; i < n; ++i) {
+                const uint64_t ad = smem_desc_sw128(sm.a(r.stage) + (uint32_t)i * kATileBytes);
+                const uint64_t bd = smem_desc_sw128(sm.b(r.stage) + (uint32_t)i * sm.b_tile_bytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    tc_mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, first ? 0u : 1u);
+                    first = false;
+                }
+            }
+            tc_commit(bar_addr(&ctl->empty[r.stage]));
+            r.next(S);
+            seg_end = w.advance(n);
+        }
+        tc_commit(bar_addr(&ctl->tfull[buf]));
+        ++gseg;
+    }
+    return true;
+}
+
+// Publication of a finished gate_up tile (m) for readers of h in the same launch: every
+// epilogue thread's h stores, then one GPU-scope release of the tile's flag and of the
+// count of published tiles.
+__device__ __forceinline__ void publish_h_tile(const SwapAbParams &p, int *hflags, int *hcount, int m) {
+    fence_proxy_async_global();
+    named_barrier_sync(1, 128);
+    if (threadIdx.x == 64) {
+        st_release_gpu(hflags + p.a_row_base / 64 + m, 1);
+        red_add_release_gpu(hcount, 1);
+    }
+}
+
+// ---- epilogue (warps 2..5, 128 threads) ----
+// ring_idle_at_end: after this phase's last MMA the ring is idle, so a split tile
+//   finished in the CTA's last segment may stage the parts in the ring's memory.
+// hflags: publish each completed tile (gate_up phase of the fused layer).
+template <int EPI>
+__device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring, uint32_t ring_base,
+                                uint32_t ring_bytes, int &gseg, uint32_t &fix_round, uint32_t tmem_base,
+                                bool ring_idle_at_end, int *hflags, int *hcount, volatile int *abort_flag) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int tid = threadIdx.x - 64;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const int bn = p.bn, kbp = p.kb_per_tile;
+    const int nchunks = bn / 16;
     const StreamK sk{p.total_units, gridDim.x};
     const int64_t ub = sk.begin(blockIdx.x), ue = sk.begin(blockIdx.x + 1);
-    const int kbp = p.kb_per_tile;
+    const size_t slot_floats = (size_t)128 * bn;
+    for (int64_t u = ub; u < ue;) {
+        const int64_t tile = u / kbp;
+        const int kb0 = (int)(u % kbp);
+        const int64_t rem = ue - u;
+        const int kb1 = (int)((kbp - kb0) < rem ? kbp : kb0 + rem);
+        const int buf = gseg & 1;
+        const uint32_t use = (uint32_t)(gseg >> 1);
+        const int group = (int)(tile / p.n_mtiles);
+        const int m = (int)(tile % p.n_mtiles);
+        u = tile * kbp + kb1;
+        ++gseg;
+        const bool got = mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
+        if (!named_barrier_and(1, 128, got)) return false;   // all epilogue warps take the same branch
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + (uint32_t)(buf * (p.tmem_cols / 2)) + lane_off;
+        if (kb0 == 0 && kb1 == kbp) {
+            for (int c = 0; c < nchunks; ++c) {
+                float v[16];
+                load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
+                swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(&ctl->tempty[buf]));
+            if (hflags) publish_h_tile(p, hflags, hcount, m);
+            continue;
+        }
+        // Tile shared with other CTAs: park the fp32 partial in this CTA's slot, laid
+        // out [token column][accumulator row] (each warp store is a 128-byte run).
+        const int which = (ub / kbp == tile) ? 0 : 1;
+        float *slot = p.slots + ((size_t)blockIdx.x * 2 + which) * slot_floats;
+        for (int c = 0; c < nchunks; ++c) {
+            float v[16];
+            load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) __stcg(slot + (size_t)(c * 16 + i) * 128 + row, v[i]);
+        }
+        fence_proxy_async_global();   // a finisher may fetch this slot with a bulk copy
+        named_barrier_sync(1, 128);
+        const int64_t c_first = sk.owner(tile * kbp), c_last = sk.owner(tile * kbp + kbp - 1);
+        const int nseg = (int)(c_last - c_first + 1);
+        if (threadIdx.x == 64) {
+            // release: the barrier above orders every epilogue thread's slot stores
+            // before this atomic; acquire: the finisher then sees all other parts
+            const int prev = atomic_add_acq_rel_gpu(p.counters + tile, 1);
+            ctl->fin_flag = (prev == nseg - 1) ? 1 : 0;
+        }
+        named_barrier_sync(1, 128);
+        if (!ctl->fin_flag) {
+            tc_fence_before();
+            mbar_arrive(bar_addr(&ctl->tempty[buf]));
+            named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
+            continue;
+        }
+        // This CTA arrived last: sum the parts in ascending part (CTA) order starting
+        // from 0, so the result does not depend on which CTA finishes the tile.
+        // slot of each part: CTA cc's first segment uses slot 2cc, its last one 2cc+1
+        for (int k = tid; k < nseg && k < 128; k += 128) {
+            const int64_t cc = c_first + k;
+            ctl->seg_slot[k] = (int)(cc * 2 + ((sk.begin(cc) >= tile * kbp) ? 0 : 1));
+        }
+        named_barrier_sync(1, 128);
+        auto slot_of = [&](int k) -> int {
+            return k < 128 ? ctl->seg_slot[k]
+                           : (int)((c_first + k) * 2 + ((sk.begin(c_first + k) >= tile * kbp) ? 0 : 1));
+        };
+        const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
+        const int per_round = (int)(ring_bytes / slot_bytes);
+        if (ring_idle_at_end && u == ue && per_round >= 2 && nseg <= 128) {
+            // Last segment of the phase with the ring idle: the parts are bulk-copied into
+            // the ring's memory (buffer 0 keeps the running sum) and summed element-wise.
+            tc_fence_before();
+            mbar_arrive(bar_addr(&ctl->tempty[buf]));
+            fence_proxy_async_global();
+            float *buf0 = reinterpret_cast<float *>(ring);
+            bool fix_ok = true;
+            int k0 = 0;
+            while (k0 < nseg) {
+                const int first_buf = k0 == 0 ? 0 : 1;
+                const int nload = min(nseg - k0, per_round - first_buf);
+                if (threadIdx.x == 64) {
+                    mbar_arrive_expect_tx(bar_addr(&ctl->fixbar), (uint32_t)nload * slot_bytes);
+                    for (int i = 0; i < nload; ++i)
+                        bulk_load(ring_base + (uint32_t)(first_buf + i) * slot_bytes,
+                                  p.slots + (size_t)ctl->seg_slot[k0 + i] * slot_floats, slot_bytes,
+                                  bar_addr(&ctl->fixbar));
+                }
+                const bool got_fix = mbar_wait_bounded(bar_addr(&ctl->fixbar), fix_round & 1u, abort_flag,
+                                                       p.wait_limit_ns, p.err);
+                ++fix_round;
+                if (!named_barrier_and(1, 128, got_fix)) {
+                    // copies into the ring may still be in flight: let them land first
+                    if (threadIdx.x == 64)
+                        (void)mbar_wait_drain(bar_addr(&ctl->fixbar), (fix_round - 1) & 1u,
+                                              drain_limit_ns(p.wait_limit_ns));
+                    fix_ok = false;
+                    break;
+                }
+                const int nsum = first_buf + nload;
+                float4 *b0 = reinterpret_cast<float4 *>(buf0);
+                const int n4 = (int)(slot_floats / 4);   // a multiple of 512
+                for (int e = tid; e < n4; e += 512) {    // 4 independent float4 per thread per step
+                    float4 a[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        a[r] = b0[e + r * 128];
+                        if (k0 == 0) a[r] = make_float4(0.f + a[r].x, 0.f + a[r].y, 0.f + a[r].z, 0.f + a[r].w);
+                    }
+                    for (int bb = 1; bb < nsum; ++bb) {
+                        const float4 *src = reinterpret_cast<const float4 *>(buf0 + (size_t)bb * slot_floats);
+                        float4 t4[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) t4[r] = src[e + r * 128];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            a[r].x += t4[r].x; a[r].y += t4[r].y; a[r].z += t4[r].z; a[r].w += t4[r].w;
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) b0[e + r * 128] = a[r];
+                }
+                k0 += nload;
+                named_barrier_sync(1, 128);   // buffers 1.. are refilled by the next round
+            }
+            if (!fix_ok) return false;
+            swapab_epilogue_smem<EPI>(p, buf0, group, m, tid);
+        } else {
+            // In registers: this CTA's own part straight from tensor memory (its buffer is
+            // released afterwards), the others from their slots in L2; two chunks of 16
+            // tokens x two parts per round keep 64 loads per thread in flight.
+            constexpr int NB = 2, NP = 2;
+            const int k_own = (int)(blockIdx.x - c_first);
+            for (int c0 = 0; c0 < nchunks; c0 += NB) {
+                float acc[NB][16];
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[b][i] = 0.f;
+                for (int k0 = 0; k0 < nseg; k0 += NP) {
+                    float t[NP][NB][16];
+#pragma unroll
+                    for (int s = 0; s < NP; ++s) {
+                        const int k = k0 + s;
+                        if (k < nseg && k != k_own) {
+                            const float *src = p.slots + (size_t)slot_of(k) * slot_floats + row;
+#pragma unroll
+                            for (int b = 0; b < NB; ++b) {
+                                if (c0 + b < nchunks) {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i)
+                                        t[s][b][i] = __ldcg(src + (size_t)((c0 + b) * 16 + i) * 128);
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int s = 0; s < NP; ++s) {
+                        if (k0 + s == k_own) {
+#pragma unroll
+                            for (int b = 0; b < NB; ++b)
+                                if (c0 + b < nchunks) load_tmem_chunk(tacc + (uint32_t)((c0 + b) * 16), t[s][b]);
+                        }
+                    }
+#pragma unroll
+                    for (int s = 0; s < NP; ++s) {
+                        if (k0 + s < nseg) {
+#pragma unroll
+                            for (int b = 0; b < NB; ++b)
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) acc[b][i] += t[s][b][i];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    if (c0 + b < nchunks) swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c0 + b, acc[b]);
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(&ctl->tempty[buf]));
+        }
+        if (threadIdx.x == 64) p.counters[tile] = 0;
+        if (hflags) publish_h_tile(p, hflags, hcount, m);
+        named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
+    }
+    return true;
+}
 
+// ---- set-up and teardown shared by the swap-AB kernels ----
+__device__ __forceinline__ void swapab_setup(Ctrl *ctl, int S, int tmem_cols, const CUtensorMap *const *maps,
+                                             int n_maps) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_addr(&ctl->full[s]), 1);
@@ -239,327 +701,142 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-    }
+    if (warp == 0 && lane == 0)
+        for (int i = 0; i < n_maps; ++i) tma_prefetch_desc(maps[i]);
     if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), (uint32_t)p.tmem_cols);
+        tmem_alloc(smem_u32(&ctl->tmem_base), (uint32_t)tmem_cols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = ctl->tmem_base;
-    volatile int *abort_flag = &ctl->abort_flag;
-    pdl_launch_dependents();
+}
 
-    // The CTA's units [ub, ue) form segments (one per tile touched); each segment is cut
-    // into stages of up to KBS consecutive k-blocks.  Producer and MMA walk the same
-    // sequence with incremental counters (no divisions inside the loops).
-    struct Walk {
-        int64_t u, ue;
-        int kbp, n_mtiles;
-        int kb, kb_end, m, group;     // current stage starts at k-block kb of tile (group, m)
-        int seg;                      // segment index within this CTA
-        __device__ void init(int64_t ub_, int64_t ue_, int kbp_, int n_mtiles_) {
-            u = ub_; ue = ue_; kbp = kbp_; n_mtiles = n_mtiles_; seg = 0;
-            const int64_t tile = ub_ / kbp_;
-            kb = (int)(ub_ - tile * kbp_);
-            group = (int)(tile / n_mtiles_);
-            m = (int)(tile - (int64_t)group * n_mtiles_);
-            set_end();
-        }
-        __device__ void set_end() {
-            const int64_t rem = ue - u;
-            kb_end = (kbp - kb) < rem ? kbp : kb + (int)rem;
-        }
-        __device__ bool done() const { return u >= ue; }
-        // k-blocks of the current stage
-        __device__ int count(int kbs) const { return (kb_end - kb) < kbs ? (kb_end - kb) : kbs; }
-        // advance past a stage of n k-blocks; returns true when that stage ended its segment
-        __device__ bool advance(int n) {
-            kb += n;
-            u += n;
-            if (kb < kb_end) return false;
-            kb = 0;
-            ++seg;
-            if (++m == n_mtiles) { m = 0; ++group; }
-            set_end();
-            return true;
-        }
-    };
-
-    int issued = 0;   // producer: stages whose loads were issued
-
-    if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol_w = l2_policy_evict_first();
-            const uint64_t pol_x = l2_policy_evict_last();
-            const bool hints = p.cache_hints != 0;
-            auto kglob = [&](const Walk &w, int i) { return p.kb_first + w.group * p.kb_group_stride + w.kb + i; };
-            auto load_a = [&](const Walk &w, int n, int st) {
-                const uint32_t fb = bar_addr(&ctl->full[st]);
-                for (int i = 0; i < n; ++i) {
-                    const int k = kglob(w, i) * 64;
-                    const uint32_t dst = sA(st) + (uint32_t)i * kATileBytes;
-                    if constexpr (EPI == EPI_SWIGLU) {
-                        // rows 0-63: gate rows j0..j0+63; rows 64-127: the up rows of the same j
-                        const int j0 = p.a_row_base + w.m * 64;
-                        if (hints) {
-                            tma_load_2d(dst, &tmA, fb, k, j0, pol_w);
-                            tma_load_2d(dst + 8192u, &tmA, fb, k, p.a_up_offset + j0, pol_w);
-                        } else {
-                            tma_load_2d_nohint(dst, &tmA, fb, k, j0);
-                            tma_load_2d_nohint(dst + 8192u, &tmA, fb, k, p.a_up_offset + j0);
-                        }
-                    } else {
-                        if (hints) tma_load_2d(dst, &tmA, fb, k, w.m * 128, pol_w);
-                        else tma_load_2d_nohint(dst, &tmA, fb, k, w.m * 128);
-                    }
-                }
-            };
-            auto load_b = [&](const Walk &w, int n, int st) {
-                const uint32_t fb = bar_addr(&ctl->full[st]);
-                for (int i = 0; i < n; ++i) {
-                    const int k = kglob(w, i) * 64;
-                    const uint32_t dst = sB(st) + (uint32_t)i * b_tile_bytes;
-                    if (hints) tma_load_2d(dst, &tmB, fb, k, 0, pol_x);
-                    else tma_load_2d_nohint(dst, &tmB, fb, k, 0);
-                }
-            };
-            Walk w;
-            w.init(ub, ue, kbp, p.n_mtiles);
-            // Prologue: weight tiles do not depend on the previous kernel, so they are
-            // requested before waiting for it; the token tiles follow the wait.
-            {
-                Walk a = w;
-                int st = 0;
-                for (; st < S && !a.done(); ++st) {
-                    const int n = a.count(KBS);
-                    mbar_arrive_expect_tx(bar_addr(&ctl->full[st]), (uint32_t)n * (kATileBytes + b_tile_bytes));
-                    load_a(a, n, st);
-                    a.advance(n);
-                }
-                pdl_wait();
-                for (int t = 0; t < st; ++t) {
-                    const int n = w.count(KBS);
-                    load_b(w, n, t);
-                    w.advance(n);
-                }
-                issued = st;
-            }
-            int stage = issued == S ? 0 : issued;
-            uint32_t phase = issued == S ? 1u : 0u;
-            while (!w.done()) {
-                if (!mbar_wait_bounded(bar_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns, p.err,
-                                       p.spin_wait != 0))
-                    break;
-                const int n = w.count(KBS);
-                mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), (uint32_t)n * (kATileBytes + b_tile_bytes));
-                load_a(w, n, stage);
-                load_b(w, n, stage);
-                w.advance(n);
-                ++issued;
-                if (++stage == S) { stage = 0; phase ^= 1u; }
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)bn);
-            int stage = 0;
-            uint32_t phase = 0;
-            Walk w;
-            w.init(ub, ue, kbp, p.n_mtiles);
-            bool ok = true;
-            while (!w.done() && ok) {
-                const int buf = w.seg & 1;
-                const uint32_t use = (uint32_t)(w.seg >> 1);
-                if (!mbar_wait_bounded(bar_addr(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, p.wait_limit_ns,
-                                       p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(buf * (p.tmem_cols / 2));
-                bool first = true, seg_end = false;
-                while (!seg_end) {
-                    if (!mbar_wait_bounded(bar_addr(&ctl->full[stage]), phase, abort_flag, p.wait_limit_ns, p.err,
-                                           p.spin_wait != 0)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const int n = w.count(KBS);
-                    for (int i = 0; i < n; ++i) {
-                        const uint64_t ad = smem_desc_sw128(sA(stage) + (uint32_t)i * kATileBytes);
-                        const uint64_t bd = smem_desc_sw128(sB(stage) + (uint32_t)i * b_tile_bytes);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            tc_mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, first ? 0u : 1u);
-                            first = false;
-                        }
-                    }
-                    tc_commit(bar_addr(&ctl->empty[stage]));
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
-                    seg_end = w.advance(n);
-                }
-                if (!ok) break;
-                tc_commit(bar_addr(&ctl->tfull[buf]));
-            }
-        }
-    } else {
-        // epilogue warps 2..5
-        const int q = warp & 3;
-        const int row = q * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        pdl_wait();
-        int seg = 0;
-        uint32_t fix_round = 0;   // completed phases of fixbar
-        for (int64_t u = ub; u < ue; ++seg) {
-            const int64_t tile = u / kbp;
-            const int kb0 = (int)(u % kbp);
-            const int64_t rem = ue - u;
-            const int kb1 = (int)((kbp - kb0) < rem ? kbp : kb0 + rem);
-            const int buf = seg & 1;
-            const uint32_t use = (uint32_t)(seg >> 1);
-            const int group = (int)(tile / p.n_mtiles);
-            const int m = (int)(tile % p.n_mtiles);
-            u = tile * kbp + kb1;
-            const bool got = mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
-            if (!named_barrier_and(1, 128, got)) break;   // all epilogue warps take the same branch
-            tc_fence_after();
-            const uint32_t tacc = tmem_base + (uint32_t)(buf * (p.tmem_cols / 2)) + lane_off;
-            const int nchunks = bn / 16;
-            if (kb0 == 0 && kb1 == kbp) {
-                for (int c = 0; c < nchunks; ++c) {
-                    float v[16];
-                    load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
-                    swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
-                }
-                tc_fence_before();
-                mbar_arrive(bar_addr(&ctl->tempty[buf]));
-                continue;
-            }
-            // Tile shared with other CTAs: park the fp32 partial in this CTA's slot, laid
-            // out [token column][accumulator row] (each warp store is a 128-byte run).
-            const int which = (sk.begin(blockIdx.x) / kbp == tile) ? 0 : 1;
-            float *slot = p.slots + ((size_t)blockIdx.x * 2 + which) * (size_t)(128 * bn);
-            for (int c = 0; c < nchunks; ++c) {
-                float v[16];
-                load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) __stcg(slot + (size_t)(c * 16 + i) * 128 + row, v[i]);
-            }
-            tc_fence_before();
-            mbar_arrive(bar_addr(&ctl->tempty[buf]));
-            fence_proxy_async_global();   // a finisher may fetch this slot with a bulk copy
-            named_barrier_sync(1, 128);
-            const int64_t c_first = sk.owner(tile * kbp), c_last = sk.owner(tile * kbp + kbp - 1);
-            const int nseg = (int)(c_last - c_first + 1);
-            if (threadIdx.x == 64) {
-                // release: the barrier above orders every epilogue thread's slot stores
-                // before this atomic; acquire: the finisher then sees all other parts
-                const int prev = atomic_add_acq_rel_gpu(p.counters + tile, 1);
-                ctl->fin_flag = (prev == nseg - 1) ? 1 : 0;
-            }
-            named_barrier_sync(1, 128);
-            if (ctl->fin_flag) {
-                // slot of each part: CTA cc's first segment uses slot 2cc, its last one 2cc+1
-                for (int k = threadIdx.x - 64; k < nseg && k < 128; k += 128) {
-                    const int64_t cc = c_first + k;
-                    ctl->seg_slot[k] = (int)(cc * 2 + ((sk.begin(cc) >= tile * kbp) ? 0 : 1));
-                }
-                named_barrier_sync(1, 128);
-                const size_t slot_floats = (size_t)128 * bn;
-                const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
-                const int per_round = (int)(((size_t)S * stage_bytes) / slot_bytes);
-                const int tid = threadIdx.x - 64;
-                if (u == ue && per_round >= 2 && nseg <= 128) {
-                    // Last segment of this CTA: the pipeline's shared memory is idle, so the
-                    // parts are bulk-copied into it (buffer 0 keeps the running sum) and summed
-                    // element-wise in ascending part order starting from 0, as the fallback does.
-                    fence_proxy_async_global();
-                    float *buf0 = reinterpret_cast<float *>(smem_raw + (base - raw));
-                    bool fix_ok = true;
-                    int k0 = 0;
-                    while (k0 < nseg) {
-                        const int first_buf = k0 == 0 ? 0 : 1;
-                        const int nload = min(nseg - k0, per_round - first_buf);
-                        if (threadIdx.x == 64) {
-                            mbar_arrive_expect_tx(bar_addr(&ctl->fixbar), (uint32_t)nload * slot_bytes);
-                            for (int i = 0; i < nload; ++i)
-                                bulk_load(base + (uint32_t)(first_buf + i) * slot_bytes,
-                                          p.slots + (size_t)ctl->seg_slot[k0 + i] * slot_floats, slot_bytes,
-                                          bar_addr(&ctl->fixbar));
-                        }
-                        const bool got_fix = mbar_wait_bounded(bar_addr(&ctl->fixbar), fix_round & 1u, abort_flag,
-                                                               p.wait_limit_ns, p.err);
-                        ++fix_round;
-                        if (!named_barrier_and(1, 128, got_fix)) { fix_ok = false; break; }
-                        const int nsum = first_buf + nload;
-                        float4 *b0 = reinterpret_cast<float4 *>(buf0);
-                        const int n4 = (int)(slot_floats / 4);   // a multiple of 512
-                        for (int e = tid; e < n4; e += 512) {    // 4 independent float4 per thread per step
-                            float4 a[4];
-#pragma unroll
-                            for (int r = 0; r < 4; ++r) {
-                                a[r] = b0[e + r * 128];
-                                if (k0 == 0) a[r] = make_float4(0.f + a[r].x, 0.f + a[r].y, 0.f + a[r].z, 0.f + a[r].w);
-                            }
-                            for (int bb = 1; bb < nsum; ++bb) {
-                                const float4 *src = reinterpret_cast<const float4 *>(buf0 + (size_t)bb * slot_floats);
-                                float4 t4[4];
-#pragma unroll
-                                for (int r = 0; r < 4; ++r) t4[r] = src[e + r * 128];
-#pragma unroll
-                                for (int r = 0; r < 4; ++r) {
-                                    a[r].x += t4[r].x; a[r].y += t4[r].y; a[r].z += t4[r].z; a[r].w += t4[r].w;
-                                }
-                            }
-#pragma unroll
-                            for (int r = 0; r < 4; ++r) b0[e + r * 128] = a[r];
-                        }
-                        k0 += nload;
-                        named_barrier_sync(1, 128);   // buffers 1.. are refilled by the next round
-                    }
-                    if (fix_ok) swapab_epilogue_smem<EPI>(p, buf0, group, m, tid);
-                } else {
-                    for (int c = 0; c < nchunks; ++c) {
-                        float v[16] = {};
-                        for (int k = 0; k < nseg; ++k) {
-                            const int sl = k < 128 ? ctl->seg_slot[k]
-                                                   : (int)((c_first + k) * 2 + ((sk.begin(c_first + k) >= tile * kbp) ? 0 : 1));
-                            const float *src = p.slots + (size_t)sl * slot_floats + (size_t)(c * 16) * 128 + row;
-                            float t16[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) t16[i] = __ldcg(src + (size_t)i * 128);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] += t16[i];
-                        }
-                        swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
-                    }
-                }
-                if (threadIdx.x == 64) p.counters[tile] = 0;
-            }
-            named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
-        }
-    }
-
-    // ---- teardown: drain in-flight copies and MMAs, then free tensor memory ----
+// Drain in-flight copies and MMAs, then free tensor memory (all threads).
+__device__ __forceinline__ void swapab_teardown(Ctrl *ctl, int S, int issued, uint32_t tmem_base, int tmem_cols,
+                                                uint64_t limit_ns) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0 && lane == 0) {
         const int first = issued > S ? issued - S : 0;
         for (int i = first; i < issued; ++i)
-            (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1), p.wait_limit_ns);
+            (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1), drain_limit_ns(limit_ns));
     }
     if (warp == 1 && lane == 0) {
         tc_commit(bar_addr(&ctl->drain));
-        (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, p.wait_limit_ns);
+        (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, drain_limit_ns(limit_ns));
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+    if (warp == 1) tmem_dealloc(tmem_base, (uint32_t)tmem_cols);
+}
+
+// One stream-K pass: out = epilogue(A . B^T) over p's (group, m-tile, k-block) units.
+template <int EPI>
+__global__ void __launch_bounds__(kSwapAbThreads, 1)
+    swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const SwapAbParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const SwapAbSmem sm(base, p.bn, p.kbs);
+    const int S = p.stages;
+    uint8_t *ring = smem_raw + (base - raw);
+    Ctrl *ctl = reinterpret_cast<Ctrl *>(ring + (uint32_t)S * sm.stage_bytes);
+    const CUtensorMap *maps[2] = {&tmA, &tmB};
+    swapab_setup(ctl, S, p.tmem_cols, maps, 2);
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile int *abort_flag = &ctl->abort_flag;
+    pdl_launch_dependents();
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    int issued = 0;
+    if (warp == 0) {
+        if (lane == 0) {
+            RingPos r;
+            (void)swapab_produce<EPI>(p, &tmA, &tmB, ctl, sm, r, issued, true, nullptr, nullptr, 0, abort_flag);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            RingPos r;
+            int gseg = 0;
+            (void)swapab_mma(p, ctl, sm, r, gseg, tmem_base, abort_flag);
+        }
+    } else {
+        pdl_wait();
+        int gseg = 0;
+        uint32_t fix_round = 0;
+        (void)swapab_epilogue<EPI>(p, ctl, ring, base, (uint32_t)S * sm.stage_bytes, gseg, fix_round, tmem_base,
+                                   true, nullptr, nullptr, abort_flag);
+    }
+    swapab_teardown(ctl, S, issued, tmem_base, p.tmem_cols, p.wait_limit_ns);
+}
+
+// The whole shared-expert layer at decode token counts in one launch:
+//   phase 0  h = silu(x W_gate^T) * (x W_up^T)   (stream-K over gate_up tiles)
+//   phase 1  out = h W_down^T                     (stream-K over down tiles)
+// Every CTA runs its share of phase 0 and then its share of phase 1 through the same
+// ring.  Phase-1 weight tiles stream into stages as soon as phase-0 MMAs free them;
+// its token tiles (h) wait for the flag of the gate_up tile that writes them.  One
+// CTA per SM and grid <= SMs: every CTA is resident once the previous work on the
+// stream leaves, and every wait is bounded.  The last CTA to leave clears the flags
+// and counts, so the sync words are zero again on exit.
+template <int EPI1>
+__global__ void __launch_bounds__(kSwapAbThreads, 1)
+    swapab_mlp_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                      const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                      const SwapAbMlpParams fp) {
+    const SwapAbParams &p0 = fp.ph[0];
+    const SwapAbParams &p1 = fp.ph[1];
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const SwapAbSmem sm(base, p0.bn, p0.kbs);
+    const int S = p0.stages;
+    uint8_t *ring = smem_raw + (base - raw);
+    Ctrl *ctl = reinterpret_cast<Ctrl *>(ring + (uint32_t)S * sm.stage_bytes);
+    const CUtensorMap *maps[4] = {&tmA0, &tmB0, &tmA1, &tmB1};
+    swapab_setup(ctl, S, p0.tmem_cols, maps, 4);
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile int *abort_flag = &ctl->abort_flag;
+    pdl_launch_dependents();
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    int issued = 0;
+    if (warp == 0) {
+        if (lane == 0) {
+            RingPos r;
+            if (swapab_produce<EPI_SWIGLU>(p0, &tmA0, &tmB0, ctl, sm, r, issued, true, nullptr, nullptr, 0,
+                                           abort_flag))
+                (void)swapab_produce<EPI1>(p1, &tmA1, &tmB1, ctl, sm, r, issued, false, fp.hflags, fp.hcount,
+                                           p0.n_mtiles, abort_flag);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            RingPos r;
+            int gseg = 0;
+            if (swapab_mma(p0, ctl, sm, r, gseg, tmem_base, abort_flag))
+                (void)swapab_mma(p1, ctl, sm, r, gseg, tmem_base, abort_flag);
+        }
+    } else {
+        pdl_wait();
+        int gseg = 0;
+        uint32_t fix_round = 0;
+        const uint32_t ring_bytes = (uint32_t)S * sm.stage_bytes;
+        if (swapab_epilogue<EPI_SWIGLU>(p0, ctl, ring, base, ring_bytes, gseg, fix_round, tmem_base, false, fp.hflags,
+                                        fp.hcount, abort_flag))
+            (void)swapab_epilogue<EPI1>(p1, ctl, ring, base, ring_bytes, gseg, fix_round, tmem_base, true, nullptr,
+                                        nullptr, abort_flag);
+    }
+    swapab_teardown(ctl, S, issued, tmem_base, p0.tmem_cols, p0.wait_limit_ns);
+    if (threadIdx.x == 0 && !*abort_flag) {
+        // every flag read of this CTA precedes this increment; the last CTA clears them
+        if (atomic_add_acq_rel_gpu(fp.exit_count, 1) == (int)gridDim.x - 1) {
+            for (int t = 0; t < p0.n_mtiles; ++t) fp.hflags[p0.a_row_base / 64 + t] = 0;
+            *fp.hcount = 0;
+            *fp.exit_count = 0;
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -768,11 +1045,11 @@ __global__ void __launch_bounds__(kStdThreads, 1)
     if (warp == 0 && lane == 0) {
         const int64_t first = issued > S ? issued - S : 0;
         for (int64_t i = first; i < issued; ++i)
-            (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1), p.wait_limit_ns);
+            (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1), drain_limit_ns(p.wait_limit_ns));
     }
     if (warp == 1 && lane == 0) {
         tc_commit(bar_addr(&ctl->drain));
-        (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, p.wait_limit_ns);
+        (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, drain_limit_ns(p.wait_limit_ns));
     }
     tc_fence_before();
     __syncthreads();
@@ -995,13 +1272,13 @@ __global__ void __launch_bounds__(kStdThreads, 1)
         // (from both CTAs) have landed and been consumed
         const int64_t first = issued > S ? issued - S : 0;
         for (int64_t i = first; i < issued; ++i) {
-            const bool done = mbar_wait_drain(bar_addr(&ctl->empty[i % S]), (uint32_t)((i / S) & 1), p.wait_limit_ns);
+            const bool done = mbar_wait_drain(bar_addr(&ctl->empty[i % S]), (uint32_t)((i / S) & 1), drain_limit_ns(p.wait_limit_ns));
             if (!done) __nanosleep(200000);   // abort path: let in-flight copies land
         }
     }
     if (warp == 1 && lane == 0 && leader) {
         tc_commit_pair_multicast(bar_addr(&ctl->drain), (uint16_t)0x1);
-        (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, p.wait_limit_ns);
+        (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, drain_limit_ns(p.wait_limit_ns));
     }
     tc_fence_before();
     __syncthreads();
@@ -1069,6 +1346,37 @@ cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb,
             e = ensure_smem_attr(swapab_kernel<EPI_MERGED>, 3);
             if (e != cudaSuccess) return e;
             return cudaLaunchKernelEx(&cfg, swapab_kernel<EPI_MERGED>, ta, tb, p);
+    }
+}
+
+// One CTA per SM (the ring takes most of the shared memory) and grid <= SMs, so every
+// CTA of the launch is resident once the previous work on the stream has left its SM;
+// phase 1's waits on other CTAs are bounded like every other wait.
+cudaError_t launch_swapab_mlp(int epi1, const CUtensorMap &ta0, const CUtensorMap &tb0, const CUtensorMap &ta1,
+                              const CUtensorMap &tb1, const SwapAbMlpParams &fp, int grid, bool pdl, cudaStream_t s) {
+    const SwapAbParams &p0 = fp.ph[0];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)kSwapAbThreads);
+    cfg.dynamicSmemBytes = swapab_smem_bytes(p0.bn, p0.stages, p0.kbs);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e;
+    switch (epi1) {
+        case EPI_BF16:
+            e = ensure_smem_attr(swapab_mlp_kernel<EPI_BF16>, 12);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, swapab_mlp_kernel<EPI_BF16>, ta0, tb0, ta1, tb1, fp);
+        case EPI_F32:
+            e = ensure_smem_attr(swapab_mlp_kernel<EPI_F32>, 13);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, swapab_mlp_kernel<EPI_F32>, ta0, tb0, ta1, tb1, fp);
+        default:
+            return cudaErrorInvalidValue;
     }
 }
 

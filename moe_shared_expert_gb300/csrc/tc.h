@@ -42,6 +42,16 @@ struct SwapAbParams {
     uint32_t *err;
 };
 
+// The decode-size shared-expert layer in one launch: phase 0 = gate_up + SiluAndMul
+// into h (EPI_SWIGLU), phase 1 = down projection of h (EPI_BF16 or EPI_F32, groups =
+// shards).  Both phases use the same bn, stages and kbs.
+struct SwapAbMlpParams {
+    SwapAbParams ph[2];
+    int *hflags;       // per 64-column block of h: 1 once its gate_up tile is written
+    int *hcount;       // gate_up tiles written so far
+    int *exit_count;   // CTAs done; the last one clears hflags, hcount and this word
+};
+
 // Persistent standard-orientation kernel (tokens on the 128-row MMA side,
 // weights on N = 256), one tile = 128 tokens x 256 output columns, full K.
 struct StdParams {
@@ -66,6 +76,7 @@ struct StdParams {
 constexpr int kSwapAbThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kStdThreads = 192;
 constexpr int kMaxStages = 12;
+constexpr int kMaxKbs = 4;            // k-blocks per pipeline stage (issue group)
 constexpr int kMaxGrid = 160;         // cap on stream-K grids (one CTA per SM)
 constexpr int kMaxPersistentGrid = 160; // cap on the persistent prefill grids
 
@@ -79,6 +90,9 @@ int std_stages();
 
 cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
                           bool pdl, cudaStream_t s);
+// The one-launch decode layer (grid <= SMs, one CTA per SM).
+cudaError_t launch_swapab_mlp(int epi1, const CUtensorMap &ta0, const CUtensorMap &tb0, const CUtensorMap &ta1,
+                              const CUtensorMap &tb1, const SwapAbMlpParams &fp, int grid, bool pdl, cudaStream_t s);
 cudaError_t launch_std(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const StdParams &p, int grid, bool pdl,
                        cudaStream_t s);
 // CTA-pair kernel: 256 tokens x 256 columns per tile, grid = 2 x clusters.
