@@ -207,10 +207,10 @@ MSE_API mse_status merged_proj_reorder(const mse_bf16 *rank_major, mse_bf16 *log
  * at all (cudaMalloc can synchronise the device and fail under memory pressure).
  * This entry point computes exactly what mlp_swiglu_forward computes, with the
  * same arguments minus the workspace: its scratch (h, split-K partial tiles,
- * tile counters) is a fixed 24 MiB file-scope device array inside the library,
+ * tile counters) is a fixed 32 MiB file-scope device array inside the library,
  * which every device that loads the library holds until the process exits.
  *
- *  - Limit: mlp_swiglu_workspace_bytes(T, H, I) <= 24 MiB, e.g. T <= 64 tokens
+ *  - Limit: mlp_swiglu_workspace_bytes(T, H, I) <= 32 MiB, e.g. T <= 64 tokens
  *    at hidden 7168 / intermediate 6144.  Larger calls return MSE_ERR_WORKSPACE
  *    and launch nothing.
  *  - It calls no cudaMalloc, cudaFree or allocating library routine.
@@ -255,10 +255,16 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *   MSE_TUNE_CACHE_HINTS  1 = weights evict-first / tokens evict-last in L2 (default), 0 = none
  *   MSE_TUNE_GRID         CTAs of the stream-K grid (0 = one per SM, default; at most 160)
  *   MSE_TUNE_SPIN_WAIT    1 = pipeline waits poll (mbarrier.test_wait) instead of suspending
- *   MSE_TUNE_ONE_LAUNCH   1 = at decode token counts (T <= 256) gate_up + SiluAndMul and the
- *                         down projection run as two phases of one cooperative launch, the
- *                         down weights streaming while the last gate_up tiles finish
- *                         (default); 0 = two launches
+ *   MSE_TUNE_ONE_LAUNCH   decode token counts (T <= 256): 0 = gate_up + SiluAndMul and the down
+ *                         projection as two launches (default: with programmatic dependent
+ *                         launch this measured fastest); 1 = as passes of one launch, the down
+ *                         weights streaming while the last gate_up tiles finish; 2 = one
+ *                         launch with the gate_up tiles in two halves, the down pass taking
+ *                         the first half's k-blocks first (replicated layer, else as 1)
+ *   MSE_TUNE_PDL          1 = kernels are launched with programmatic dependent launch: a kernel
+ *                         starts while the previous one in the stream drains and fetches its
+ *                         first weight tiles before waiting for it (default); 0 = plain
+ *                         stream order
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -267,7 +273,8 @@ typedef enum {
     MSE_TUNE_CACHE_HINTS = 3,
     MSE_TUNE_GRID = 4,
     MSE_TUNE_SPIN_WAIT = 6,
-    MSE_TUNE_ONE_LAUNCH = 7
+    MSE_TUNE_ONE_LAUNCH = 7,
+    MSE_TUNE_PDL = 8
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

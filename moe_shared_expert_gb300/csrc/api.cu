@@ -19,7 +19,7 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_path{MSE_PATH_AUTO};
 std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
-    g_tune_spin_wait{0}, g_tune_one_launch{1};
+    g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -86,13 +86,14 @@ int pow2_at_least(int v) {
 }
 
 // ----------------------------------------------------------------- workspace
-// h | split-K slots of the gate_up pass | split-K slots of the down pass | counters of
-// the gate_up tiles | counters of the down tiles | h-tile flags | exit and h-tile counts.  The
+// h | split-K slots of the (first) gate_up pass | of the down pass | of the second gate_up
+// pass | counters of the gate_up tiles | counters of the down tiles | h-tile flags | exit
+// and published-tile counts.  The
 // region from the first counter to the end must be zero before a call and is left
 // zero by every call that completes.
 struct MlpWs {
-    size_t h_off = 0, slots_off = 0, slots_dn_off = 0, cnt_gu_off = 0, cnt_dn_off = 0, flags_off = 0, exit_off = 0,
-           total = 0;
+    size_t h_off = 0, slots_off = 0, slots_dn_off = 0, slots_gu2_off = 0, cnt_gu_off = 0, cnt_dn_off = 0,
+           flags_off = 0, exit_off = 0, total = 0;
 };
 
 constexpr int64_t kSwapAbMaxT = 256;   // token counts served by the swap-AB kernels
@@ -109,14 +110,16 @@ MlpWs mlp_ws_layout(int64_t T, int64_t H, int64_t I) {
         off = align_up(off + slot_region, 256);
         w.slots_dn_off = off;
         off = align_up(off + slot_region, 256);
+        w.slots_gu2_off = off;
+        off = align_up(off + slot_region, 256);
         w.cnt_gu_off = off;
         off = align_up(off + (size_t)((I + 63) / 64) * 4, 256);
         w.cnt_dn_off = off;
         off = align_up(off + (size_t)((I + 63) / 64) * (size_t)((H + 127) / 128) * 4, 256);
         w.flags_off = off;
         off = align_up(off + (size_t)((I + 63) / 64) * 4, 256);
-        w.exit_off = off;   // exit counter, then the count of published h tiles
-        off = align_up(off + 8, 256);
+        w.exit_off = off;   // exit count, then the published-tile counts of the two gate_up passes
+        off = align_up(off + 12, 256);
     }
     w.total = off;
     return w;
@@ -241,6 +244,7 @@ tc::SwapAbParams swapab_base(int64_t T, int total_units) {
     while (max_stages < 2 && p.kbs > 1) max_stages = tc::swapab_stages_for(p.bn, --p.kbs);
     const int want = g_tune_stages.load();
     p.stages = (want >= 2 && want < max_stages) ? want : max_stages;
+    p.halves = 1;
     p.cache_hints = g_tune_cache_hints.load();
     p.spin_wait = g_tune_spin_wait.load();
     p.tmem_cols = pow2_at_least(2 * p.bn);
@@ -249,6 +253,8 @@ tc::SwapAbParams swapab_base(int64_t T, int total_units) {
     p.wait_limit_ns = g_wait_limit_ns.load();
     return p;
 }
+
+bool use_pdl() { return g_tune_pdl.load() != 0; }
 
 int swapab_grid(const DeviceInfo &d, int total_units) {
     int g = d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid;
@@ -308,7 +314,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         p.slots = reinterpret_cast<float *>(ws + L.slots_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_gu_off);
         p.err = d.err;
-        return from_cuda(tc::launch_swapab(tc::EPI_SWIGLU, ta, tb, p, swapab_grid(d, p.total_units), true, s));
+        return from_cuda(tc::launch_swapab(tc::EPI_SWIGLU, ta, tb, p, swapab_grid(d, p.total_units), use_pdl(), s));
     }
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
@@ -328,7 +334,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         p.ldo = I;
         p.err = d.err;
         return from_cuda(tc::launch_pair(tc::EPI_SWIGLU, ta, tb, p,
-                                         pair_clusters(d, (int64_t)p.n_mtiles * p.n_ntiles), true, s));
+                                         pair_clusters(d, (int64_t)p.n_mtiles * p.n_ntiles), use_pdl(), s));
     }
     if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
     if ((st = map_gate_up_halves(&tb, w_gate_up, H, I, 128)) != MSE_OK) return st;
@@ -342,7 +348,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
     p.ldo = I;
     p.err = d.err;
     const int64_t n_tiles = (int64_t)p.n_mtiles * p.n_ntiles;
-    return from_cuda(tc::launch_std(tc::EPI_SWIGLU, ta, tb, p, std_grid(d, n_tiles), true, s));
+    return from_cuda(tc::launch_std(tc::EPI_SWIGLU, ta, tb, p, std_grid(d, n_tiles), use_pdl(), s));
 }
 
 // out[g] = h[:, slice g] . W_down[:, slice g]^T for groups g, slices of `s_width`
@@ -370,7 +376,7 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
         p.slots = reinterpret_cast<float *>(ws + L.slots_dn_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_dn_off);
         p.err = d.err;
-        return from_cuda(tc::launch_swapab(epi, ta, tb, p, swapab_grid(d, p.total_units), true, s));
+        return from_cuda(tc::launch_swapab(epi, ta, tb, p, swapab_grid(d, p.total_units), use_pdl(), s));
     }
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
@@ -392,7 +398,7 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
         p.o_group_stride = T * H;
         p.err = d.err;
         return from_cuda(tc::launch_pair(epi, ta, tb, p,
-                                         pair_clusters(d, (int64_t)groups * p.n_mtiles * p.n_ntiles), true, s));
+                                         pair_clusters(d, (int64_t)groups * p.n_mtiles * p.n_ntiles), use_pdl(), s));
     }
     if ((st = map_2d(&ta, h, T, I, I, 128)) != MSE_OK) return st;
     if ((st = map_2d(&tb, w_down, H, I, I, 256)) != MSE_OK) return st;
@@ -408,7 +414,7 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
     p.o_group_stride = T * H;
     p.err = d.err;
     const int64_t n_tiles = (int64_t)groups * p.n_mtiles * p.n_ntiles;
-    return from_cuda(tc::launch_std(epi, ta, tb, p, std_grid(d, n_tiles), true, s));
+    return from_cuda(tc::launch_std(epi, ta, tb, p, std_grid(d, n_tiles), use_pdl(), s));
 }
 
 // The decode-size layer in one launch: gate_up + SiluAndMul over intermediate columns
@@ -423,17 +429,21 @@ mse_status tc_mlp_one_launch(const DeviceInfo &d, const uint16_t *x, int64_t T, 
     mse_status st;
     const int n0 = (int)(width / 64), kbp0 = (int)(H / 64);
     const int n1 = (int)((H + 127) / 128), kbp1 = (int)(s_width / 64);
+    // two gate_up passes (first and second half of the tiles) when the down pass can take
+    // its k-blocks in matching halves
+    const bool two = g_tune_one_launch.load() == 2 && groups == 1 && n0 >= 2 && n0 % 2 == 0 && kbp1 == n0;
+    const int n0a = two ? n0 / 2 : n0;
     tc::SwapAbMlpParams fp;
     std::memset(&fp, 0, sizeof fp);
     tc::SwapAbParams &p0 = fp.ph[0];
-    tc::SwapAbParams &p1 = fp.ph[1];
-    p0 = swapab_base(T, n0 * kbp0);
-    p1 = swapab_base(T, groups * n1 * kbp1);
+    tc::SwapAbParams &p1 = fp.ph[2];
+    p0 = swapab_base(T, n0a * kbp0);
+    p1 = swapab_base(T, groups * n1 * (two ? kbp1 / 2 : kbp1));
     if ((st = map_2d(&ta0, w_gate_up, 2 * I, H, H, 64)) != MSE_OK) return st;
     if ((st = map_2d(&tb0, x, T, H, H, p0.bn)) != MSE_OK) return st;
     if ((st = map_2d(&ta1, w_down, H, I, I, 128)) != MSE_OK) return st;
     if ((st = map_2d(&tb1, h, T, I, I, p1.bn)) != MSE_OK) return st;
-    p0.n_mtiles = n0;
+    p0.n_mtiles = n0a;
     p0.n_groups = 1;
     p0.kb_per_tile = kbp0;
     p0.a_row_base = (int)j0;
@@ -446,7 +456,8 @@ mse_status tc_mlp_one_launch(const DeviceInfo &d, const uint16_t *x, int64_t T, 
     p0.err = d.err;
     p1.n_mtiles = n1;
     p1.n_groups = groups;
-    p1.kb_per_tile = kbp1;
+    p1.kb_per_tile = two ? kbp1 / 2 : kbp1;
+    p1.halves = two ? 2 : 1;
     p1.kb_first = (int)(j0 / 64);
     p1.kb_group_stride = kbp1;
     p1.m_valid = H;
@@ -456,14 +467,28 @@ mse_status tc_mlp_one_launch(const DeviceInfo &d, const uint16_t *x, int64_t T, 
     p1.slots = reinterpret_cast<float *>(ws + L.slots_dn_off);
     p1.counters = reinterpret_cast<int *>(ws + L.cnt_dn_off);
     p1.err = d.err;
+    fp.n_gate_up_passes = 1;
+    if (two) {
+        tc::SwapAbParams &pb = fp.ph[1];
+        pb = p0;
+        pb.a_row_base = (int)j0 + n0a * 64;
+        pb.n_mtiles = n0 - n0a;
+        pb.total_units = pb.n_mtiles * kbp0;
+        pb.slots = reinterpret_cast<float *>(ws + L.slots_gu2_off);
+        pb.counters = p0.counters + n0a;
+        fp.n_gate_up_passes = 2;
+    }
     fp.hflags = reinterpret_cast<int *>(ws + L.flags_off);
+    fp.hflag_first = (int)(j0 / 64);
+    fp.n_htiles = n0;
     fp.hcount = reinterpret_cast<int *>(ws + L.exit_off) + 1;
     fp.exit_count = reinterpret_cast<int *>(ws + L.exit_off);
-    // every CTA needs units in both phases: a split tile counts one part per CTA in
-    // the range of its owners
-    const int units = p0.total_units < p1.total_units ? p0.total_units : p1.total_units;
+    // every CTA needs units in every pass: a split tile counts one part per CTA in the
+    // range of its owners
+    int units = p0.total_units < p1.total_units ? p0.total_units : p1.total_units;
+    if (two && fp.ph[1].total_units < units) units = fp.ph[1].total_units;
     const int grid = swapab_grid(d, units);
-    return from_cuda(tc::launch_swapab_mlp(epi1, ta0, tb0, ta1, tb1, fp, grid, true, s));
+    return from_cuda(tc::launch_swapab_mlp(epi1, ta0, tb0, ta1, tb1, fp, grid, use_pdl(), s));
 }
 
 bool one_launch_enabled(int64_t T) { return T <= kSwapAbMaxT && g_tune_one_launch.load() != 0; }
@@ -678,7 +703,7 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
         p.slots = reinterpret_cast<float *>(ws + L.slots_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_off);
         p.err = d->err;
-        return from_cuda(tc::launch_swapab(tc::EPI_MERGED, ta, tb, p, swapab_grid(*d, p.total_units), true, s));
+        return from_cuda(tc::launch_swapab(tc::EPI_MERGED, ta, tb, p, swapab_grid(*d, p.total_units), use_pdl(), s));
     }
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
@@ -699,7 +724,7 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
         p.q_dim = q_dim; p.kv_dim = kv_dim; p.tp = tp;
         p.err = d->err;
         return from_cuda(tc::launch_pair(tc::EPI_MERGED, ta, tb, p,
-                                         pair_clusters(*d, (int64_t)p.n_mtiles * p.n_ntiles), true, s));
+                                         pair_clusters(*d, (int64_t)p.n_mtiles * p.n_ntiles), use_pdl(), s));
     }
     if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
     if ((st = map_2d(&tb, w, C, H, H, 256)) != MSE_OK) return st;
@@ -713,7 +738,7 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
     p.out_rm = out_rank_major;
     p.q_dim = q_dim; p.kv_dim = kv_dim; p.tp = tp;
     p.err = d->err;
-    return from_cuda(tc::launch_std(tc::EPI_MERGED, ta, tb, p, std_grid(*d, (int64_t)p.n_mtiles * p.n_ntiles), true, s));
+    return from_cuda(tc::launch_std(tc::EPI_MERGED, ta, tb, p, std_grid(*d, (int64_t)p.n_mtiles * p.n_ntiles), use_pdl(), s));
 }
 
 mse_status merged_proj_reorder(const mse_bf16 *rank_major, mse_bf16 *logical, int64_t T, int64_t q_dim,
@@ -770,7 +795,8 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_CACHE_HINTS: slot = &g_tune_cache_hints; ok = value == 0 || value == 1; break;
         case MSE_TUNE_GRID: slot = &g_tune_grid; ok = value >= 0 && value <= tc::kMaxGrid; break;
         case MSE_TUNE_SPIN_WAIT: slot = &g_tune_spin_wait; ok = value == 0 || value == 1; break;
-        case MSE_TUNE_ONE_LAUNCH: slot = &g_tune_one_launch; ok = value == 0 || value == 1; break;
+        case MSE_TUNE_ONE_LAUNCH: slot = &g_tune_one_launch; ok = value >= 0 && value <= 2; break;
+        case MSE_TUNE_PDL: slot = &g_tune_pdl; ok = value == 0 || value == 1; break;
         default: return -1;
     }
     if (!ok) return -1;

@@ -15,11 +15,11 @@ void mlp_workspace_counter_range(int64_t T, int64_t H, int64_t I, size_t *off, s
 
 namespace {
 
-// 24 MiB: enough for the decode-size shared-expert layer (T <= 64 tokens at
-// hidden 7168 / intermediate 6144 needs 20.8 MiB: h, the split-K partial tiles of
-// both passes and the sync words).  Every device that loads the library holds this
+// 32 MiB: enough for the decode-size shared-expert layer (T <= 64 tokens at
+// hidden 7168 / intermediate 6144 needs 30.8 MiB: h, the split-K partial tiles of
+// the three passes and the sync words).  Every device that loads the library holds this
 // array until the process exits.
-constexpr size_t kStaticScratchBytes = (size_t)24 << 20;
+constexpr size_t kStaticScratchBytes = (size_t)32 << 20;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;

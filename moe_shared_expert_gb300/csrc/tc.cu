@@ -232,66 +232,103 @@ struct SwapAbSmem {
     __device__ __forceinline__ uint32_t b(int st) const { return a(st) + a_stage_bytes; }
 };
 
-// The CTA's units [ub, ue) of one phase form segments (one per tile touched); each
-// segment is cut into stages of up to kbs consecutive k-blocks.  Producer and MMA
-// walk the same sequence with incremental counters (no divisions inside the loops).
-struct Walk {
-    int64_t u, ue;
-    int kbp, n_mtiles;
-    int kb, kb_end, m, group;   // the current stage starts at k-block kb of tile (group, m)
-    int seg;                    // segments completed in this phase
-    __device__ void init(int64_t ub_, int64_t ue_, int kbp_, int n_mtiles_) {
-        u = ub_; ue = ue_; kbp = kbp_; n_mtiles = n_mtiles_; seg = 0;
-        const int64_t tile = ub_ / kbp_;
-        kb = (int)(ub_ - tile * kbp_);
-        group = (int)(tile / n_mtiles_);
-        m = (int)(tile - (int64_t)group * n_mtiles_);
-        set_end();
+// The work of one CTA in one pass.  The pass's units are (tile, u), u in [0, kbu), split
+// stream-K over the grid; the CTA's range [ub, ue) touches `nseg` consecutive tiles (its
+// segments).  With halves == 1 unit u is k-block u of the tile and a segment is one run
+// of k-blocks.  With halves == 2 unit u stands for the two k-blocks u and kbu + u: each
+// segment is processed as two runs (first halves, then second halves), and when the CTA
+// touches at most two tiles the first halves of all its segments come before the second
+// halves, so that both of its accumulators are open at once.
+struct Plan {
+    int64_t ub, ue, tile0;
+    int kbu, halves, n_mtiles, nseg;
+    bool inter;
+    __device__ void init(const SwapAbParams &p) {
+        const StreamK sk{p.total_units, gridDim.x};
+        ub = sk.begin(blockIdx.x);
+        ue = sk.begin(blockIdx.x + 1);
+        kbu = p.kb_per_tile;
+        halves = p.halves;
+        n_mtiles = p.n_mtiles;
+        tile0 = ub / kbu;
+        nseg = ue > ub ? (int)((ue - 1) / kbu - tile0 + 1) : 0;
+        inter = halves == 2 && nseg <= 2;
     }
-    __device__ void set_end() {
-        const int64_t rem = ue - u;
-        kb_end = (kbp - kb) < rem ? kbp : kb + (int)rem;
+    __device__ int nruns() const { return nseg * halves; }
+    __device__ void run(int r, int &seg, int &half) const {
+        if (halves == 1) { seg = r; half = 0; }
+        else if (inter) { half = r >= nseg ? 1 : 0; seg = r - half * nseg; }
+        else { seg = r >> 1; half = r & 1; }
     }
-    __device__ bool done() const { return u >= ue; }
-    __device__ int count(int kbs) const { return (kb_end - kb) < kbs ? (kb_end - kb) : kbs; }
-    // advance past a stage of n k-blocks; true when that stage ended its segment
-    __device__ bool advance(int n) {
-        kb += n;
-        u += n;
-        if (kb < kb_end) return false;
-        kb = 0;
-        ++seg;
-        if (++m == n_mtiles) { m = 0; ++group; }
-        set_end();
-        return true;
+    // tile of segment s and its unit range [kb0, kb1) within the tile
+    __device__ void seg_range(int s, int64_t &tile, int &kb0, int &kb1) const {
+        tile = tile0 + s;
+        const int64_t t0 = tile * kbu;
+        kb0 = (int)(ub > t0 ? ub - t0 : 0);
+        kb1 = (int)(ue < t0 + kbu ? ue - t0 : kbu);
     }
 };
 
-__device__ __forceinline__ Walk cta_walk(const SwapAbParams &p) {
-    const StreamK sk{p.total_units, gridDim.x};
-    Walk w;
-    w.init(sk.begin(blockIdx.x), sk.begin(blockIdx.x + 1), p.kb_per_tile, p.n_mtiles);
-    return w;
-}
+// Stages of a Plan in order: runs cut into stages of up to kbs k-blocks.
+struct StageIter {
+    const Plan *pl;
+    int r, nr;            // current run, number of runs
+    int kb, kb1;          // stage start and run end (units within the tile)
+    int half, group, m;   // of the current run
+    __device__ void start(const Plan &p) {
+        pl = &p;
+        nr = p.nruns();
+        r = -1;
+        kb = kb1 = 0;
+        next_run();
+    }
+    __device__ void next_run() {
+        while (kb >= kb1 && ++r < nr) {
+            int seg;
+            pl->run(r, seg, half);
+            int64_t tile;
+            pl->seg_range(seg, tile, kb, kb1);
+            group = (int)(tile / pl->n_mtiles);
+            m = (int)(tile - (int64_t)group * pl->n_mtiles);
+        }
+    }
+    __device__ bool done() const { return r >= nr; }
+    __device__ int count(int kbs) const { return (kb1 - kb) < kbs ? (kb1 - kb) : kbs; }
+    __device__ void advance(int n) {
+        kb += n;
+        if (kb >= kb1) next_run();
+    }
+    // k-block index, within the group's reduction, of the i-th k-block of the stage
+    __device__ int kblock(int i) const { return half * pl->kbu + kb + i; }
+};
 
 // ---- producer (one elected thread of warp 0) ----
 // pdl_prologue: the weight tiles of the first stages are requested before waiting for
-//   the previous kernel of the stream, the token tiles after that wait (first phase).
+//   the previous kernel of the stream, the token tiles after that wait (first pass).
 // hflags: the token operand is the intermediate h written earlier in this launch; a
 //   stage's token tiles are requested once every gate_up tile they read has been
 //   published there, while weight tiles keep filling the free stages meanwhile.
 // `issued` counts stages whose loads were requested.  Returns false after an abort.
+// The h flags of a launch: flags[first + t] is set once the gate_up tile writing h
+// columns 64 (first + t) .. is published; tiles t < n0 belong to gate_up pass 0, the
+// next n1 to pass 1, and counts[k] is the number of tiles pass k has published.
+struct HFlags {
+    const int *flags;
+    const int *counts;
+    int first, n0, n1;
+};
+
 template <int EPI>
 __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB, Ctrl *ctl,
-                               const SwapAbSmem &sm, RingPos &r, int &issued, bool pdl_prologue, const int *hflags,
-                               const int *hcount, int n_htiles, volatile int *abort_flag) {
+                               const SwapAbSmem &sm, RingPos &r, int &issued, bool pdl_prologue, const HFlags *hf,
+                               volatile int *abort_flag) {
     const int S = p.stages, KBS = p.kbs;
     const uint32_t kb_tx = kATileBytes + sm.b_tile_bytes;
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_x = l2_policy_evict_last();
     const bool hints = p.cache_hints != 0;
-    auto kglob = [&](const Walk &w, int i) { return p.kb_first + w.group * p.kb_group_stride + w.kb + i; };
-    auto load_a = [&](const Walk &w, int n, int st) {
+    auto kglob = [&](const StageIter &w, int i) { return p.kb_first + w.group * p.kb_group_stride + w.kblock(i); };
+    auto load_a = [&](const StageIter &w, int n, int st) {
         const uint32_t fb = bar_addr(&ctl->full[st]);
         for (int i = 0; i < n; ++i) {
             const int k = kglob(w, i) * 64;
@@ -312,7 +349,7 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
             }
         }
     };
-    auto load_b = [&](const Walk &w, int n, int st) {
+    auto load_b = [&](const StageIter &w, int n, int st) {
         const uint32_t fb = bar_addr(&ctl->full[st]);
         for (int i = 0; i < n; ++i) {
             const int k = kglob(w, i) * 64;
@@ -321,10 +358,13 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
             else tma_load_2d_nohint(dst, tmB, fb, k, 0);
         }
     };
-    Walk w = cta_walk(p);
+    Plan pl;
+    pl.init(p);
+    StageIter w;
+    w.start(pl);
     if (pdl_prologue) {
         // the ring is fresh: stages 0.. in their first use
-        Walk a = w;
+        StageIter a = w;
         int st = 0;
         for (; st < S && !a.done(); ++st) {
             const int n = a.count(KBS);
@@ -342,7 +382,7 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
         r.stage = st == S ? 0 : st;
         r.phase = st == S ? 1u : 0u;
     }
-    if (!hflags) {
+    if (!hf) {
         while (!w.done()) {
             if (!mbar_wait_bounded(bar_addr(&ctl->empty[r.stage]), r.phase ^ 1u, abort_flag, p.wait_limit_ns, p.err,
                                    p.spin_wait != 0))
@@ -361,13 +401,16 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
     // follows with the token tiles once their h columns are published.  After an abort
     // the pending token tiles are still requested (without waiting) so that every
     // issued stage completes and the teardown drain ends.
-    // Flags are polled with relaxed loads (all of a stage's at once) and one fence once
-    // they are seen set; after the count of published tiles reaches n_htiles no flag is
-    // read again.
-    Walk wb = w;
+    // Readiness is read with relaxed loads, at most every 256 ns (polling harder slows the
+    // publishers): first the published counts of the passes the stage reads; a pass
+    // found complete is never read again; while one is not, the stage's flags of that
+    // pass.  One fence follows the poll that finds the stage ready.
+    StageIter wb = w;
     RingPos rb = r;
     int pending = 0;
-    bool aborted = false, all_ready = false;
+    bool aborted = false;
+    bool done0 = hf->n0 == 0, done1 = hf->n1 == 0;   // pass complete
+    uint64_t next_poll = 0;
     uint64_t idle_since = 0;
     while (true) {
         bool progress = false;
@@ -384,17 +427,45 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
         if (pending > 0) {
             const int n = wb.count(KBS);
             bool ready = true;
-            if (!aborted && !all_ready) {
-                if (ld_relaxed_gpu(hcount) >= n_htiles) {
-                    all_ready = true;
-                } else {
-                    int f[kMaxKbs];
+            if (!aborted) {
+                int fi[kMaxKbs];
+                bool in1[kMaxKbs];
+                bool need0 = false, need1 = false;
 #pragma unroll
-                    for (int i = 0; i < kMaxKbs; ++i) f[i] = i < n ? ld_relaxed_gpu(hflags + kglob(wb, i)) : 1;
-#pragma unroll
-                    for (int i = 0; i < kMaxKbs; ++i) ready = ready && f[i] != 0;
+                for (int i = 0; i < kMaxKbs; ++i) {
+                    fi[i] = i < n ? kglob(wb, i) : hf->first;
+                    in1[i] = fi[i] >= hf->first + hf->n0;
+                    if (i < n) {
+                        if (in1[i]) need1 = need1 || !done1;
+                        else need0 = need0 || !done0;
+                    }
                 }
-                if (ready) fence_acq_rel_gpu();   // acquire the publishers' h stores
+                if (need0 || need1) {
+                    ready = false;
+                    const uint64_t now = global_timer_ns();
+                    if (now >= next_poll) {
+                        const int c0 = need0 ? ld_relaxed_gpu(hf->counts) : 0;
+                        const int c1 = need1 ? ld_relaxed_gpu(hf->counts + 1) : 0;
+                        if (need0 && c0 >= hf->n0) done0 = true;
+                        if (need1 && c1 >= hf->n1) done1 = true;
+                        bool all = true;
+                        bool polled = false;
+#pragma unroll
+                        for (int i = 0; i < kMaxKbs; ++i) {
+                            if (i < n && !(in1[i] ? done1 : done0)) {
+                                polled = true;
+                                all = all && ld_relaxed_gpu(hf->flags + fi[i]) != 0;
+                            }
+                        }
+                        (void)polled;
+                        if (all) {
+                            fence_acq_rel_gpu();   // acquire the publishers' h stores
+                            ready = true;
+                        } else {
+                            next_poll = now + 256;
+                        }
+                    }
+                }
             }
             if (ready) {
                 fence_proxy_async_global();   // h was written through the generic proxy
@@ -428,26 +499,38 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
 }
 
 // ---- MMA issuer (one elected thread of warp 1) ----
-// Segment `gseg` (counted over all phases) accumulates in TMEM buffer gseg & 1.
+// Segment s of the pass accumulates in TMEM buffer (gseg + s) & 1, gseg counting the
+// segments of earlier passes; its first run starts the accumulator, its last run
+// hands it to the epilogue.
 __device__ bool swapab_mma(const SwapAbParams &p, Ctrl *ctl, const SwapAbSmem &sm, RingPos &r, int &gseg,
                            uint32_t tmem_base, volatile int *abort_flag) {
     const int S = p.stages, KBS = p.kbs;
     const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)p.bn);
-    Walk w = cta_walk(p);
-    while (!w.done()) {
-        const int buf = gseg & 1;
-        const uint32_t use = (uint32_t)(gseg >> 1);
-        if (!mbar_wait_bounded(bar_addr(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, p.wait_limit_ns, p.err))
-            return false;
-        tc_fence_after();
+    Plan pl;
+    pl.init(p);
+    const int nr = pl.nruns();
+    for (int rr = 0; rr < nr; ++rr) {
+        int seg, half;
+        pl.run(rr, seg, half);
+        int64_t tile;
+        int kb0, kb1;
+        pl.seg_range(seg, tile, kb0, kb1);
+        const int g = gseg + seg;
+        const int buf = g & 1;
+        const uint32_t use = (uint32_t)(g >> 1);
+        if (half == 0) {
+            if (!mbar_wait_bounded(bar_addr(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, p.wait_limit_ns, p.err))
+                return false;
+            tc_fence_after();
+        }
         const uint32_t d = tmem_base + (uint32_t)(buf * (p.tmem_cols / 2));
-        bool first = true, seg_end = false;
-        while (!seg_end) {
+        bool first = half == 0;
+        for (int kb = kb0; kb < kb1;) {
+            const int n = (kb1 - kb) < KBS ? (kb1 - kb) : KBS;
             if (!mbar_wait_bounded(bar_addr(&ctl->full[r.stage]), r.phase, abort_flag, p.wait_limit_ns, p.err,
                                    p.spin_wait != 0))
                 return false;
             tc_fence_after();
-            const int n = w.count(KBS);
             for (int i = 0; i < n; ++i) {
                 const uint64_t ad = smem_desc_sw128(sm.a(r.stage) + (uint32_t)i * kATileBytes);
                 const uint64_t bd = smem_desc_sw128(sm.b(r.stage) + (uint32_t)i * sm.b_tile_bytes);
@@ -459,17 +542,17 @@ __device__ bool swapab_mma(const SwapAbParams &p, Ctrl *ctl, const SwapAbSmem &s
             }
             tc_commit(bar_addr(&ctl->empty[r.stage]));
             r.next(S);
-            seg_end = w.advance(n);
+            kb += n;
         }
-        tc_commit(bar_addr(&ctl->tfull[buf]));
-        ++gseg;
+        if (half == pl.halves - 1) tc_commit(bar_addr(&ctl->tfull[buf]));
     }
+    gseg += pl.nseg;
     return true;
 }
 
 // Publication of a finished gate_up tile (m) for readers of h in the same launch: every
-// epilogue thread's h stores, then one GPU-scope release of the tile's flag and of the
-// count of published tiles.
+// epilogue thread's h stores, then GPU-scope releases of the tile's flag and of the
+// pass's count of published tiles.
 __device__ __forceinline__ void publish_h_tile(const SwapAbParams &p, int *hflags, int *hcount, int m) {
     fence_proxy_async_global();
     named_barrier_sync(1, 128);
@@ -480,9 +563,9 @@ __device__ __forceinline__ void publish_h_tile(const SwapAbParams &p, int *hflag
 }
 
 // ---- epilogue (warps 2..5, 128 threads) ----
-// ring_idle_at_end: after this phase's last MMA the ring is idle, so a split tile
+// ring_idle_at_end: after this pass's last MMA the ring is idle, so a split tile
 //   finished in the CTA's last segment may stage the parts in the ring's memory.
-// hflags: publish each completed tile (gate_up phase of the fused layer).
+// hflags: publish each completed tile (gate_up passes of the fused layer).
 template <int EPI>
 __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring, uint32_t ring_base,
                                 uint32_t ring_bytes, int &gseg, uint32_t &fix_round, uint32_t tmem_base,
@@ -495,19 +578,20 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
     const int bn = p.bn, kbp = p.kb_per_tile;
     const int nchunks = bn / 16;
     const StreamK sk{p.total_units, gridDim.x};
-    const int64_t ub = sk.begin(blockIdx.x), ue = sk.begin(blockIdx.x + 1);
+    Plan pl;
+    pl.init(p);
     const size_t slot_floats = (size_t)128 * bn;
-    for (int64_t u = ub; u < ue;) {
-        const int64_t tile = u / kbp;
-        const int kb0 = (int)(u % kbp);
-        const int64_t rem = ue - u;
-        const int kb1 = (int)((kbp - kb0) < rem ? kbp : kb0 + rem);
-        const int buf = gseg & 1;
-        const uint32_t use = (uint32_t)(gseg >> 1);
+    const int gbase = gseg;
+    gseg += pl.nseg;
+    for (int s = 0; s < pl.nseg; ++s) {
+        int64_t tile;
+        int kb0, kb1;
+        pl.seg_range(s, tile, kb0, kb1);
+        const int g = gbase + s;
+        const int buf = g & 1;
+        const uint32_t use = (uint32_t)(g >> 1);
         const int group = (int)(tile / p.n_mtiles);
-        const int m = (int)(tile % p.n_mtiles);
-        u = tile * kbp + kb1;
-        ++gseg;
+        const int m = (int)(tile - (int64_t)group * p.n_mtiles);
         const bool got = mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
         if (!named_barrier_and(1, 128, got)) return false;   // all epilogue warps take the same branch
         tc_fence_after();
@@ -525,7 +609,8 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         }
         // Tile shared with other CTAs: park the fp32 partial in this CTA's slot, laid
         // out [token column][accumulator row] (each warp store is a 128-byte run).
-        const int which = (ub / kbp == tile) ? 0 : 1;
+        // A CTA's first segment uses its slot 0, a later one its slot 1.
+        const int which = s == 0 ? 0 : 1;
         float *slot = p.slots + ((size_t)blockIdx.x * 2 + which) * slot_floats;
         for (int c = 0; c < nchunks; ++c) {
             float v[16];
@@ -533,7 +618,9 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
 #pragma unroll
             for (int i = 0; i < 16; ++i) __stcg(slot + (size_t)(c * 16 + i) * 128 + row, v[i]);
         }
-        fence_proxy_async_global();   // a finisher may fetch this slot with a bulk copy
+        tc_fence_before();
+        mbar_arrive(bar_addr(&ctl->tempty[buf]));
+        if (ring_idle_at_end) fence_proxy_async_global();   // a finisher may fetch this slot with a bulk copy
         named_barrier_sync(1, 128);
         const int64_t c_first = sk.owner(tile * kbp), c_last = sk.owner(tile * kbp + kbp - 1);
         const int nseg = (int)(c_last - c_first + 1);
@@ -545,14 +632,12 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         }
         named_barrier_sync(1, 128);
         if (!ctl->fin_flag) {
-            tc_fence_before();
-            mbar_arrive(bar_addr(&ctl->tempty[buf]));
             named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
             continue;
         }
         // This CTA arrived last: sum the parts in ascending part (CTA) order starting
         // from 0, so the result does not depend on which CTA finishes the tile.
-        // slot of each part: CTA cc's first segment uses slot 2cc, its last one 2cc+1
+        // Slot of each part: CTA cc's first segment uses slot 2cc, a later one 2cc+1.
         for (int k = tid; k < nseg && k < 128; k += 128) {
             const int64_t cc = c_first + k;
             ctl->seg_slot[k] = (int)(cc * 2 + ((sk.begin(cc) >= tile * kbp) ? 0 : 1));
@@ -564,11 +649,9 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         };
         const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
         const int per_round = (int)(ring_bytes / slot_bytes);
-        if (ring_idle_at_end && u == ue && per_round >= 2 && nseg <= 128) {
-            // Last segment of the phase with the ring idle: the parts are bulk-copied into
+        if (ring_idle_at_end && s == pl.nseg - 1 && per_round >= 2 && nseg <= 128) {
+            // Last segment of the pass with the ring idle: the parts are bulk-copied into
             // the ring's memory (buffer 0 keeps the running sum) and summed element-wise.
-            tc_fence_before();
-            mbar_arrive(bar_addr(&ctl->tempty[buf]));
             fence_proxy_async_global();
             float *buf0 = reinterpret_cast<float *>(ring);
             bool fix_ok = true;
@@ -600,22 +683,22 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
                 for (int e = tid; e < n4; e += 512) {    // 4 independent float4 per thread per step
                     float4 a[4];
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        a[r] = b0[e + r * 128];
-                        if (k0 == 0) a[r] = make_float4(0.f + a[r].x, 0.f + a[r].y, 0.f + a[r].z, 0.f + a[r].w);
+                    for (int rr = 0; rr < 4; ++rr) {
+                        a[rr] = b0[e + rr * 128];
+                        if (k0 == 0) a[rr] = make_float4(0.f + a[rr].x, 0.f + a[rr].y, 0.f + a[rr].z, 0.f + a[rr].w);
                     }
                     for (int bb = 1; bb < nsum; ++bb) {
                         const float4 *src = reinterpret_cast<const float4 *>(buf0 + (size_t)bb * slot_floats);
                         float4 t4[4];
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) t4[r] = src[e + r * 128];
+                        for (int rr = 0; rr < 4; ++rr) t4[rr] = src[e + rr * 128];
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            a[r].x += t4[r].x; a[r].y += t4[r].y; a[r].z += t4[r].z; a[r].w += t4[r].w;
+                        for (int rr = 0; rr < 4; ++rr) {
+                            a[rr].x += t4[rr].x; a[rr].y += t4[rr].y; a[rr].z += t4[rr].z; a[rr].w += t4[rr].w;
                         }
                     }
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) b0[e + r * 128] = a[r];
+                    for (int rr = 0; rr < 4; ++rr) b0[e + rr * 128] = a[rr];
                 }
                 k0 += nload;
                 named_barrier_sync(1, 128);   // buffers 1.. are refilled by the next round
@@ -623,11 +706,9 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
             if (!fix_ok) return false;
             swapab_epilogue_smem<EPI>(p, buf0, group, m, tid);
         } else {
-            // In registers: this CTA's own part straight from tensor memory (its buffer is
-            // released afterwards), the others from their slots in L2; two chunks of 16
-            // tokens x two parts per round keep 64 loads per thread in flight.
+            // In registers, every part from its slot in L2: two chunks of 16 tokens x two
+            // parts per round keep 64 loads per thread in flight.
             constexpr int NB = 2, NP = 2;
-            const int k_own = (int)(blockIdx.x - c_first);
             for (int c0 = 0; c0 < nchunks; c0 += NB) {
                 float acc[NB][16];
 #pragma unroll
@@ -637,35 +718,26 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
                 for (int k0 = 0; k0 < nseg; k0 += NP) {
                     float t[NP][NB][16];
 #pragma unroll
-                    for (int s = 0; s < NP; ++s) {
-                        const int k = k0 + s;
-                        if (k < nseg && k != k_own) {
-                            const float *src = p.slots + (size_t)slot_of(k) * slot_floats + row;
+                    for (int sp = 0; sp < NP; ++sp) {
+                        if (k0 + sp < nseg) {
+                            const float *src = p.slots + (size_t)slot_of(k0 + sp) * slot_floats + row;
 #pragma unroll
                             for (int b = 0; b < NB; ++b) {
                                 if (c0 + b < nchunks) {
 #pragma unroll
                                     for (int i = 0; i < 16; ++i)
-                                        t[s][b][i] = __ldcg(src + (size_t)((c0 + b) * 16 + i) * 128);
+                                        t[sp][b][i] = __ldcg(src + (size_t)((c0 + b) * 16 + i) * 128);
                                 }
                             }
                         }
                     }
 #pragma unroll
-                    for (int s = 0; s < NP; ++s) {
-                        if (k0 + s == k_own) {
-#pragma unroll
-                            for (int b = 0; b < NB; ++b)
-                                if (c0 + b < nchunks) load_tmem_chunk(tacc + (uint32_t)((c0 + b) * 16), t[s][b]);
-                        }
-                    }
-#pragma unroll
-                    for (int s = 0; s < NP; ++s) {
-                        if (k0 + s < nseg) {
+                    for (int sp = 0; sp < NP; ++sp) {
+                        if (k0 + sp < nseg) {
 #pragma unroll
                             for (int b = 0; b < NB; ++b)
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) acc[b][i] += t[s][b][i];
+                                for (int i = 0; i < 16; ++i) acc[b][i] += t[sp][b][i];
                         }
                     }
                 }
@@ -673,8 +745,6 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
                 for (int b = 0; b < NB; ++b)
                     if (c0 + b < nchunks) swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c0 + b, acc[b]);
             }
-            tc_fence_before();
-            mbar_arrive(bar_addr(&ctl->tempty[buf]));
         }
         if (threadIdx.x == 64) p.counters[tile] = 0;
         if (hflags) publish_h_tile(p, hflags, hcount, m);
@@ -754,7 +824,7 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             RingPos r;
-            (void)swapab_produce<EPI>(p, &tmA, &tmB, ctl, sm, r, issued, true, nullptr, nullptr, 0, abort_flag);
+            (void)swapab_produce<EPI>(p, &tmA, &tmB, ctl, sm, r, issued, true, nullptr, abort_flag);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -773,21 +843,25 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
 }
 
 // The whole shared-expert layer at decode token counts in one launch:
-//   phase 0  h = silu(x W_gate^T) * (x W_up^T)   (stream-K over gate_up tiles)
-//   phase 1  out = h W_down^T                     (stream-K over down tiles)
-// Every CTA runs its share of phase 0 and then its share of phase 1 through the same
-// ring.  Phase-1 weight tiles stream into stages as soon as phase-0 MMAs free them;
-// its token tiles (h) wait for the flag of the gate_up tile that writes them.  One
-// CTA per SM and grid <= SMs: every CTA is resident once the previous work on the
-// stream leaves, and every wait is bounded.  The last CTA to leave clears the flags
-// and counts, so the sync words are zero again on exit.
+//   gate_up passes  h = silu(x W_gate^T) * (x W_up^T)   (stream-K over gate_up tiles)
+//   down pass       out = h W_down^T                     (stream-K over down tiles)
+// Every CTA runs its share of each pass in turn through the same ring.  Down weight
+// tiles stream into stages as soon as gate_up MMAs free them; their token tiles (h)
+// wait for the flag of the gate_up tile that writes them.  With two gate_up passes
+// (the first and the second half of the tiles) the first half's tiles are finished
+// while the second half streams, and the down pass takes its units as pairs of
+// k-blocks from the two halves, the first-half k-blocks first: the second half's
+// split-K tail then overlaps down work.  One CTA per SM and grid <= SMs: every CTA is
+// resident once the previous work on the stream leaves, and every wait is bounded.
+// The last CTA to leave clears the flags and counts, so the sync words are zero again.
 template <int EPI1>
 __global__ void __launch_bounds__(kSwapAbThreads, 1)
     swapab_mlp_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                       const SwapAbMlpParams fp) {
     const SwapAbParams &p0 = fp.ph[0];
-    const SwapAbParams &p1 = fp.ph[1];
+    const SwapAbParams &pd = fp.ph[2];
+    const int n_gu = fp.n_gate_up_passes;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -806,34 +880,42 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             RingPos r;
-            if (swapab_produce<EPI_SWIGLU>(p0, &tmA0, &tmB0, ctl, sm, r, issued, true, nullptr, nullptr, 0,
-                                           abort_flag))
-                (void)swapab_produce<EPI1>(p1, &tmA1, &tmB1, ctl, sm, r, issued, false, fp.hflags, fp.hcount,
-                                           p0.n_mtiles, abort_flag);
+            bool ok = true;
+            for (int ph = 0; ph < n_gu && ok; ++ph)
+                ok = swapab_produce<EPI_SWIGLU>(fp.ph[ph], &tmA0, &tmB0, ctl, sm, r, issued, ph == 0, nullptr,
+                                                abort_flag);
+            const HFlags hf = {fp.hflags, fp.hcount, fp.hflag_first, fp.ph[0].n_mtiles,
+                               n_gu == 2 ? fp.ph[1].n_mtiles : 0};
+            if (ok) (void)swapab_produce<EPI1>(pd, &tmA1, &tmB1, ctl, sm, r, issued, false, &hf, abort_flag);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             RingPos r;
             int gseg = 0;
-            if (swapab_mma(p0, ctl, sm, r, gseg, tmem_base, abort_flag))
-                (void)swapab_mma(p1, ctl, sm, r, gseg, tmem_base, abort_flag);
+            bool ok = true;
+            for (int ph = 0; ph < n_gu && ok; ++ph) ok = swapab_mma(fp.ph[ph], ctl, sm, r, gseg, tmem_base, abort_flag);
+            if (ok) (void)swapab_mma(pd, ctl, sm, r, gseg, tmem_base, abort_flag);
         }
     } else {
         pdl_wait();
         int gseg = 0;
         uint32_t fix_round = 0;
         const uint32_t ring_bytes = (uint32_t)S * sm.stage_bytes;
-        if (swapab_epilogue<EPI_SWIGLU>(p0, ctl, ring, base, ring_bytes, gseg, fix_round, tmem_base, false, fp.hflags,
-                                        fp.hcount, abort_flag))
-            (void)swapab_epilogue<EPI1>(p1, ctl, ring, base, ring_bytes, gseg, fix_round, tmem_base, true, nullptr,
+        bool ok = true;
+        for (int ph = 0; ph < n_gu && ok; ++ph)
+            ok = swapab_epilogue<EPI_SWIGLU>(fp.ph[ph], ctl, ring, base, ring_bytes, gseg, fix_round, tmem_base, false,
+                                             fp.hflags, fp.hcount + ph, abort_flag);
+        if (ok)
+            (void)swapab_epilogue<EPI1>(pd, ctl, ring, base, ring_bytes, gseg, fix_round, tmem_base, true, nullptr,
                                         nullptr, abort_flag);
     }
     swapab_teardown(ctl, S, issued, tmem_base, p0.tmem_cols, p0.wait_limit_ns);
     if (threadIdx.x == 0 && !*abort_flag) {
         // every flag read of this CTA precedes this increment; the last CTA clears them
         if (atomic_add_acq_rel_gpu(fp.exit_count, 1) == (int)gridDim.x - 1) {
-            for (int t = 0; t < p0.n_mtiles; ++t) fp.hflags[p0.a_row_base / 64 + t] = 0;
-            *fp.hcount = 0;
+            for (int t = 0; t < fp.n_htiles; ++t) fp.hflags[fp.hflag_first + t] = 0;
+            fp.hcount[0] = 0;
+            fp.hcount[1] = 0;
             *fp.exit_count = 0;
         }
     }

@@ -19,7 +19,8 @@ enum Epi : int {
 struct SwapAbParams {
     int n_mtiles;          // 128-row A tiles per group
     int n_groups;          // independent outputs (shards); 1 when replicated
-    int kb_per_tile;       // 64-wide k-blocks reduced by one tile
+    int kb_per_tile;       // units per tile: 64-wide k-blocks (halves = 1) or pairs of them (halves = 2)
+    int halves;            // 2: unit u of a tile stands for k-blocks u and kb_per_tile + u
     int kb_first;          // k-block index of group 0's first block
     int kb_group_stride;   // k-block offset between groups
     int total_units;       // n_groups * n_mtiles * kb_per_tile
@@ -42,14 +43,17 @@ struct SwapAbParams {
     uint32_t *err;
 };
 
-// The decode-size shared-expert layer in one launch: phase 0 = gate_up + SiluAndMul
-// into h (EPI_SWIGLU), phase 1 = down projection of h (EPI_BF16 or EPI_F32, groups =
-// shards).  Both phases use the same bn, stages and kbs.
+// The decode-size shared-expert layer in one launch: one or two gate_up + SiluAndMul
+// passes into h (EPI_SWIGLU; ph[0], ph[1]), then the down projection of h (ph[2];
+// EPI_BF16 or EPI_F32, groups = shards).  All passes use the same bn, stages and kbs.
 struct SwapAbMlpParams {
-    SwapAbParams ph[2];
-    int *hflags;       // per 64-column block of h: 1 once its gate_up tile is written
-    int *hcount;       // gate_up tiles written so far
-    int *exit_count;   // CTAs done; the last one clears hflags, hcount and this word
+    SwapAbParams ph[3];
+    int n_gate_up_passes;   // 1 or 2
+    int *hflags;            // per 64-column block of h: 1 once its gate_up tile is written
+    int hflag_first;        // first flag index of this launch's h columns
+    int n_htiles;           // gate_up tiles (flags) of this launch
+    int *hcount;            // [2]: tiles published so far by gate_up pass 0 / pass 1
+    int *exit_count;        // CTAs done; the last one clears hflags, hcount and this word
 };
 
 // Persistent standard-orientation kernel (tokens on the 128-row MMA side,

@@ -1,8 +1,10 @@
-"""The decode-size layer as one cooperative launch (gate_up + SiluAndMul, then the
-down projection, in two phases of one kernel) against the fp64 oracle, against the
-two-launch path, and across repeated calls, CUDA-graph replays and shard subsets.
+"""The decode-size layer as one launch (gate_up + SiluAndMul passes, then the down
+projection, in one kernel) against the fp64 oracle, against the two-launch path,
+and across repeated calls, CUDA-graph replays and shard subsets.  Mode 1 runs one
+gate_up pass; mode 2 (the default) two half passes with the down pass taking the
+first half's k-blocks first.
 
-The down phase reads h tiles that other CTAs of the same launch write; per-tile
+The down pass reads h tiles that other CTAs of the same launch write; per-tile
 flags order the two.  These tests check the results of that hand-off and that
 every completed call leaves the workspace's sync words zero for the next one.
 """
@@ -34,9 +36,9 @@ def _lib():
 
 
 @contextlib.contextmanager
-def one_launch(on: bool):
-    old = mse.set_tuning(mse.TUNE_ONE_LAUNCH, 1 if on else 0)
-    assert old in (0, 1)
+def one_launch(mode: int):
+    old = mse.set_tuning(mse.TUNE_ONE_LAUNCH, int(mode))
+    assert old in (0, 1, 2)
     try:
         yield
     finally:
@@ -51,11 +53,11 @@ def case(T, H, I, seed):
 
 
 def sync_region_offset(T, H, I):
-    """Start of the counters/flags region of an mlp workspace (after h and the two
+    """Start of the counters/flags region of an mlp workspace (after h and the three
     split-K slot regions of 160 CTAs x 2 slots x 128 x bn fp32)."""
     a = lambda v: (v + 255) // 256 * 256
     bn = (T + 15) // 16 * 16
-    return a(T * I * 2) + 2 * a(160 * 2 * 128 * bn * 4)
+    return a(T * I * 2) + 3 * a(160 * 2 * 128 * bn * 4)
 
 
 def forward(x, wgu, wd, ws=None):
@@ -67,28 +69,30 @@ def forward(x, wgu, wd, ws=None):
     return to_bits(y), ws
 
 
+@pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("T,H,I", [(1, 384, 320), (7, 384, 320), (24, 512, 256), (64, 1024, 768),
-                                   (100, 640, 448), (256, 384, 320)])
-def test_one_launch_matches_oracle_and_two_launches(T, H, I):
+                                   (100, 640, 448), (256, 384, 320), (40, 768, 640)])
+def test_one_launch_matches_oracle_and_two_launches(T, H, I, mode):
     x, wgu, wd = case(T, H, I, 7000 + T + H)
     y_ref, _, _ = oracle.mlp_forward(x, wgu, wd)
-    with one_launch(True):
+    with one_launch(mode):
         y1, ws = forward(x, wgu, wd)
-    with one_launch(False):
+    with one_launch(0):
         y2, _ = forward(x, wgu, wd)
-    assert_close(bits_f64(y1), bits_f64(y_ref), f"one launch T={T}")
+    assert_close(bits_f64(y1), bits_f64(y_ref), f"one launch (mode {mode}) T={T}")
     assert_close(bits_f64(y2), bits_f64(y_ref), f"two launches T={T}")
     tail = ws[sync_region_offset(T, H, I):]
     assert int(torch.count_nonzero(tail).item()) == 0, "sync words not left zero"
 
 
-def test_one_launch_decode_t64_sampled_rows():
+@pytest.mark.parametrize("mode", [1, 2])
+def test_one_launch_decode_t64_sampled_rows(mode):
     w = W.DECODE_T64
     wgu, wd = W.make_mlp_weights(w)
     x = W.make_x(w)
     rows = [0, 17, 31, 63]
     y_ref, _, _ = oracle.mlp_forward(x[rows], wgu, wd)
-    with one_launch(True):
+    with one_launch(mode):
         y, ws = forward(x, wgu, wd)
         y_again, _ = forward(x, wgu, wd, ws)
     assert_close(bits_f64(y[rows]), bits_f64(y_ref), "decode T=64 one launch")
@@ -104,7 +108,7 @@ def test_one_launch_alternating_inputs_on_one_workspace():
     refs = [oracle.mlp_forward(*c)[0] for c in cases]
     ws = mse.new_mlp_workspace(T, H, I)
     dev = [tuple(to_dev(a) for a in c) for c in cases]
-    with one_launch(True):
+    with one_launch(2):
         for it in range(6):
             k = it % 2
             y = mse.mlp_swiglu_forward(*dev[k], workspace=ws)
@@ -115,7 +119,7 @@ def test_one_launch_alternating_inputs_on_one_workspace():
 def test_one_launch_shard_partials():
     T, H, I, tp = 32, 768, 384, 3
     x, wgu, wd = case(T, H, I, 7200)
-    with one_launch(True):
+    with one_launch(2):
         parts = mse.mlp_swiglu_shard_partial(to_dev(x), to_dev(wgu), to_dev(wd), tp, partial_dtype=torch.float32)
         sub = mse.mlp_swiglu_shard_partial(to_dev(x), to_dev(wgu), to_dev(wd), tp, rank_first=1, rank_count=2,
                                            partial_dtype=torch.float32)
@@ -137,7 +141,7 @@ def test_one_launch_cuda_graph_replay():
     dgu, dwd = to_dev(wgu), to_dev(wd)
     ws = mse.new_mlp_workspace(T, H, I)
     y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-    with one_launch(True):
+    with one_launch(2):
         mse.mlp_swiglu_forward(dx, dgu, dwd, y, ws)   # set-up outside the capture
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
