@@ -265,6 +265,12 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         starts while the previous one in the stream drains and fetches its
  *                         first weight tiles before waiting for it (default); 0 = plain
  *                         stream order
+ *   MSE_TUNE_COOP_FINISH  merged projection at decode token counts: a tile whose reduction is
+ *                         split between at least this many CTAs (0..128; 0 = never) is
+ *                         finished jointly by the CTAs for which it is the final segment: each
+ *                         waits (bounded) for all parts, then sums and writes one slice of the
+ *                         tile's token columns.  Other split tiles are finished by the CTA
+ *                         arriving last.  Default 6
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -274,7 +280,8 @@ typedef enum {
     MSE_TUNE_GRID = 4,
     MSE_TUNE_SPIN_WAIT = 6,
     MSE_TUNE_ONE_LAUNCH = 7,
-    MSE_TUNE_PDL = 8
+    MSE_TUNE_PDL = 8,
+    MSE_TUNE_COOP_FINISH = 9
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

@@ -19,7 +19,8 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_path{MSE_PATH_AUTO};
 std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
-    g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1};
+    g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
+    g_tune_coop_finish{6};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -247,6 +248,7 @@ tc::SwapAbParams swapab_base(int64_t T, int total_units) {
     p.halves = 1;
     p.cache_hints = g_tune_cache_hints.load();
     p.spin_wait = g_tune_spin_wait.load();
+    p.coop_finish = g_tune_coop_finish.load();
     p.tmem_cols = pow2_at_least(2 * p.bn);
     p.T = (int)T;
     p.total_units = total_units;
@@ -797,6 +799,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_SPIN_WAIT: slot = &g_tune_spin_wait; ok = value == 0 || value == 1; break;
         case MSE_TUNE_ONE_LAUNCH: slot = &g_tune_one_launch; ok = value >= 0 && value <= 2; break;
         case MSE_TUNE_PDL: slot = &g_tune_pdl; ok = value == 0 || value == 1; break;
+        case MSE_TUNE_COOP_FINISH: slot = &g_tune_coop_finish; ok = value >= 0 && value <= 128; break;
         default: return -1;
     }
     if (!ok) return -1;

@@ -152,50 +152,56 @@ __device__ __forceinline__ void swapab_epilogue_chunk(const SwapAbParams &p, Ctr
     }
 }
 
-// Epilogue of a whole swap-AB tile held in shared memory as fp32 [token][row]
-// (row = accumulator row, 128 per token).  All 128 epilogue threads (tid 0..127)
-// work element-wise: a fixed row per thread, tokens strided, so shared reads are
-// conflict-free and the 32 lanes of a warp store 32 consecutive outputs.
+// Epilogue of token columns [t0, t1) of a swap-AB tile held in shared memory as fp32
+// [token][row] (row = accumulator row, 128 per token; tilebuf starts at column t0).
+// All 128 epilogue threads (tid 0..127) work element-wise: a fixed row per thread,
+// tokens strided, so shared reads are conflict-free and the 32 lanes of a warp store
+// 32 consecutive outputs.
 template <int EPI>
 __device__ __forceinline__ void swapab_epilogue_smem(const SwapAbParams &p, const float *tilebuf, int group, int m,
-                                                     int tid) {
+                                                     int tid, int t0, int t1) {
+    if (t1 > p.T) t1 = p.T;
     if constexpr (EPI == EPI_SWIGLU) {
         // rows 0-63: g of j = j0 + r; rows 64-127: u of the same j
         const int jr = tid & 63;
         uint16_t *h = static_cast<uint16_t *>(p.out) + (int64_t)p.a_row_base + (int64_t)m * 64 + jr;
-        int t = tid >> 6;
-        for (; t + 6 < p.T; t += 8) {   // 4 tokens per step, computed before storing
+        int t = t0 + (tid >> 6);
+        for (; t + 6 < t1; t += 8) {   // 4 tokens per step, computed before storing
             uint16_t hv[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-                hv[r] = f32_to_bf16_bits(silu_f32(tilebuf[(t + 2 * r) * 128 + jr]) * tilebuf[(t + 2 * r) * 128 + 64 + jr]);
+            for (int r = 0; r < 4; ++r) {
+                const float *c = tilebuf + (t + 2 * r - t0) * 128;
+                hv[r] = f32_to_bf16_bits(silu_f32(c[jr]) * c[64 + jr]);
+            }
 #pragma unroll
             for (int r = 0; r < 4; ++r) h[(int64_t)(t + 2 * r) * p.ldo] = hv[r];
         }
-        for (; t < p.T; t += 2)
-            h[(int64_t)t * p.ldo] = f32_to_bf16_bits(silu_f32(tilebuf[t * 128 + jr]) * tilebuf[t * 128 + 64 + jr]);
+        for (; t < t1; t += 2) {
+            const float *c = tilebuf + (t - t0) * 128;
+            h[(int64_t)t * p.ldo] = f32_to_bf16_bits(silu_f32(c[jr]) * c[64 + jr]);
+        }
     } else {
         const int64_t n = (int64_t)m * 128 + tid;
         if (n >= p.m_valid) return;
         if constexpr (EPI == EPI_F32) {
             float *o = static_cast<float *>(p.out) + group * p.o_group_stride + n;
-            for (int t = 0; t < p.T; ++t) o[(int64_t)t * p.ldo] = tilebuf[t * 128 + tid];
+            for (int t = t0; t < t1; ++t) o[(int64_t)t * p.ldo] = tilebuf[(t - t0) * 128 + tid];
         } else if constexpr (EPI == EPI_BF16) {
             uint16_t *o = static_cast<uint16_t *>(p.out) + group * p.o_group_stride + n;
-            int t = 0;
-            for (; t + 3 < p.T; t += 4) {
+            int t = t0;
+            for (; t + 3 < t1; t += 4) {
                 uint16_t b[4];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) b[r] = f32_to_bf16_bits(tilebuf[(t + r) * 128 + tid]);
+                for (int r = 0; r < 4; ++r) b[r] = f32_to_bf16_bits(tilebuf[(t + r - t0) * 128 + tid]);
 #pragma unroll
                 for (int r = 0; r < 4; ++r) o[(int64_t)(t + r) * p.ldo] = b[r];
             }
-            for (; t < p.T; ++t) o[(int64_t)t * p.ldo] = f32_to_bf16_bits(tilebuf[t * 128 + tid]);
+            for (; t < t1; ++t) o[(int64_t)t * p.ldo] = f32_to_bf16_bits(tilebuf[(t - t0) * 128 + tid]);
         } else {
             uint16_t *lo = static_cast<uint16_t *>(p.out);
             const int64_t gcol = logical_to_gathered(n, p.q_dim, p.kv_dim, p.tp);
-            for (int t = 0; t < p.T; ++t) {
-                const uint16_t b = f32_to_bf16_bits(tilebuf[t * 128 + tid]);
+            for (int t = t0; t < t1; ++t) {
+                const uint16_t b = f32_to_bf16_bits(tilebuf[(t - t0) * 128 + tid]);
                 if (lo) lo[(int64_t)t * p.ldo + n] = b;
                 if (p.out_rm) p.out_rm[(int64_t)t * p.ldo + gcol] = b;
             }
@@ -550,6 +556,79 @@ __device__ bool swapab_mma(const SwapAbParams &p, Ctrl *ctl, const SwapAbSmem &s
     return true;
 }
 
+// Sum, in ascending part order starting from 0, token columns [c0, c1) of the nseg parts
+// listed in ctl->seg_slot (nseg <= 128), staged in the idle ring's shared memory by bulk
+// copies (buffer 0 keeps the running sum; each round refills buffers 1..), then run the
+// epilogue on those columns.  All 128 epilogue threads call it; false after an abort.
+template <int EPI>
+__device__ bool finish_cols_smem(const SwapAbParams &p, Ctrl *ctl, float *ring, uint32_t ring_base,
+                                 uint32_t ring_bytes, uint32_t &fix_round, int nseg, int c0, int c1, int group,
+                                 int m, int tid, volatile int *abort_flag) {
+    const size_t slot_floats = (size_t)128 * p.bn;
+    const uint32_t sl_bytes = (uint32_t)(c1 - c0) * 512u;   // 128 fp32 rows per token column
+    const int n4 = (c1 - c0) * 32;                           // float4 of the slice
+    const int per_round = (int)(ring_bytes / sl_bytes);
+    fence_proxy_async_global();
+    int k0 = 0;
+    while (k0 < nseg) {
+        const int first_buf = k0 == 0 ? 0 : 1;
+        const int nload = min(nseg - k0, per_round - first_buf);
+        if (threadIdx.x == 64) {
+            mbar_arrive_expect_tx(bar_addr(&ctl->fixbar), (uint32_t)nload * sl_bytes);
+            for (int i = 0; i < nload; ++i)
+                bulk_load(ring_base + (uint32_t)(first_buf + i) * sl_bytes,
+                          p.slots + (size_t)ctl->seg_slot[k0 + i] * slot_floats + (size_t)c0 * 128, sl_bytes,
+                          bar_addr(&ctl->fixbar));
+        }
+        const bool got_fix =
+            mbar_wait_bounded(bar_addr(&ctl->fixbar), fix_round & 1u, abort_flag, p.wait_limit_ns, p.err);
+        ++fix_round;
+        if (!named_barrier_and(1, 128, got_fix)) {
+            // copies into the ring may still be in flight: let them land first
+            if (threadIdx.x == 64)
+                (void)mbar_wait_drain(bar_addr(&ctl->fixbar), (fix_round - 1) & 1u, drain_limit_ns(p.wait_limit_ns));
+            return false;
+        }
+        const int nsum = first_buf + nload;
+        float4 *b0 = reinterpret_cast<float4 *>(ring);
+        const size_t bstride = sl_bytes / 16;   // float4 per buffer
+        int e = tid;
+        for (; e + 384 < n4; e += 512) {   // 4 independent float4 per thread per step
+            float4 a[4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                a[rr] = b0[e + rr * 128];
+                if (k0 == 0) a[rr] = make_float4(0.f + a[rr].x, 0.f + a[rr].y, 0.f + a[rr].z, 0.f + a[rr].w);
+            }
+            for (int bb = 1; bb < nsum; ++bb) {
+                const float4 *src = b0 + (size_t)bb * bstride;
+                float4 t4[4];
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) t4[rr] = src[e + rr * 128];
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    a[rr].x += t4[rr].x; a[rr].y += t4[rr].y; a[rr].z += t4[rr].z; a[rr].w += t4[rr].w;
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) b0[e + rr * 128] = a[rr];
+        }
+        for (; e < n4; e += 128) {
+            float4 a = b0[e];
+            if (k0 == 0) a = make_float4(0.f + a.x, 0.f + a.y, 0.f + a.z, 0.f + a.w);
+            for (int bb = 1; bb < nsum; ++bb) {
+                const float4 t4 = b0[(size_t)bb * bstride + e];
+                a.x += t4.x; a.y += t4.y; a.z += t4.z; a.w += t4.w;
+            }
+            b0[e] = a;
+        }
+        k0 += nload;
+        named_barrier_sync(1, 128);   // buffers 1.. are refilled by the next round
+    }
+    swapab_epilogue_smem<EPI>(p, ring, group, m, tid, c0, c1);
+    return true;
+}
+
 // Publication of a finished gate_up tile (m) for readers of h in the same launch: every
 // epilogue thread's h stores, then GPU-scope releases of the tile's flag and of the
 // pass's count of published tiles.
@@ -624,6 +703,60 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         named_barrier_sync(1, 128);
         const int64_t c_first = sk.owner(tile * kbp), c_last = sk.owner(tile * kbp + kbp - 1);
         const int nseg = (int)(c_last - c_first + 1);
+        // Cooperative finish (the ring is idle after the pass, the tile has at least
+        // coop_finish parts): every part for which the tile is its CTA's final segment
+        // waits for all parts, then sums and finishes its own slice of token columns.  Only the last CTA's part can be a non-final segment
+        // (the tile is that CTA's first); it hands its part over and goes on.  All parts
+        // of the tile take the same decision.
+        // (compiled into the merged-projection kernel only: its tiles are split about nine
+        // ways; the MLP kernels' tiles are split two to four ways, where the CTA arriving
+        // last finishing alone measured faster)
+        int n_fin = 0;   // parts that finish jointly; 0: the CTA arriving last finishes alone
+        if constexpr (EPI == EPI_MERGED) {
+            if (ring_idle_at_end && p.coop_finish > 0 && nseg >= p.coop_finish && nseg <= 128) {
+                n_fin = nseg - (sk.begin(c_last + 1) <= (tile + 1) * kbp ? 0 : 1);
+                if (ring_bytes / ((uint32_t)((bn + n_fin - 1) / n_fin) * 512u) < 2) n_fin = 0;
+            }
+        }
+        if (n_fin > 0) {
+            if (s != pl.nseg - 1) {
+                if (threadIdx.x == 64) (void)atomic_add_acq_rel_gpu(p.counters + tile, 1);
+                continue;
+            }
+            if (threadIdx.x == 64) {
+                (void)atomic_add_acq_rel_gpu(p.counters + tile, 1);
+                bool ok = true;
+                const uint64_t t0 = global_timer_ns();
+                while (ld_acquire_gpu(p.counters + tile) < nseg) {
+                    if (*abort_flag) { ok = false; break; }
+                    if (global_timer_ns() - t0 > p.wait_limit_ns) {
+                        *abort_flag = 1;
+                        raise_device_error(p.err, DEV_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                }
+                ctl->fin_flag = ok ? 1 : 0;
+            }
+            named_barrier_sync(1, 128);
+            if (!ctl->fin_flag) return false;
+            for (int k = tid; k < nseg; k += 128) {
+                const int64_t cc = c_first + k;
+                ctl->seg_slot[k] = (int)(cc * 2 + ((sk.begin(cc) >= tile * kbp) ? 0 : 1));
+            }
+            named_barrier_sync(1, 128);
+            const int idx = (int)(blockIdx.x - c_first);
+            const int col0 = idx * bn / n_fin, col1 = (idx + 1) * bn / n_fin;
+            if (col1 > col0 && !finish_cols_smem<EPI>(p, ctl, reinterpret_cast<float *>(ring), ring_base, ring_bytes,
+                                                       fix_round, nseg, col0, col1, group, m, tid, abort_flag))
+                return false;
+            if (threadIdx.x == 64) {
+                // every finisher is past its wait once all have counted themselves here
+                if (atomic_add_acq_rel_gpu(p.counters + tile, 1) == nseg + n_fin - 1) p.counters[tile] = 0;
+            }
+            named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
+            continue;
+        }
         if (threadIdx.x == 64) {
             // release: the barrier above orders every epilogue thread's slot stores
             // before this atomic; acquire: the finisher then sees all other parts
@@ -648,63 +781,12 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
                            : (int)((c_first + k) * 2 + ((sk.begin(c_first + k) >= tile * kbp) ? 0 : 1));
         };
         const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
-        const int per_round = (int)(ring_bytes / slot_bytes);
-        if (ring_idle_at_end && s == pl.nseg - 1 && per_round >= 2 && nseg <= 128) {
-            // Last segment of the pass with the ring idle: the parts are bulk-copied into
-            // the ring's memory (buffer 0 keeps the running sum) and summed element-wise.
-            fence_proxy_async_global();
-            float *buf0 = reinterpret_cast<float *>(ring);
-            bool fix_ok = true;
-            int k0 = 0;
-            while (k0 < nseg) {
-                const int first_buf = k0 == 0 ? 0 : 1;
-                const int nload = min(nseg - k0, per_round - first_buf);
-                if (threadIdx.x == 64) {
-                    mbar_arrive_expect_tx(bar_addr(&ctl->fixbar), (uint32_t)nload * slot_bytes);
-                    for (int i = 0; i < nload; ++i)
-                        bulk_load(ring_base + (uint32_t)(first_buf + i) * slot_bytes,
-                                  p.slots + (size_t)ctl->seg_slot[k0 + i] * slot_floats, slot_bytes,
-                                  bar_addr(&ctl->fixbar));
-                }
-                const bool got_fix = mbar_wait_bounded(bar_addr(&ctl->fixbar), fix_round & 1u, abort_flag,
-                                                       p.wait_limit_ns, p.err);
-                ++fix_round;
-                if (!named_barrier_and(1, 128, got_fix)) {
-                    // copies into the ring may still be in flight: let them land first
-                    if (threadIdx.x == 64)
-                        (void)mbar_wait_drain(bar_addr(&ctl->fixbar), (fix_round - 1) & 1u,
-                                              drain_limit_ns(p.wait_limit_ns));
-                    fix_ok = false;
-                    break;
-                }
-                const int nsum = first_buf + nload;
-                float4 *b0 = reinterpret_cast<float4 *>(buf0);
-                const int n4 = (int)(slot_floats / 4);   // a multiple of 512
-                for (int e = tid; e < n4; e += 512) {    // 4 independent float4 per thread per step
-                    float4 a[4];
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) {
-                        a[rr] = b0[e + rr * 128];
-                        if (k0 == 0) a[rr] = make_float4(0.f + a[rr].x, 0.f + a[rr].y, 0.f + a[rr].z, 0.f + a[rr].w);
-                    }
-                    for (int bb = 1; bb < nsum; ++bb) {
-                        const float4 *src = reinterpret_cast<const float4 *>(buf0 + (size_t)bb * slot_floats);
-                        float4 t4[4];
-#pragma unroll
-                        for (int rr = 0; rr < 4; ++rr) t4[rr] = src[e + rr * 128];
-#pragma unroll
-                        for (int rr = 0; rr < 4; ++rr) {
-                            a[rr].x += t4[rr].x; a[rr].y += t4[rr].y; a[rr].z += t4[rr].z; a[rr].w += t4[rr].w;
-                        }
-                    }
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) b0[e + rr * 128] = a[rr];
-                }
-                k0 += nload;
-                named_barrier_sync(1, 128);   // buffers 1.. are refilled by the next round
-            }
-            if (!fix_ok) return false;
-            swapab_epilogue_smem<EPI>(p, buf0, group, m, tid);
+        if (ring_idle_at_end && s == pl.nseg - 1 && ring_bytes / slot_bytes >= 2 && nseg <= 128) {
+            // Last segment of the pass with the ring idle: the parts are staged in the
+            // ring's memory and summed there.
+            if (!finish_cols_smem<EPI>(p, ctl, reinterpret_cast<float *>(ring), ring_base, ring_bytes, fix_round,
+                                       nseg, 0, bn, group, m, tid, abort_flag))
+                return false;
         } else {
             // In registers, every part from its slot in L2: two chunks of 16 tokens x two
             // parts per round keep 64 loads per thread in flight.

@@ -33,6 +33,9 @@ struct SwapAbParams {
                            // kbs x 128 contiguous bytes at a time; DRAM row-buffer locality)
     int cache_hints;       // 1: weights evict_first, tokens evict_last in L2; 0: no hints
     int spin_wait;         // 1: pipeline waits poll without suspending the thread
+    int coop_finish;       // > 0: a tile split into at least this many parts, in the CTAs' final
+                           // segments, is finished jointly (each part's CTA sums one slice of
+                           // token columns) when the ring is idle; 0: never
     int T;                 // valid tokens
     int64_t m_valid;       // valid output features (A rows) for masking
     void *out; int64_t ldo; int64_t o_group_stride;
