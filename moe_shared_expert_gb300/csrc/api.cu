@@ -659,7 +659,7 @@ mse_status shard_sum(const void *partials, mse_dtype partial_dtype, int n_parts,
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
     return from_cuda(launch_shard_sum(partials, partial_dtype == MSE_F32, n_parts, T * H, out, d->sm_count,
-                                      static_cast<cudaStream_t>(stream)));
+                                      use_pdl(), static_cast<cudaStream_t>(stream)));
 }
 
 mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const mse_bf16 *w, int64_t q_dim,
@@ -755,7 +755,8 @@ mse_status merged_proj_reorder(const mse_bf16 *rank_major, mse_bf16 *logical, in
     DeviceInfo *d = nullptr;
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
-    return from_cuda(launch_reorder(rank_major, logical, T, q_dim, kv_dim, tp, static_cast<cudaStream_t>(stream)));
+    return from_cuda(
+        launch_reorder(rank_major, logical, T, q_dim, kv_dim, tp, use_pdl(), static_cast<cudaStream_t>(stream)));
 }
 
 mse_status mse_poll_device_error(void *stream) {

@@ -8,18 +8,32 @@ namespace mse {
 namespace {
 
 // out[e] = bf16( sum_{r ascending} p[r*plane + e] ), fp32 accumulate, 8 bf16 per thread-step.
+// The parts' loads are requested in batches of kPartBatch before any is summed, so a
+// thread waits for one DRAM round trip per batch, not one per part.
+constexpr int kPartBatch = 8;
+
 __global__ void __launch_bounds__(256) shard_sum_bf16_vec(const uint4 *__restrict__ p, int n_parts, int64_t plane8,
                                                           uint4 *__restrict__ out) {
+    pdl_launch_dependents();   // the next kernel may start fetching its weights
+    pdl_wait();                // inputs written by the previous kernel
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < plane8;
          i += (int64_t)gridDim.x * blockDim.x) {
         float acc[8] = {};
-        for (int r = 0; r < n_parts; ++r) {
-            const uint4 v = __ldcs(p + r * plane8 + i);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int r0 = 0; r0 < n_parts; r0 += kPartBatch) {
+            uint4 v[kPartBatch];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                acc[2 * k] += __uint_as_float(w[k] << 16);
-                acc[2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+            for (int b = 0; b < kPartBatch; ++b)
+                if (r0 + b < n_parts) v[b] = __ldcs(p + (int64_t)(r0 + b) * plane8 + i);
+#pragma unroll
+            for (int b = 0; b < kPartBatch; ++b) {
+                if (r0 + b < n_parts) {
+                    const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        acc[2 * k] += __uint_as_float(w[k] << 16);
+                        acc[2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+                    }
+                }
             }
         }
         uint32_t o[4];
@@ -32,12 +46,22 @@ __global__ void __launch_bounds__(256) shard_sum_bf16_vec(const uint4 *__restric
 
 __global__ void __launch_bounds__(256) shard_sum_f32_vec(const float4 *__restrict__ p, int n_parts, int64_t plane4,
                                                          uint2 *__restrict__ out) {
+    pdl_launch_dependents();   // the next kernel may start fetching its weights
+    pdl_wait();                // inputs written by the previous kernel
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < plane4;
          i += (int64_t)gridDim.x * blockDim.x) {
         float acc[4] = {};
-        for (int r = 0; r < n_parts; ++r) {
-            const float4 v = __ldcs(p + r * plane4 + i);
-            acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+        for (int r0 = 0; r0 < n_parts; r0 += kPartBatch) {
+            float4 v[kPartBatch];
+#pragma unroll
+            for (int b = 0; b < kPartBatch; ++b)
+                if (r0 + b < n_parts) v[b] = __ldcs(p + (int64_t)(r0 + b) * plane4 + i);
+#pragma unroll
+            for (int b = 0; b < kPartBatch; ++b) {
+                if (r0 + b < n_parts) {
+                    acc[0] += v[b].x; acc[1] += v[b].y; acc[2] += v[b].z; acc[3] += v[b].w;
+                }
+            }
         }
         out[i] = make_uint2((uint32_t)f32_to_bf16_bits(acc[0]) | ((uint32_t)f32_to_bf16_bits(acc[1]) << 16),
                             (uint32_t)f32_to_bf16_bits(acc[2]) | ((uint32_t)f32_to_bf16_bits(acc[3]) << 16));
@@ -46,6 +70,8 @@ __global__ void __launch_bounds__(256) shard_sum_f32_vec(const float4 *__restric
 
 __global__ void __launch_bounds__(256) shard_sum_scalar(const void *__restrict__ p, int is_f32, int n_parts,
                                                         int64_t plane, uint16_t *__restrict__ out) {
+    pdl_launch_dependents();   // the next kernel may start fetching its weights
+    pdl_wait();                // inputs written by the previous kernel
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < plane;
          i += (int64_t)gridDim.x * blockDim.x) {
         float acc = 0.f;
@@ -59,6 +85,8 @@ __global__ void __launch_bounds__(256) shard_sum_scalar(const void *__restrict__
 // logical[t, c] = rank_major[t, gathered(c)]; one thread per output word.
 __global__ void __launch_bounds__(256) reorder_kernel(const uint16_t *__restrict__ rm, uint16_t *__restrict__ lo,
                                                       int64_t T, int64_t C, int64_t q_dim, int64_t qs, int64_t ks) {
+    pdl_launch_dependents();   // the next kernel may start fetching its weights
+    pdl_wait();                // inputs written by the previous kernel
     const int64_t total = T * C, w = qs + ks;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -90,35 +118,48 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns, uint32_t *err) {
 
 }  // namespace
 
+// Launch with programmatic dependent launch when `pdl` (the kernels wait for their
+// predecessor before reading and let their successor start early).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ew(void (*kern)(KArgs...), int blocks, bool pdl, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_shard_sum(const void *partials, int dtype_f32, int n_parts, int64_t plane, uint16_t *out,
-                             int sm_count, cudaStream_t s) {
+                             int sm_count, bool pdl, cudaStream_t s) {
     if (plane <= 0) return cudaSuccess;
     const int blocks_cap = sm_count * 8;
     const uintptr_t pa = reinterpret_cast<uintptr_t>(partials), oa = reinterpret_cast<uintptr_t>(out);
     if (!dtype_f32 && plane % 8 == 0 && pa % 16 == 0 && oa % 16 == 0) {
         const int64_t n = plane / 8;
         const int blocks = (int)std::min<int64_t>((n + 255) / 256, blocks_cap);
-        shard_sum_bf16_vec<<<blocks, 256, 0, s>>>(static_cast<const uint4 *>(partials), n_parts, n,
-                                                  reinterpret_cast<uint4 *>(out));
+        return launch_ew(shard_sum_bf16_vec, blocks, pdl, s, static_cast<const uint4 *>(partials), n_parts, n,
+                         reinterpret_cast<uint4 *>(out));
     } else if (dtype_f32 && plane % 4 == 0 && pa % 16 == 0 && oa % 8 == 0) {
         const int64_t n = plane / 4;
         const int blocks = (int)std::min<int64_t>((n + 255) / 256, blocks_cap);
-        shard_sum_f32_vec<<<blocks, 256, 0, s>>>(static_cast<const float4 *>(partials), n_parts, n,
-                                                 reinterpret_cast<uint2 *>(out));
-    } else {
-        const int blocks = (int)std::min<int64_t>((plane + 255) / 256, blocks_cap);
-        shard_sum_scalar<<<blocks, 256, 0, s>>>(partials, dtype_f32, n_parts, plane, out);
+        return launch_ew(shard_sum_f32_vec, blocks, pdl, s, static_cast<const float4 *>(partials), n_parts, n,
+                         reinterpret_cast<uint2 *>(out));
     }
-    return cudaGetLastError();
+    const int blocks = (int)std::min<int64_t>((plane + 255) / 256, blocks_cap);
+    return launch_ew(shard_sum_scalar, blocks, pdl, s, partials, dtype_f32, n_parts, plane, out);
 }
 
 cudaError_t launch_reorder(const uint16_t *rm, uint16_t *logical, int64_t T, int64_t q_dim, int64_t kv_dim, int tp,
-                           cudaStream_t s) {
+                           bool pdl, cudaStream_t s) {
     const int64_t C = q_dim + kv_dim, total = T * C;
     if (total <= 0) return cudaSuccess;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
-    reorder_kernel<<<blocks, 256, 0, s>>>(rm, logical, T, C, q_dim, q_dim / tp, kv_dim / tp);
-    return cudaGetLastError();
+    return launch_ew(reorder_kernel, blocks, pdl, s, rm, logical, T, C, q_dim, q_dim / tp, kv_dim / tp);
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *err, cudaStream_t s) {

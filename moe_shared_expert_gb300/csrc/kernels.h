@@ -29,10 +29,11 @@ struct SimtGemmArgs {
 cudaError_t launch_simt_gemm(const SimtGemmArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- elementwise
+// pdl: launched with programmatic dependent launch (waits for its predecessor in-kernel)
 cudaError_t launch_shard_sum(const void *partials, int dtype_f32, int n_parts, int64_t plane, uint16_t *out,
-                             int sm_count, cudaStream_t s);
+                             int sm_count, bool pdl, cudaStream_t s);
 cudaError_t launch_reorder(const uint16_t *rm, uint16_t *logical, int64_t T, int64_t q_dim, int64_t kv_dim, int tp,
-                           cudaStream_t s);
+                           bool pdl, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *err, cudaStream_t s);
 
 }  // namespace mse
