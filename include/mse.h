@@ -271,6 +271,11 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         waits (bounded) for all parts, then sums and writes one slice of the
  *                         tile's token columns.  Other split tiles are finished by the CTA
  *                         arriving last.  Default 6
+ *   MSE_TUNE_PAIR_MIN_T   token counts from which the decode-size kernels run as CTA pairs: one
+ *                         256-row weight tile per pair (one M = 256 MMA over both CTAs), each
+ *                         CTA holding half of the token rows, so that more weight bytes are in
+ *                         flight per SM (0 = never, the default: at 64 and 128 tokens it
+ *                         measured no faster than single CTAs)
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -281,7 +286,8 @@ typedef enum {
     MSE_TUNE_SPIN_WAIT = 6,
     MSE_TUNE_ONE_LAUNCH = 7,
     MSE_TUNE_PDL = 8,
-    MSE_TUNE_COOP_FINISH = 9
+    MSE_TUNE_COOP_FINISH = 9,
+    MSE_TUNE_PAIR_MIN_T = 10
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

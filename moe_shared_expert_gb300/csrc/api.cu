@@ -20,7 +20,7 @@ std::atomic<int> g_path{MSE_PATH_AUTO};
 std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
     g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
-    g_tune_coop_finish{6};
+    g_tune_coop_finish{6}, g_tune_pair_min_t{0};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -236,13 +236,15 @@ mse_status map_gate_up_halves(CUtensorMap *m, const void *w, int64_t H, int64_t 
 }
 
 // ----------------------------------------------------------------- launch helpers
-tc::SwapAbParams swapab_base(int64_t T, int total_units) {
+// pair: the CTA-pair kernel, whose CTAs each hold half of the token rows
+tc::SwapAbParams swapab_base(int64_t T, int total_units, bool pair = false) {
     tc::SwapAbParams p;
     std::memset(&p, 0, sizeof p);
     p.bn = round_up16(T);
     p.kbs = g_tune_issue_group.load();
-    int max_stages = tc::swapab_stages_for(p.bn, p.kbs);
-    while (max_stages < 2 && p.kbs > 1) max_stages = tc::swapab_stages_for(p.bn, --p.kbs);
+    const int b_rows = pair ? p.bn / 2 : p.bn;
+    int max_stages = tc::swapab_stages_for(b_rows, p.kbs);
+    while (max_stages < 2 && p.kbs > 1) max_stages = tc::swapab_stages_for(b_rows, --p.kbs);
     const int want = g_tune_stages.load();
     p.stages = (want >= 2 && want < max_stages) ? want : max_stages;
     p.halves = 1;
@@ -263,6 +265,44 @@ int swapab_grid(const DeviceInfo &d, int total_units) {
     const int want = g_tune_grid.load();
     if (want > 0 && want < g) g = want;
     return g < total_units ? g : total_units;
+}
+
+// Swap-AB launch shape for n_real 128-row weight tiles per group: CTA pairs (each CTA
+// one 128-row half of a 256-row tile, half of the tokens) from MSE_TUNE_PAIR_MIN_T tokens
+// on, when the device can hold the clusters; single CTAs otherwise.  grid = workers.
+struct SwapAbShape {
+    tc::SwapAbParams p;
+    bool pair;
+    int grid;
+    int b_box_rows;   // token rows of one B copy (each CTA's half for pairs)
+};
+SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups, int kbp) {
+    SwapAbShape r;
+    const int pmin = g_tune_pair_min_t.load();
+    if (pmin > 0 && T >= pmin) {
+        const int n_mt = (n_real + 1) / 2;
+        r.p = swapab_base(T, groups * n_mt * kbp, true);
+        const int mc = tc::swapab_pair_max_clusters(r.p.bn, r.p.stages, r.p.kbs);
+        if (mc > 0) {
+            r.pair = true;
+            r.p.n_mtiles = n_mt;
+            r.p.n_mtiles_real = n_real;
+            int g = std::min(d.sm_count, tc::kMaxGrid) / 2;
+            const int want = g_tune_grid.load() / 2;
+            if (want > 0 && want < g) g = want;
+            g = std::min(g, mc);
+            r.grid = std::max(1, std::min(g, r.p.total_units));
+            r.b_box_rows = r.p.bn / 2;
+            return r;
+        }
+    }
+    r.pair = false;
+    r.p = swapab_base(T, groups * n_real * kbp, false);
+    r.p.n_mtiles = n_real;
+    r.p.n_mtiles_real = n_real;
+    r.grid = swapab_grid(d, r.p.total_units);
+    r.b_box_rows = r.p.bn;
+    return r;
 }
 
 tc::StdParams std_base(int64_t T) {
@@ -298,12 +338,11 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
     CUtensorMap ta, tb;
     mse_status st;
     if (T <= kSwapAbMaxT) {
-        const int n_mtiles = (int)(width / 64);
         const int kbp = (int)(H / 64);
-        tc::SwapAbParams p = swapab_base(T, n_mtiles * kbp);
+        SwapAbShape sh = swapab_shape(d, T, (int)(width / 64), 1, kbp);
+        tc::SwapAbParams &p = sh.p;
         if ((st = map_2d(&ta, w_gate_up, 2 * I, H, H, 64)) != MSE_OK) return st;
-        if ((st = map_2d(&tb, x, T, H, H, p.bn)) != MSE_OK) return st;
-        p.n_mtiles = n_mtiles;
+        if ((st = map_2d(&tb, x, T, H, H, sh.b_box_rows)) != MSE_OK) return st;
         p.n_groups = 1;
         p.kb_per_tile = kbp;
         p.kb_first = 0;
@@ -316,7 +355,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         p.slots = reinterpret_cast<float *>(ws + L.slots_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_gu_off);
         p.err = d.err;
-        return from_cuda(tc::launch_swapab(tc::EPI_SWIGLU, ta, tb, p, swapab_grid(d, p.total_units), use_pdl(), s));
+        return from_cuda(tc::launch_swapab(tc::EPI_SWIGLU, ta, tb, p, sh.grid, use_pdl(), sh.pair, s));
     }
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
@@ -361,12 +400,11 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
     CUtensorMap ta, tb;
     mse_status st;
     if (T <= kSwapAbMaxT) {
-        const int n_mtiles = (int)((H + 127) / 128);
         const int kbp = (int)(s_width / 64);
-        tc::SwapAbParams p = swapab_base(T, groups * n_mtiles * kbp);
+        SwapAbShape sh = swapab_shape(d, T, (int)((H + 127) / 128), groups, kbp);
+        tc::SwapAbParams &p = sh.p;
         if ((st = map_2d(&ta, w_down, H, I, I, 128)) != MSE_OK) return st;
-        if ((st = map_2d(&tb, h, T, I, I, p.bn)) != MSE_OK) return st;
-        p.n_mtiles = n_mtiles;
+        if ((st = map_2d(&tb, h, T, I, I, sh.b_box_rows)) != MSE_OK) return st;
         p.n_groups = groups;
         p.kb_per_tile = kbp;
         p.kb_first = (int)(kcol0 / 64);
@@ -378,7 +416,7 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
         p.slots = reinterpret_cast<float *>(ws + L.slots_dn_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_dn_off);
         p.err = d.err;
-        return from_cuda(tc::launch_swapab(epi, ta, tb, p, swapab_grid(d, p.total_units), use_pdl(), s));
+        return from_cuda(tc::launch_swapab(epi, ta, tb, p, sh.grid, use_pdl(), sh.pair, s));
     }
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
@@ -690,11 +728,11 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
     CUtensorMap ta, tb;
     char *ws = static_cast<char *>(workspace);
     if (T <= kSwapAbMaxT) {
-        const int n_mtiles = (int)((C + 127) / 128), kbp = (int)(H / 64);
-        tc::SwapAbParams p = swapab_base(T, n_mtiles * kbp);
+        const int kbp = (int)(H / 64);
+        SwapAbShape sh = swapab_shape(*d, T, (int)((C + 127) / 128), 1, kbp);
+        tc::SwapAbParams &p = sh.p;
         if ((st = map_2d(&ta, w, C, H, H, 128)) != MSE_OK) return st;
-        if ((st = map_2d(&tb, x, T, H, H, p.bn)) != MSE_OK) return st;
-        p.n_mtiles = n_mtiles;
+        if ((st = map_2d(&tb, x, T, H, H, sh.b_box_rows)) != MSE_OK) return st;
         p.n_groups = 1;
         p.kb_per_tile = kbp;
         p.m_valid = C;
@@ -705,7 +743,7 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
         p.slots = reinterpret_cast<float *>(ws + L.slots_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_off);
         p.err = d->err;
-        return from_cuda(tc::launch_swapab(tc::EPI_MERGED, ta, tb, p, swapab_grid(*d, p.total_units), use_pdl(), s));
+        return from_cuda(tc::launch_swapab(tc::EPI_MERGED, ta, tb, p, sh.grid, use_pdl(), sh.pair, s));
     }
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
@@ -801,6 +839,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_ONE_LAUNCH: slot = &g_tune_one_launch; ok = value >= 0 && value <= 2; break;
         case MSE_TUNE_PDL: slot = &g_tune_pdl; ok = value == 0 || value == 1; break;
         case MSE_TUNE_COOP_FINISH: slot = &g_tune_coop_finish; ok = value >= 0 && value <= 128; break;
+        case MSE_TUNE_PAIR_MIN_T: slot = &g_tune_pair_min_t; ok = value >= 0 && value <= 100000; break;
         default: return -1;
     }
     if (!ok) return -1;

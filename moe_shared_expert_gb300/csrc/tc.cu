@@ -249,10 +249,11 @@ struct Plan {
     int64_t ub, ue, tile0;
     int kbu, halves, n_mtiles, nseg;
     bool inter;
-    __device__ void init(const SwapAbParams &p) {
-        const StreamK sk{p.total_units, gridDim.x};
-        ub = sk.begin(blockIdx.x);
-        ue = sk.begin(blockIdx.x + 1);
+    // worker w of nw: a CTA, or a CTA pair (both CTAs of a pair share the plan)
+    __device__ void init(const SwapAbParams &p, int64_t w, int64_t nw) {
+        const StreamK sk{p.total_units, nw};
+        ub = sk.begin(w);
+        ue = sk.begin(w + 1);
         kbu = p.kb_per_tile;
         halves = p.halves;
         n_mtiles = p.n_mtiles;
@@ -274,6 +275,15 @@ struct Plan {
         kb1 = (int)(ue < t0 + kbu ? ue - t0 : kbu);
     }
 };
+
+// The stream-K worker of this CTA: the CTA itself, or its pair (clusters of two CTAs,
+// both take the same units, each its own 128-row half of the 256-row weight tile).
+template <bool PAIR>
+__device__ __forceinline__ int64_t worker_index() { return PAIR ? blockIdx.x / 2 : blockIdx.x; }
+template <bool PAIR>
+__device__ __forceinline__ int64_t worker_count() { return PAIR ? gridDim.x / 2 : gridDim.x; }
+template <bool PAIR>
+__device__ __forceinline__ uint32_t pair_rank() { return PAIR ? cluster_ctarank() : 0u; }
 
 // Stages of a Plan in order: runs cut into stages of up to kbs k-blocks.
 struct StageIter {
@@ -324,48 +334,63 @@ struct HFlags {
     int first, n0, n1;
 };
 
-template <int EPI>
+// PAIR: each CTA of the pair loads its own weight rows (m-tile 2 m' + rank of pair tile
+// m') and its half of the token rows; both signal the first CTA's full barriers, which
+// expect the bytes of both.
+template <int EPI, bool PAIR = false>
 __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB, Ctrl *ctl,
                                const SwapAbSmem &sm, RingPos &r, int &issued, bool pdl_prologue, const HFlags *hf,
                                volatile int *abort_flag) {
     const int S = p.stages, KBS = p.kbs;
-    const uint32_t kb_tx = kATileBytes + sm.b_tile_bytes;
+    const uint32_t rank = pair_rank<PAIR>();
+    const bool leader = rank == 0;
+    const uint32_t kb_tx = (PAIR ? 2u : 1u) * (kATileBytes + sm.b_tile_bytes);   // per k-block, both CTAs
+    const int b_row0 = PAIR ? (int)rank * (p.bn / 2) : 0;
+    auto mreal = [&](int m) { return PAIR ? 2 * m + (int)rank : m; };
+    auto fbar = [&](int st) {
+        return PAIR ? map_to_rank(bar_addr(&ctl->full[st]), 0) : bar_addr(&ctl->full[st]);
+    };
+    auto expect = [&](int st, int n) {
+        if (!PAIR || leader) mbar_arrive_expect_tx(bar_addr(&ctl->full[st]), (uint32_t)n * kb_tx);
+    };
+    auto tma2d = [&](uint32_t dst, const CUtensorMap *map, uint32_t fb, int c0, int c1, uint64_t pol, bool hint) {
+        if constexpr (PAIR) {
+            tma_load_2d_pair_hint(dst, map, fb, c0, c1, pol);
+            (void)hint;
+        } else {
+            if (hint) tma_load_2d(dst, map, fb, c0, c1, pol);
+            else tma_load_2d_nohint(dst, map, fb, c0, c1);
+        }
+    };
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_x = l2_policy_evict_last();
     const bool hints = p.cache_hints != 0;
     auto kglob = [&](const StageIter &w, int i) { return p.kb_first + w.group * p.kb_group_stride + w.kblock(i); };
     auto load_a = [&](const StageIter &w, int n, int st) {
-        const uint32_t fb = bar_addr(&ctl->full[st]);
+        const uint32_t fb = fbar(st);
         for (int i = 0; i < n; ++i) {
             const int k = kglob(w, i) * 64;
             const uint32_t dst = sm.a(st) + (uint32_t)i * kATileBytes;
             if constexpr (EPI == EPI_SWIGLU) {
                 // rows 0-63: gate rows j0..j0+63; rows 64-127: the up rows of the same j
-                const int j0 = p.a_row_base + w.m * 64;
-                if (hints) {
-                    tma_load_2d(dst, tmA, fb, k, j0, pol_w);
-                    tma_load_2d(dst + 8192u, tmA, fb, k, p.a_up_offset + j0, pol_w);
-                } else {
-                    tma_load_2d_nohint(dst, tmA, fb, k, j0);
-                    tma_load_2d_nohint(dst + 8192u, tmA, fb, k, p.a_up_offset + j0);
-                }
+                const int j0 = p.a_row_base + mreal(w.m) * 64;
+                tma2d(dst, tmA, fb, k, j0, pol_w, hints);
+                tma2d(dst + 8192u, tmA, fb, k, p.a_up_offset + j0, pol_w, hints);
             } else {
-                if (hints) tma_load_2d(dst, tmA, fb, k, w.m * 128, pol_w);
-                else tma_load_2d_nohint(dst, tmA, fb, k, w.m * 128);
+                tma2d(dst, tmA, fb, k, mreal(w.m) * 128, pol_w, hints);
             }
         }
     };
     auto load_b = [&](const StageIter &w, int n, int st) {
-        const uint32_t fb = bar_addr(&ctl->full[st]);
+        const uint32_t fb = fbar(st);
         for (int i = 0; i < n; ++i) {
             const int k = kglob(w, i) * 64;
             const uint32_t dst = sm.b(st) + (uint32_t)i * sm.b_tile_bytes;
-            if (hints) tma_load_2d(dst, tmB, fb, k, 0, pol_x);
-            else tma_load_2d_nohint(dst, tmB, fb, k, 0);
+            tma2d(dst, tmB, fb, k, b_row0, pol_x, hints);
         }
     };
     Plan pl;
-    pl.init(p);
+    pl.init(p, worker_index<PAIR>(), worker_count<PAIR>());
     StageIter w;
     w.start(pl);
     if (pdl_prologue) {
@@ -374,7 +399,7 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
         int st = 0;
         for (; st < S && !a.done(); ++st) {
             const int n = a.count(KBS);
-            mbar_arrive_expect_tx(bar_addr(&ctl->full[st]), (uint32_t)n * kb_tx);
+            expect(st, n);
             load_a(a, n, st);
             a.advance(n);
         }
@@ -394,7 +419,7 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
                                    p.spin_wait != 0))
                 return false;
             const int n = w.count(KBS);
-            mbar_arrive_expect_tx(bar_addr(&ctl->full[r.stage]), (uint32_t)n * kb_tx);
+            expect(r.stage, n);
             load_a(w, n, r.stage);
             load_b(w, n, r.stage);
             w.advance(n);
@@ -422,7 +447,7 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
         bool progress = false;
         if (!aborted && !w.done() && mbar_test_wait(bar_addr(&ctl->empty[r.stage]), r.phase ^ 1u)) {
             const int n = w.count(KBS);
-            mbar_arrive_expect_tx(bar_addr(&ctl->full[r.stage]), (uint32_t)n * kb_tx);
+            expect(r.stage, n);
             load_a(w, n, r.stage);
             w.advance(n);
             ++issued;
@@ -508,12 +533,15 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
 // Segment s of the pass accumulates in TMEM buffer (gseg + s) & 1, gseg counting the
 // segments of earlier passes; its first run starts the accumulator, its last run
 // hands it to the epilogue.
+// PAIR: run by the first CTA of the pair only; each MMA covers both CTAs' weight rows
+// (M = 256) and both token halves, and the commits reach both CTAs' barriers.
+template <bool PAIR = false>
 __device__ bool swapab_mma(const SwapAbParams &p, Ctrl *ctl, const SwapAbSmem &sm, RingPos &r, int &gseg,
                            uint32_t tmem_base, volatile int *abort_flag) {
     const int S = p.stages, KBS = p.kbs;
-    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)p.bn);
+    const uint32_t idesc = idesc_bf16_f32(PAIR ? 256 : 128, (uint32_t)p.bn);
     Plan pl;
-    pl.init(p);
+    pl.init(p, worker_index<PAIR>(), worker_count<PAIR>());
     const int nr = pl.nruns();
     for (int rr = 0; rr < nr; ++rr) {
         int seg, half;
@@ -542,15 +570,22 @@ __device__ bool swapab_mma(const SwapAbParams &p, Ctrl *ctl, const SwapAbSmem &s
                 const uint64_t bd = smem_desc_sw128(sm.b(r.stage) + (uint32_t)i * sm.b_tile_bytes);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    tc_mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, first ? 0u : 1u);
+                    if constexpr (PAIR)
+                        tc_mma_bf16_pair(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, first ? 0u : 1u);
+                    else
+                        tc_mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, first ? 0u : 1u);
                     first = false;
                 }
             }
-            tc_commit(bar_addr(&ctl->empty[r.stage]));
+            if constexpr (PAIR) tc_commit_pair_multicast(bar_addr(&ctl->empty[r.stage]), (uint16_t)0x3);
+            else tc_commit(bar_addr(&ctl->empty[r.stage]));
             r.next(S);
             kb += n;
         }
-        if (half == pl.halves - 1) tc_commit(bar_addr(&ctl->tfull[buf]));
+        if (half == pl.halves - 1) {
+            if constexpr (PAIR) tc_commit_pair_multicast(bar_addr(&ctl->tfull[buf]), (uint16_t)0x3);
+            else tc_commit(bar_addr(&ctl->tfull[buf]));
+        }
     }
     gseg += pl.nseg;
     return true;
@@ -645,7 +680,9 @@ __device__ __forceinline__ void publish_h_tile(const SwapAbParams &p, int *hflag
 // ring_idle_at_end: after this pass's last MMA the ring is idle, so a split tile
 //   finished in the CTA's last segment may stage the parts in the ring's memory.
 // hflags: publish each completed tile (gate_up passes of the fused layer).
-template <int EPI>
+// PAIR: each CTA finishes its own 128-row half (m-tile 2 m' + rank) of the pair tile;
+// the parts of a split tile are the same halves of the pairs sharing it.
+template <int EPI, bool PAIR = false>
 __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring, uint32_t ring_base,
                                 uint32_t ring_bytes, int &gseg, uint32_t &fix_round, uint32_t tmem_base,
                                 bool ring_idle_at_end, int *hflags, int *hcount, volatile int *abort_flag) {
@@ -656,9 +693,25 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int bn = p.bn, kbp = p.kb_per_tile;
     const int nchunks = bn / 16;
-    const StreamK sk{p.total_units, gridDim.x};
+    const StreamK sk{p.total_units, worker_count<PAIR>()};
+    const uint32_t rank = pair_rank<PAIR>();
+    const int n_real = PAIR ? p.n_mtiles_real : p.n_mtiles;   // m-tiles of 128 rows
     Plan pl;
-    pl.init(p);
+    pl.init(p, worker_index<PAIR>(), worker_count<PAIR>());
+    // slot index of the part of worker cc (a CTA, or this CTA's counterpart in pair cc)
+    auto part_slot = [&](int64_t cc, int64_t tile) -> int {
+        const int64_t cta = PAIR ? cc * 2 + rank : cc;
+        return (int)(cta * 2 + ((sk.begin(cc) >= tile * kbp) ? 0 : 1));
+    };
+    auto release = [&](int buf) {   // hand the accumulator back to the MMA issuer
+        tc_fence_before();
+        if constexpr (PAIR) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(bar_addr(&ctl->tempty[buf]), 0));
+        } else {
+            mbar_arrive(bar_addr(&ctl->tempty[buf]));
+        }
+    };
     const size_t slot_floats = (size_t)128 * bn;
     const int gbase = gseg;
     gseg += pl.nseg;
@@ -670,10 +723,16 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         const int buf = g & 1;
         const uint32_t use = (uint32_t)(g >> 1);
         const int group = (int)(tile / p.n_mtiles);
-        const int m = (int)(tile - (int64_t)group * p.n_mtiles);
+        const int mp = (int)(tile - (int64_t)group * p.n_mtiles);
+        const int m = PAIR ? 2 * mp + (int)rank : mp;         // this CTA's m-tile
+        const int64_t ctile = (int64_t)group * n_real + m;    // its counter
         const bool got = mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
         if (!named_barrier_and(1, 128, got)) return false;   // all epilogue warps take the same branch
         tc_fence_after();
+        if (PAIR && m >= n_real) {   // the second half of a pair tile past the last m-tile
+            release(buf);
+            continue;
+        }
         const uint32_t tacc = tmem_base + (uint32_t)(buf * (p.tmem_cols / 2)) + lane_off;
         if (kb0 == 0 && kb1 == kbp) {
             for (int c = 0; c < nchunks; ++c) {
@@ -681,8 +740,7 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
                 load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
                 swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
             }
-            tc_fence_before();
-            mbar_arrive(bar_addr(&ctl->tempty[buf]));
+            release(buf);
             if (hflags) publish_h_tile(p, hflags, hcount, m);
             continue;
         }
@@ -697,8 +755,7 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
 #pragma unroll
             for (int i = 0; i < 16; ++i) __stcg(slot + (size_t)(c * 16 + i) * 128 + row, v[i]);
         }
-        tc_fence_before();
-        mbar_arrive(bar_addr(&ctl->tempty[buf]));
+        release(buf);
         if (ring_idle_at_end) fence_proxy_async_global();   // a finisher may fetch this slot with a bulk copy
         named_barrier_sync(1, 128);
         const int64_t c_first = sk.owner(tile * kbp), c_last = sk.owner(tile * kbp + kbp - 1);
@@ -720,14 +777,14 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         }
         if (n_fin > 0) {
             if (s != pl.nseg - 1) {
-                if (threadIdx.x == 64) (void)atomic_add_acq_rel_gpu(p.counters + tile, 1);
+                if (threadIdx.x == 64) (void)atomic_add_acq_rel_gpu(p.counters + ctile, 1);
                 continue;
             }
             if (threadIdx.x == 64) {
-                (void)atomic_add_acq_rel_gpu(p.counters + tile, 1);
+                (void)atomic_add_acq_rel_gpu(p.counters + ctile, 1);
                 bool ok = true;
                 const uint64_t t0 = global_timer_ns();
-                while (ld_acquire_gpu(p.counters + tile) < nseg) {
+                while (ld_acquire_gpu(p.counters + ctile) < nseg) {
                     if (*abort_flag) { ok = false; break; }
                     if (global_timer_ns() - t0 > p.wait_limit_ns) {
                         *abort_flag = 1;
@@ -740,19 +797,16 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
             }
             named_barrier_sync(1, 128);
             if (!ctl->fin_flag) return false;
-            for (int k = tid; k < nseg; k += 128) {
-                const int64_t cc = c_first + k;
-                ctl->seg_slot[k] = (int)(cc * 2 + ((sk.begin(cc) >= tile * kbp) ? 0 : 1));
-            }
+            for (int k = tid; k < nseg; k += 128) ctl->seg_slot[k] = part_slot(c_first + k, tile);
             named_barrier_sync(1, 128);
-            const int idx = (int)(blockIdx.x - c_first);
+            const int idx = (int)(worker_index<PAIR>() - c_first);
             const int col0 = idx * bn / n_fin, col1 = (idx + 1) * bn / n_fin;
             if (col1 > col0 && !finish_cols_smem<EPI>(p, ctl, reinterpret_cast<float *>(ring), ring_base, ring_bytes,
                                                        fix_round, nseg, col0, col1, group, m, tid, abort_flag))
                 return false;
             if (threadIdx.x == 64) {
                 // every finisher is past its wait once all have counted themselves here
-                if (atomic_add_acq_rel_gpu(p.counters + tile, 1) == nseg + n_fin - 1) p.counters[tile] = 0;
+                if (atomic_add_acq_rel_gpu(p.counters + ctile, 1) == nseg + n_fin - 1) p.counters[ctile] = 0;
             }
             named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
             continue;
@@ -760,7 +814,7 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         if (threadIdx.x == 64) {
             // release: the barrier above orders every epilogue thread's slot stores
             // before this atomic; acquire: the finisher then sees all other parts
-            const int prev = atomic_add_acq_rel_gpu(p.counters + tile, 1);
+            const int prev = atomic_add_acq_rel_gpu(p.counters + ctile, 1);
             ctl->fin_flag = (prev == nseg - 1) ? 1 : 0;
         }
         named_barrier_sync(1, 128);
@@ -771,15 +825,9 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         // This CTA arrived last: sum the parts in ascending part (CTA) order starting
         // from 0, so the result does not depend on which CTA finishes the tile.
         // Slot of each part: CTA cc's first segment uses slot 2cc, a later one 2cc+1.
-        for (int k = tid; k < nseg && k < 128; k += 128) {
-            const int64_t cc = c_first + k;
-            ctl->seg_slot[k] = (int)(cc * 2 + ((sk.begin(cc) >= tile * kbp) ? 0 : 1));
-        }
+        for (int k = tid; k < nseg && k < 128; k += 128) ctl->seg_slot[k] = part_slot(c_first + k, tile);
         named_barrier_sync(1, 128);
-        auto slot_of = [&](int k) -> int {
-            return k < 128 ? ctl->seg_slot[k]
-                           : (int)((c_first + k) * 2 + ((sk.begin(c_first + k) >= tile * kbp) ? 0 : 1));
-        };
+        auto slot_of = [&](int k) -> int { return k < 128 ? ctl->seg_slot[k] : part_slot(c_first + k, tile); };
         const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
         if (ring_idle_at_end && s == pl.nseg - 1 && ring_bytes / slot_bytes >= 2 && nseg <= 128) {
             // Last segment of the pass with the ring idle: the parts are staged in the
@@ -828,7 +876,7 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
                     if (c0 + b < nchunks) swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c0 + b, acc[b]);
             }
         }
-        if (threadIdx.x == 64) p.counters[tile] = 0;
+        if (threadIdx.x == 64) p.counters[ctile] = 0;
         if (hflags) publish_h_tile(p, hflags, hcount, m);
         named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
     }
@@ -836,6 +884,10 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
 }
 
 // ---- set-up and teardown shared by the swap-AB kernels ----
+// PAIR: the second CTA's full barriers are unused (its copies signal the first CTA's),
+// the first CTA's tempty barriers count one arrival per epilogue warp of both CTAs, and
+// tensor memory is allocated for the pair.
+template <bool PAIR = false>
 __device__ __forceinline__ void swapab_setup(Ctrl *ctl, int S, int tmem_cols, const CUtensorMap *const *maps,
                                              int n_maps) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -846,7 +898,7 @@ __device__ __forceinline__ void swapab_setup(Ctrl *ctl, int S, int tmem_cols, co
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_addr(&ctl->tfull[b]), 1);
-            mbar_init(bar_addr(&ctl->tempty[b]), 128);
+            mbar_init(bar_addr(&ctl->tempty[b]), PAIR ? 8 : 128);
         }
         mbar_init(bar_addr(&ctl->drain), 1);
         mbar_init(bar_addr(&ctl->fixbar), 1);
@@ -856,47 +908,70 @@ __device__ __forceinline__ void swapab_setup(Ctrl *ctl, int S, int tmem_cols, co
     if (warp == 0 && lane == 0)
         for (int i = 0; i < n_maps; ++i) tma_prefetch_desc(maps[i]);
     if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), (uint32_t)tmem_cols);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(&ctl->tmem_base), (uint32_t)tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(&ctl->tmem_base), (uint32_t)tmem_cols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // the peer's barriers are initialised before any remote use
     tc_fence_after();
 }
 
-// Drain in-flight copies and MMAs, then free tensor memory (all threads).
+// Drain in-flight copies and MMAs, then free tensor memory (all threads).  PAIR: each
+// CTA's issued stages are drained through its empty barriers, which the first CTA's
+// MMA commits release once both CTAs' bytes have landed and been consumed.
+template <bool PAIR = false>
 __device__ __forceinline__ void swapab_teardown(Ctrl *ctl, int S, int issued, uint32_t tmem_base, int tmem_cols,
                                                 uint64_t limit_ns) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0 && lane == 0) {
         const int first = issued > S ? issued - S : 0;
-        for (int i = first; i < issued; ++i)
-            (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1), drain_limit_ns(limit_ns));
+        for (int i = first; i < issued; ++i) {
+            if constexpr (PAIR) {
+                const bool done =
+                    mbar_wait_drain(bar_addr(&ctl->empty[i % S]), (uint32_t)((i / S) & 1), drain_limit_ns(limit_ns));
+                if (!done) __nanosleep(200000);   // abort path: let in-flight copies land
+            } else {
+                (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1), drain_limit_ns(limit_ns));
+            }
+        }
     }
-    if (warp == 1 && lane == 0) {
-        tc_commit(bar_addr(&ctl->drain));
+    if (warp == 1 && lane == 0 && (!PAIR || cluster_ctarank() == 0)) {
+        if constexpr (PAIR) tc_commit_pair_multicast(bar_addr(&ctl->drain), (uint16_t)0x1);
+        else tc_commit(bar_addr(&ctl->drain));
         (void)mbar_wait_drain(bar_addr(&ctl->drain), 0, drain_limit_ns(limit_ns));
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, (uint32_t)tmem_cols);
+    if (warp == 1) {
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, (uint32_t)tmem_cols);
+        else tmem_dealloc(tmem_base, (uint32_t)tmem_cols);
+    }
 }
 
 // One stream-K pass: out = epilogue(A . B^T) over p's (group, m-tile, k-block) units.
-template <int EPI>
+// PAIR: clusters of two CTAs take (group, pair of m-tiles, k-block) units; one M = 256
+// MMA per k-block covers both CTAs' weight rows, each CTA holding half of the tokens.
+template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(kSwapAbThreads, 1)
     swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const SwapAbParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const SwapAbSmem sm(base, p.bn, p.kbs);
+    const SwapAbSmem sm(base, PAIR ? p.bn / 2 : p.bn, p.kbs);
     const int S = p.stages;
     uint8_t *ring = smem_raw + (base - raw);
     Ctrl *ctl = reinterpret_cast<Ctrl *>(ring + (uint32_t)S * sm.stage_bytes);
     const CUtensorMap *maps[2] = {&tmA, &tmB};
-    swapab_setup(ctl, S, p.tmem_cols, maps, 2);
+    swapab_setup<PAIR>(ctl, S, p.tmem_cols, maps, 2);
     const uint32_t tmem_base = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort_flag;
     pdl_launch_dependents();
@@ -906,22 +981,22 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             RingPos r;
-            (void)swapab_produce<EPI>(p, &tmA, &tmB, ctl, sm, r, issued, true, nullptr, abort_flag);
+            (void)swapab_produce<EPI, PAIR>(p, &tmA, &tmB, ctl, sm, r, issued, true, nullptr, abort_flag);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && pair_rank<PAIR>() == 0) {
             RingPos r;
             int gseg = 0;
-            (void)swapab_mma(p, ctl, sm, r, gseg, tmem_base, abort_flag);
+            (void)swapab_mma<PAIR>(p, ctl, sm, r, gseg, tmem_base, abort_flag);
         }
     } else {
         pdl_wait();
         int gseg = 0;
         uint32_t fix_round = 0;
-        (void)swapab_epilogue<EPI>(p, ctl, ring, base, (uint32_t)S * sm.stage_bytes, gseg, fix_round, tmem_base,
-                                   true, nullptr, nullptr, abort_flag);
+        (void)swapab_epilogue<EPI, PAIR>(p, ctl, ring, base, (uint32_t)S * sm.stage_bytes, gseg, fix_round,
+                                         tmem_base, true, nullptr, nullptr, abort_flag);
     }
-    swapab_teardown(ctl, S, issued, tmem_base, p.tmem_cols, p.wait_limit_ns);
+    swapab_teardown<PAIR>(ctl, S, issued, tmem_base, p.tmem_cols, p.wait_limit_ns);
 }
 
 // The whole shared-expert layer at decode token counts in one launch:
@@ -1452,9 +1527,12 @@ __global__ void __launch_bounds__(kStdThreads, 1)
 }
 
 // Opt the kernel into the largest dynamic shared memory once per device.
+constexpr int kSmemAttrSlots = 32;   // one per kernel instantiation (slots 0..17 in use)
+
 template <typename Kern>
 cudaError_t ensure_smem_attr(Kern kern, int slot) {
-    static std::atomic<uint64_t> done[16];   // bit per device, per kernel slot
+    static std::atomic<uint64_t> done[kSmemAttrSlots];   // bit per device, per kernel slot
+    if (slot < 0 || slot >= kSmemAttrSlots) return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1480,37 +1558,81 @@ int swapab_stages_for(int bn, int kbs) {
 int std_stages() { return 4; }
 
 cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
-                          bool pdl, cudaStream_t s) {
-    const size_t smem = swapab_smem_bytes(p.bn, p.stages, p.kbs);
+                          bool pdl, bool pair, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)kSwapAbThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = swapab_smem_bytes(pair ? p.bn / 2 : p.bn, p.stages, p.kbs);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    cudaError_t e;
-    switch (epi) {
-        case EPI_SWIGLU:
-            e = ensure_smem_attr(swapab_kernel<EPI_SWIGLU>, 0);
-            if (e != cudaSuccess) return e;
-            return cudaLaunchKernelEx(&cfg, swapab_kernel<EPI_SWIGLU>, ta, tb, p);
-        case EPI_BF16:
-            e = ensure_smem_attr(swapab_kernel<EPI_BF16>, 1);
-            if (e != cudaSuccess) return e;
-            return cudaLaunchKernelEx(&cfg, swapab_kernel<EPI_BF16>, ta, tb, p);
-        case EPI_F32:
-            e = ensure_smem_attr(swapab_kernel<EPI_F32>, 2);
-            if (e != cudaSuccess) return e;
-            return cudaLaunchKernelEx(&cfg, swapab_kernel<EPI_F32>, ta, tb, p);
-        default:
-            e = ensure_smem_attr(swapab_kernel<EPI_MERGED>, 3);
-            if (e != cudaSuccess) return e;
-            return cudaLaunchKernelEx(&cfg, swapab_kernel<EPI_MERGED>, ta, tb, p);
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pair) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    cfg.gridDim = dim3((unsigned)(pair ? 2 * grid : grid));   // grid: workers (CTAs or pairs)
+    cudaError_t e;
+#define MSE_LAUNCH_SWAPAB(E, PR, SLOT)                                  \
+    e = ensure_smem_attr(swapab_kernel<E, PR>, SLOT);                   \
+    if (e != cudaSuccess) return e;                                     \
+    return cudaLaunchKernelEx(&cfg, swapab_kernel<E, PR>, ta, tb, p);
+    if (!pair) {
+        switch (epi) {
+            case EPI_SWIGLU: MSE_LAUNCH_SWAPAB(EPI_SWIGLU, false, 0)
+            case EPI_BF16: MSE_LAUNCH_SWAPAB(EPI_BF16, false, 1)
+            case EPI_F32: MSE_LAUNCH_SWAPAB(EPI_F32, false, 2)
+            default: MSE_LAUNCH_SWAPAB(EPI_MERGED, false, 3)
+        }
+    }
+    switch (epi) {
+        case EPI_SWIGLU: MSE_LAUNCH_SWAPAB(EPI_SWIGLU, true, 14)
+        case EPI_BF16: MSE_LAUNCH_SWAPAB(EPI_BF16, true, 15)
+        case EPI_F32: MSE_LAUNCH_SWAPAB(EPI_F32, true, 16)
+        default: MSE_LAUNCH_SWAPAB(EPI_MERGED, true, 17)
+    }
+#undef MSE_LAUNCH_SWAPAB
+}
+
+// Pairs of the swap-AB kernel that can be resident at once (one wave).
+int swapab_pair_max_clusters(int bn, int stages, int kbs) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    int mc = cache[dev & 63].load();
+    if (mc > 0) return mc;
+    if (ensure_smem_attr(swapab_kernel<EPI_BF16, true>, 15) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(2);
+    q.blockDim = dim3((unsigned)kSwapAbThreads);
+    q.dynamicSmemBytes = swapab_smem_bytes(bn / 2, stages, kbs);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    q.attrs = attr;
+    q.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&mc, swapab_kernel<EPI_BF16, true>, &q) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[dev & 63].store(mc);
+    return mc;
 }
 
 // One CTA per SM (the ring takes most of the shared memory) and grid <= SMs, so every

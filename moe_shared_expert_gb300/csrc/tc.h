@@ -17,7 +17,8 @@ enum Epi : int {
 // Work of one launch of the swap-AB kernel (weights on the 128-row MMA side,
 // tokens on the N side), decomposed stream-K over (group, m-tile, k-block).
 struct SwapAbParams {
-    int n_mtiles;          // 128-row A tiles per group
+    int n_mtiles;          // 128-row A tiles per group (pair kernel: pairs of them, 256 rows)
+    int n_mtiles_real;     // pair kernel: 128-row A tiles per group
     int n_groups;          // independent outputs (shards); 1 when replicated
     int kb_per_tile;       // units per tile: 64-wide k-blocks (halves = 1) or pairs of them (halves = 2)
     int halves;            // 2: unit u of a tile stands for k-blocks u and kb_per_tile + u
@@ -95,8 +96,10 @@ int pair_stages();
 int swapab_stages_for(int bn, int kbs);
 int std_stages();
 
+// grid = workers: CTAs, or CTA pairs (clusters of two) when `pair`.
 cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
-                          bool pdl, cudaStream_t s);
+                          bool pdl, bool pair, cudaStream_t s);
+int swapab_pair_max_clusters(int bn, int stages, int kbs);
 // The one-launch decode layer (grid <= SMs, one CTA per SM).
 cudaError_t launch_swapab_mlp(int epi1, const CUtensorMap &ta0, const CUtensorMap &tb0, const CUtensorMap &ta1,
                               const CUtensorMap &tb1, const SwapAbMlpParams &fp, int grid, bool pdl, cudaStream_t s);
