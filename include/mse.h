@@ -276,6 +276,7 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         CTA holding half of the token rows, so that more weight bytes are in
  *                         flight per SM (0 = never, the default: at 64 and 128 tokens it
  *                         measured no faster than single CTAs)
+ *   MSE_TUNE_GRID_DOWN    CTAs of the down-projection swap-AB kernel (0 = as MSE_TUNE_GRID)
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -287,7 +288,8 @@ typedef enum {
     MSE_TUNE_ONE_LAUNCH = 7,
     MSE_TUNE_PDL = 8,
     MSE_TUNE_COOP_FINISH = 9,
-    MSE_TUNE_PAIR_MIN_T = 10
+    MSE_TUNE_PAIR_MIN_T = 10,
+    MSE_TUNE_GRID_DOWN = 11
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

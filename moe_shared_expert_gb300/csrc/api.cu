@@ -20,7 +20,7 @@ std::atomic<int> g_path{MSE_PATH_AUTO};
 std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
     g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
-    g_tune_coop_finish{6}, g_tune_pair_min_t{0};
+    g_tune_coop_finish{6}, g_tune_pair_min_t{0}, g_tune_grid_down{0};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -260,10 +260,55 @@ tc::SwapAbParams swapab_base(int64_t T, int total_units, bool pair = false) {
 
 bool use_pdl() { return g_tune_pdl.load() != 0; }
 
-int swapab_grid(const DeviceInfo &d, int total_units) {
+// Stream-K grid for `units` units of `kbp` per tile.  Among CTA counts from 90% of the
+// SMs up to all of them, the largest one that minimises the largest number of CTAs any
+// tile is split between, if that is at most three: each extra part lengthens the tile's
+// split-K tail, which the whole launch waits for (gate_up at T = 64: 144 CTAs split every
+// tile in two, 152 split some in three; measured 54.9 against 56.2 us per layer, and the
+// T = 128 sharded layer 67.6 against 71.7 us).  Cached per shape.
+int stream_k_grid(int units, int kbp, int g_max) {
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> cache;
+    const uint64_t key = ((uint64_t)(uint32_t)units << 32) ^ ((uint64_t)(uint32_t)kbp << 12) ^ (uint64_t)g_max;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const int64_t U = units;
+    const int64_t n_tiles = U / kbp;
+    int best = g_max, best_parts = INT32_MAX;
+    const int g_min = std::max(1, (g_max * 9 + 9) / 10);
+    for (int G = g_max; G >= g_min; --G) {
+        if (n_tiles > 65536) break;   // very large shapes: keep g_max
+        auto owner = [&](int64_t u) { return ((u + 1) * G - 1) / U; };
+        int worst = 1;
+        for (int64_t t = 0; t < n_tiles && worst < best_parts; ++t)
+            worst = std::max(worst, (int)(owner(t * kbp + kbp - 1) - owner(t * kbp) + 1));
+        if (worst < best_parts) {
+            best_parts = worst;
+            best = G;
+        }
+    }
+    // fewer CTAs pay only where tiles end up split in at most three parts (the merged
+    // projection's tiles are split about nine ways: 138 CTAs measured slower than 152)
+    if (best_parts > 3) best = g_max;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache.size() > 4096) cache.clear();
+    cache.emplace(key, best);
+    return best;
+}
+
+// kbp = 0: no tile-aware choice (all SMs).  override: a CTA count for this kernel that
+// takes precedence over MSE_TUNE_GRID (0 = none).
+int swapab_grid(const DeviceInfo &d, int total_units, int kbp, int override = 0) {
     int g = d.sm_count < tc::kMaxGrid ? d.sm_count : tc::kMaxGrid;
-    const int want = g_tune_grid.load();
-    if (want > 0 && want < g) g = want;
+    const int want = override > 0 ? override : g_tune_grid.load();
+    if (want > 0) {
+        if (want < g) g = want;
+    } else if (kbp > 0 && total_units > g) {
+        g = stream_k_grid(total_units, kbp, g);
+    }
     return g < total_units ? g : total_units;
 }
 
@@ -276,7 +321,7 @@ struct SwapAbShape {
     int grid;
     int b_box_rows;   // token rows of one B copy (each CTA's half for pairs)
 };
-SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups, int kbp) {
+SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups, int kbp, bool down = false) {
     SwapAbShape r;
     const int pmin = g_tune_pair_min_t.load();
     if (pmin > 0 && T >= pmin) {
@@ -300,7 +345,7 @@ SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups,
     r.p = swapab_base(T, groups * n_real * kbp, false);
     r.p.n_mtiles = n_real;
     r.p.n_mtiles_real = n_real;
-    r.grid = swapab_grid(d, r.p.total_units);
+    r.grid = swapab_grid(d, r.p.total_units, kbp, down ? g_tune_grid_down.load() : 0);
     r.b_box_rows = r.p.bn;
     return r;
 }
@@ -401,7 +446,7 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
     mse_status st;
     if (T <= kSwapAbMaxT) {
         const int kbp = (int)(s_width / 64);
-        SwapAbShape sh = swapab_shape(d, T, (int)((H + 127) / 128), groups, kbp);
+        SwapAbShape sh = swapab_shape(d, T, (int)((H + 127) / 128), groups, kbp, true);
         tc::SwapAbParams &p = sh.p;
         if ((st = map_2d(&ta, w_down, H, I, I, 128)) != MSE_OK) return st;
         if ((st = map_2d(&tb, h, T, I, I, sh.b_box_rows)) != MSE_OK) return st;
@@ -527,7 +572,7 @@ mse_status tc_mlp_one_launch(const DeviceInfo &d, const uint16_t *x, int64_t T, 
     // range of its owners
     int units = p0.total_units < p1.total_units ? p0.total_units : p1.total_units;
     if (two && fp.ph[1].total_units < units) units = fp.ph[1].total_units;
-    const int grid = swapab_grid(d, units);
+    const int grid = swapab_grid(d, units, 0);   // one launch: every pass needs units on every CTA
     return from_cuda(tc::launch_swapab_mlp(epi1, ta0, tb0, ta1, tb1, fp, grid, use_pdl(), s));
 }
 
@@ -840,6 +885,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_PDL: slot = &g_tune_pdl; ok = value == 0 || value == 1; break;
         case MSE_TUNE_COOP_FINISH: slot = &g_tune_coop_finish; ok = value >= 0 && value <= 128; break;
         case MSE_TUNE_PAIR_MIN_T: slot = &g_tune_pair_min_t; ok = value >= 0 && value <= 100000; break;
+        case MSE_TUNE_GRID_DOWN: slot = &g_tune_grid_down; ok = value >= 0 && value <= tc::kMaxGrid; break;
         default: return -1;
     }
     if (!ok) return -1;
