@@ -148,3 +148,33 @@ def test_product_path_does_not_import_oracle():
         assert "oracle" not in src.replace("# oracle", "")
     for f in os.listdir(os.path.join(ROOT, "moe_shared_expert_gb300", "csrc")):
         assert "oracle" not in open(os.path.join(ROOT, "moe_shared_expert_gb300", "csrc", f)).read().lower()
+
+
+# key: (default, accepted values, rejected values)
+TUNING = {
+    mse.TUNE_ISSUE_GROUP: (2, [1, 4], [0, 5]),
+    mse.TUNE_STAGES: (0, [2, 12], [1, 13]),
+    mse.TUNE_CACHE_HINTS: (1, [0, 1], [2, -1]),
+    mse.TUNE_GRID: (0, [1, 160], [161, -1]),
+    mse.TUNE_SPIN_WAIT: (0, [0, 1], [2]),
+    mse.TUNE_ONE_LAUNCH: (0, [1, 2], [3]),
+    mse.TUNE_PDL: (1, [0, 1], [2]),
+    mse.TUNE_COOP_FINISH: (6, [0, 128], [129, -1]),
+    mse.TUNE_PAIR_MIN_T: (0, [1, 256], [-1]),
+    mse.TUNE_GRID_DOWN: (0, [1, 160], [161]),
+}
+
+
+def test_tuning_keys_defaults_ranges_and_restore(L):
+    for key, (default, good, bad) in TUNING.items():
+        cur = L.mse_set_tuning(key, default)   # read the current value (and set the default)
+        assert L.mse_set_tuning(key, cur) == default, f"key {key}: default"
+        for v in good:
+            prev = L.mse_set_tuning(key, v)
+            assert prev >= 0
+            assert L.mse_set_tuning(key, prev) == v, f"key {key} value {v}"
+        for v in bad:
+            assert L.mse_set_tuning(key, v) == -1, f"key {key} accepted {v}"
+        assert L.mse_set_tuning(key, cur) == cur   # unchanged by the rejected values
+    assert L.mse_set_tuning(5, 1) == -1         # unused key
+    assert L.mse_set_tuning(99, 1) == -1
