@@ -277,6 +277,10 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         flight per SM (0 = never, the default: at 64 and 128 tokens it
  *                         measured no faster than single CTAs)
  *   MSE_TUNE_GRID_DOWN    CTAs of the down-projection swap-AB kernel (0 = as MSE_TUNE_GRID)
+ *   MSE_TUNE_CLUSTER_FINISH  1 = when three CTAs of a decode-size kernel cover two tiles exactly
+ *                         (gate_up at 64 tokens on 144 CTAs), launch clusters of three and finish
+ *                         each two-part tile inside its cluster (same results bit for bit;
+ *                         measured within 0.1 us); 0 = through L2 only (default)
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -289,7 +293,8 @@ typedef enum {
     MSE_TUNE_PDL = 8,
     MSE_TUNE_COOP_FINISH = 9,
     MSE_TUNE_PAIR_MIN_T = 10,
-    MSE_TUNE_GRID_DOWN = 11
+    MSE_TUNE_GRID_DOWN = 11,
+    MSE_TUNE_CLUSTER_FINISH = 12
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

@@ -20,7 +20,7 @@ std::atomic<int> g_path{MSE_PATH_AUTO};
 std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
     g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
-    g_tune_coop_finish{6}, g_tune_pair_min_t{0}, g_tune_grid_down{0};
+    g_tune_coop_finish{6}, g_tune_pair_min_t{0}, g_tune_grid_down{0}, g_tune_cluster_finish{0};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -347,6 +347,11 @@ SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups,
     r.p.n_mtiles_real = n_real;
     r.grid = swapab_grid(d, r.p.total_units, kbp, down ? g_tune_grid_down.load() : 0);
     r.b_box_rows = r.p.bn;
+    // clusters of three when three CTAs cover two tiles exactly (every tile in two parts)
+    if (g_tune_cluster_finish.load() != 0 && r.grid % 3 == 0 &&
+        3LL * r.p.total_units == 2LL * kbp * r.grid &&
+        tc::swapab_trio_max_clusters(r.p.bn, r.p.stages, r.p.kbs) >= r.grid / 3)
+        r.p.cluster_finish = 1;
     return r;
 }
 
@@ -886,6 +891,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_COOP_FINISH: slot = &g_tune_coop_finish; ok = value >= 0 && value <= 128; break;
         case MSE_TUNE_PAIR_MIN_T: slot = &g_tune_pair_min_t; ok = value >= 0 && value <= 100000; break;
         case MSE_TUNE_GRID_DOWN: slot = &g_tune_grid_down; ok = value >= 0 && value <= tc::kMaxGrid; break;
+        case MSE_TUNE_CLUSTER_FINISH: slot = &g_tune_cluster_finish; ok = value == 0 || value == 1; break;
         default: return -1;
     }
     if (!ok) return -1;

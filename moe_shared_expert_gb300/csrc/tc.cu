@@ -36,6 +36,8 @@ struct Ctrl {
     uint64_t tempty[2];
     uint64_t drain;
     uint64_t fixbar;         // swap-AB finisher: bulk copies of partial tiles into shared memory
+    uint64_t go_bar;         // swap-AB cluster finish: the receiving CTA's ring is free
+    uint64_t recv_bar;       // swap-AB cluster finish: the sending CTA's part has landed
     uint32_t tmem_base;
     int abort_flag;
     int fin_flag;
@@ -744,6 +746,113 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
             if (hflags) publish_h_tile(p, hflags, hcount, m);
             continue;
         }
+        // Clustered finish of two-part tiles (clusters of three CTAs covering two tiles
+        // exactly; the pass's final segments; the ring idle).  Parts are summed in CTA
+        // order from 0 like every other path, so results are identical.
+        //  - the other part is the next CTA's first segment (finished long before): this
+        //    CTA finishes the tile without publishing its own part: it waits for the
+        //    other part's count, fetches that part and adds its own from tensor memory;
+        //  - both parts are final segments: the first CTA writes its part straight into
+        //    the second one's idle ring (distributed shared memory) once that ring is
+        //    free, and the second CTA finishes the tile.
+        if (!PAIR && p.cluster_finish && ring_idle_at_end && s == pl.nseg - 1) {
+            const int64_t cf = sk.owner(tile * kbp), cl = sk.owner(tile * kbp + kbp - 1);
+            const int64_t me = blockIdx.x;
+            const bool cl_early = cl == cf + 1 && sk.begin(cl + 1) > (tile + 1) * kbp;
+            const bool both_final = cl == cf + 1 && !cl_early && cf / 3 == cl / 3;
+            const uint32_t slot_bytes1 = (uint32_t)(slot_floats * 4);
+            const float *other = reinterpret_cast<const float *>(ring);
+            if (cl_early && me == cf) {
+                if (threadIdx.x == 64) {
+                    bool ok = true;
+                    const uint64_t t0 = global_timer_ns();
+                    while (ld_acquire_gpu(p.counters + ctile) < 1) {
+                        if (*abort_flag) { ok = false; break; }
+                        if (global_timer_ns() - t0 > p.wait_limit_ns) {
+                            *abort_flag = 1;
+                            raise_device_error(p.err, DEV_ERR_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (ok) {
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(bar_addr(&ctl->fixbar), slot_bytes1);
+                        bulk_load(ring_base, p.slots + (size_t)part_slot(cl, tile) * slot_floats, slot_bytes1,
+                                  bar_addr(&ctl->fixbar));
+                    }
+                    ctl->fin_flag = ok ? 1 : 0;
+                }
+                named_barrier_sync(1, 128);
+                if (!ctl->fin_flag) return false;
+                const bool got_fix =
+                    mbar_wait_bounded(bar_addr(&ctl->fixbar), fix_round & 1u, abort_flag, p.wait_limit_ns, p.err);
+                ++fix_round;
+                if (!named_barrier_and(1, 128, got_fix)) {
+                    if (threadIdx.x == 64)
+                        (void)mbar_wait_drain(bar_addr(&ctl->fixbar), (fix_round - 1) & 1u,
+                                              drain_limit_ns(p.wait_limit_ns));
+                    return false;
+                }
+                for (int c = 0; c < nchunks; ++c) {
+                    float own[16], v[16];
+                    load_tmem_chunk(tacc + (uint32_t)(c * 16), own);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = (0.f + own[i]) + other[(c * 16 + i) * 128 + row];
+                    swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
+                }
+                release(buf);
+                if (threadIdx.x == 64) p.counters[ctile] = 0;
+                named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
+                continue;
+            }
+            if (both_final && me == cf) {
+                const uint32_t peer = (uint32_t)(cl % 3);
+                bool ok = true;
+                if (threadIdx.x == 64)
+                    ok = mbar_wait_bounded(bar_addr(&ctl->go_bar), 0u, abort_flag, p.wait_limit_ns, p.err);
+                if (!named_barrier_and(1, 128, ok)) return false;
+                const uint32_t remote = map_to_rank(ring_base, peer);
+                for (int c = 0; c < nchunks; ++c) {
+                    float v[16];
+                    load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        st_cluster_f32(remote + (uint32_t)(((c * 16 + i) * 128 + row) * 4), v[i]);
+                }
+                release(buf);
+                named_barrier_sync(1, 128);   // every thread's stores precede the arrive
+                if (threadIdx.x == 64) mbar_arrive_cluster(map_to_rank(bar_addr(&ctl->recv_bar), peer));
+                continue;
+            }
+            if (both_final && me == cl) {
+                const uint32_t peer = (uint32_t)(cf % 3);
+                bool ok = true;
+                if (threadIdx.x == 64) {
+                    mbar_arrive_cluster(map_to_rank(bar_addr(&ctl->go_bar), peer));   // this ring is free
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait_acq_cluster(bar_addr(&ctl->recv_bar), 0u)) {
+                        if (*abort_flag) { ok = false; break; }
+                        if (global_timer_ns() - t0 > p.wait_limit_ns) {
+                            *abort_flag = 1;
+                            raise_device_error(p.err, DEV_ERR_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (!named_barrier_and(1, 128, ok)) return false;
+                for (int c = 0; c < nchunks; ++c) {
+                    float own[16], v[16];
+                    load_tmem_chunk(tacc + (uint32_t)(c * 16), own);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = (0.f + other[(c * 16 + i) * 128 + row]) + own[i];
+                    swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
+                }
+                release(buf);
+                continue;
+            }
+        }
         // Tile shared with other CTAs: park the fp32 partial in this CTA's slot, laid
         // out [token column][accumulator row] (each warp store is a 128-byte run).
         // A CTA's first segment uses its slot 0, a later one its slot 1.
@@ -889,7 +998,7 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
 // tensor memory is allocated for the pair.
 template <bool PAIR = false>
 __device__ __forceinline__ void swapab_setup(Ctrl *ctl, int S, int tmem_cols, const CUtensorMap *const *maps,
-                                             int n_maps) {
+                                             int n_maps, bool clustered = false) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -902,6 +1011,8 @@ __device__ __forceinline__ void swapab_setup(Ctrl *ctl, int S, int tmem_cols, co
         }
         mbar_init(bar_addr(&ctl->drain), 1);
         mbar_init(bar_addr(&ctl->fixbar), 1);
+        mbar_init(bar_addr(&ctl->go_bar), 1);
+        mbar_init(bar_addr(&ctl->recv_bar), 1);
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
@@ -918,7 +1029,7 @@ __device__ __forceinline__ void swapab_setup(Ctrl *ctl, int S, int tmem_cols, co
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR) cluster_sync();   // the peer's barriers are initialised before any remote use
+    if (PAIR || clustered) cluster_sync();   // the peers' barriers are initialised before any remote use
     tc_fence_after();
 }
 
@@ -927,7 +1038,7 @@ __device__ __forceinline__ void swapab_setup(Ctrl *ctl, int S, int tmem_cols, co
 // MMA commits release once both CTAs' bytes have landed and been consumed.
 template <bool PAIR = false>
 __device__ __forceinline__ void swapab_teardown(Ctrl *ctl, int S, int issued, uint32_t tmem_base, int tmem_cols,
-                                                uint64_t limit_ns) {
+                                                uint64_t limit_ns, bool clustered = false) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0 && lane == 0) {
         const int first = issued > S ? issued - S : 0;
@@ -948,7 +1059,7 @@ __device__ __forceinline__ void swapab_teardown(Ctrl *ctl, int S, int issued, ui
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR) cluster_sync();
+    if (PAIR || clustered) cluster_sync();   // no CTA leaves while a peer may still use its memory
     tc_fence_after();
     if (warp == 1) {
         if constexpr (PAIR) tmem_dealloc_pair(tmem_base, (uint32_t)tmem_cols);
@@ -971,7 +1082,8 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
     uint8_t *ring = smem_raw + (base - raw);
     Ctrl *ctl = reinterpret_cast<Ctrl *>(ring + (uint32_t)S * sm.stage_bytes);
     const CUtensorMap *maps[2] = {&tmA, &tmB};
-    swapab_setup<PAIR>(ctl, S, p.tmem_cols, maps, 2);
+    const bool clustered = !PAIR && p.cluster_finish != 0;
+    swapab_setup<PAIR>(ctl, S, p.tmem_cols, maps, 2, clustered);
     const uint32_t tmem_base = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort_flag;
     pdl_launch_dependents();
@@ -996,7 +1108,7 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
         (void)swapab_epilogue<EPI, PAIR>(p, ctl, ring, base, (uint32_t)S * sm.stage_bytes, gseg, fix_round,
                                          tmem_base, true, nullptr, nullptr, abort_flag);
     }
-    swapab_teardown<PAIR>(ctl, S, issued, tmem_base, p.tmem_cols, p.wait_limit_ns);
+    swapab_teardown<PAIR>(ctl, S, issued, tmem_base, p.tmem_cols, p.wait_limit_ns, clustered);
 }
 
 // The whole shared-expert layer at decode token counts in one launch:
@@ -1565,9 +1677,9 @@ cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb,
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (pair) {
+    if (pair || p.cluster_finish) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.x = pair ? 2 : 3;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -1600,6 +1712,39 @@ cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb,
         default: MSE_LAUNCH_SWAPAB(EPI_MERGED, true, 17)
     }
 #undef MSE_LAUNCH_SWAPAB
+}
+
+// Clusters of three single CTAs of the swap-AB kernel that can be resident at once.
+int swapab_trio_max_clusters(int bn, int stages, int kbs) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    int mc = cache[dev & 63].load();
+    if (mc > 0) return mc;
+    if (ensure_smem_attr(swapab_kernel<EPI_SWIGLU, false>, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(3);
+    q.blockDim = dim3((unsigned)kSwapAbThreads);
+    q.dynamicSmemBytes = swapab_smem_bytes(bn, stages, kbs);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 3;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    q.attrs = attr;
+    q.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&mc, swapab_kernel<EPI_SWIGLU, false>, &q) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[dev & 63].store(mc);
+    return mc;
 }
 
 // Pairs of the swap-AB kernel that can be resident at once (one wave).

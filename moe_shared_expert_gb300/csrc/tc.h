@@ -34,6 +34,8 @@ struct SwapAbParams {
                            // kbs x 128 contiguous bytes at a time; DRAM row-buffer locality)
     int cache_hints;       // 1: weights evict_first, tokens evict_last in L2; 0: no hints
     int spin_wait;         // 1: pipeline waits poll without suspending the thread
+    int cluster_finish;    // 1: launched in clusters of three CTAs that cover two tiles exactly; the
+                           // two-part tiles of the final segments are finished inside the cluster
     int coop_finish;       // > 0: a tile split into at least this many parts, in the CTAs' final
                            // segments, is finished jointly (each part's CTA sums one slice of
                            // token columns) when the ring is idle; 0: never
@@ -100,6 +102,8 @@ int std_stages();
 cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
                           bool pdl, bool pair, cudaStream_t s);
 int swapab_pair_max_clusters(int bn, int stages, int kbs);
+// clusters of three single CTAs of the swap-AB kernel resident at once (0 on failure)
+int swapab_trio_max_clusters(int bn, int stages, int kbs);
 // The one-launch decode layer (grid <= SMs, one CTA per SM).
 cudaError_t launch_swapab_mlp(int epi1, const CUtensorMap &ta0, const CUtensorMap &tb0, const CUtensorMap &ta1,
                               const CUtensorMap &tb1, const SwapAbMlpParams &fp, int grid, bool pdl, cudaStream_t s);

@@ -162,6 +162,7 @@ TUNING = {
     mse.TUNE_COOP_FINISH: (6, [0, 128], [129, -1]),
     mse.TUNE_PAIR_MIN_T: (0, [1, 256], [-1]),
     mse.TUNE_GRID_DOWN: (0, [1, 160], [161]),
+    mse.TUNE_CLUSTER_FINISH: (0, [0, 1], [2]),
 }
 
 
