@@ -1,8 +1,9 @@
 """Two-part split-K tiles finished inside clusters of three CTAs (the option
 MSE_TUNE_CLUSTER_FINISH, launched when three CTAs cover two tiles exactly): one
 tile's finishing CTA fetches the other part without publishing its own, the other
-tile's first part is written straight into the second CTA's shared memory.  Checked against the fp64 oracle and bit for bit against the same
-launch shape finishing every tile through L2 (the parts are summed in the same order).
+tile's first part is written straight into the second CTA's shared memory.
+Checked against the fp64 oracle and bit for bit against the same launch shape
+finishing every tile through L2 (the parts are summed in the same order).
 
 The grid is forced to the size that gives the three-CTAs-per-two-tiles pattern on each
 shape: gate_up tiles of 64 intermediate columns, H / 64 k-blocks per tile.
