@@ -828,7 +828,8 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
     p.out_rm = out_rank_major;
     p.q_dim = q_dim; p.kv_dim = kv_dim; p.tp = tp;
     p.err = d->err;
-    return from_cuda(tc::launch_std(tc::EPI_MERGED, ta, tb, p, std_grid(*d, (int64_t)p.n_mtiles * p.n_ntiles), use_pdl(), s));
+    return from_cuda(
+        tc::launch_std(tc::EPI_MERGED, ta, tb, p, std_grid(*d, (int64_t)p.n_mtiles * p.n_ntiles), use_pdl(), s));
 }
 
 mse_status merged_proj_reorder(const mse_bf16 *rank_major, mse_bf16 *logical, int64_t T, int64_t q_dim,

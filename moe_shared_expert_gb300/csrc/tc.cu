@@ -482,15 +482,9 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
                         if (need0 && c0 >= hf->n0) done0 = true;
                         if (need1 && c1 >= hf->n1) done1 = true;
                         bool all = true;
-                        bool polled = false;
 #pragma unroll
-                        for (int i = 0; i < kMaxKbs; ++i) {
-                            if (i < n && !(in1[i] ? done1 : done0)) {
-                                polled = true;
-                                all = all && ld_relaxed_gpu(hf->flags + fi[i]) != 0;
-                            }
-                        }
-                        (void)polled;
+                        for (int i = 0; i < kMaxKbs; ++i)
+                            if (i < n && !(in1[i] ? done1 : done0)) all = all && ld_relaxed_gpu(hf->flags + fi[i]) != 0;
                         if (all) {
                             fence_acq_rel_gpu();   // acquire the publishers' h stores
                             ready = true;
@@ -871,9 +865,10 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         const int nseg = (int)(c_last - c_first + 1);
         // Cooperative finish (the ring is idle after the pass, the tile has at least
         // coop_finish parts): every part for which the tile is its CTA's final segment
-        // waits for all parts, then sums and finishes its own slice of token columns.  Only the last CTA's part can be a non-final segment
-        // (the tile is that CTA's first); it hands its part over and goes on.  All parts
-        // of the tile take the same decision.
+        // waits for all parts, then sums and finishes its own slice of token columns.
+        // Only the last CTA's part can be a non-final segment (the tile is that CTA's
+        // first); it hands its part over and goes on.  All parts of the tile take the
+        // same decision.
         // (compiled into the merged-projection kernel only: its tiles are split about nine
         // ways; the MLP kernels' tiles are split two to four ways, where the CTA arriving
         // last finishing alone measured faster)
@@ -1328,7 +1323,8 @@ __global__ void __launch_bounds__(kStdThreads, 1)
             const StdTile t = std_tile(p, id);
             const int buf = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
-            const bool got = mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
+            const bool got =
+                mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
             if (!named_barrier_and(1, 128, got)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + (uint32_t)(buf * 256) + lane_off;
@@ -1365,12 +1361,14 @@ __global__ void __launch_bounds__(kStdThreads, 1)
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
                                                                  t.group * p.o_group_stride + tok * p.ldo + n);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     } else if constexpr (EPI == EPI_BF16) {
                         uint32_t w[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            w[i] = (uint32_t)f32_to_bf16_bits(v[2 * i]) | ((uint32_t)f32_to_bf16_bits(v[2 * i + 1]) << 16);
+                            w[i] = (uint32_t)f32_to_bf16_bits(v[2 * i]) |
+                                   ((uint32_t)f32_to_bf16_bits(v[2 * i + 1]) << 16);
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
                                                                t.group * p.o_group_stride + tok * p.ldo + n);
                         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -1396,7 +1394,8 @@ __global__ void __launch_bounds__(kStdThreads, 1)
     if (warp == 0 && lane == 0) {
         const int64_t first = issued > S ? issued - S : 0;
         for (int64_t i = first; i < issued; ++i)
-            (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1), drain_limit_ns(p.wait_limit_ns));
+            (void)mbar_wait_drain(bar_addr(&ctl->full[i % S]), (uint32_t)((i / S) & 1),
+                                  drain_limit_ns(p.wait_limit_ns));
     }
     if (warp == 1 && lane == 0) {
         tc_commit(bar_addr(&ctl->drain));
@@ -1497,7 +1496,8 @@ __global__ void __launch_bounds__(kStdThreads, 1)
                         break;
                     }
                     const uint32_t fb = map_to_rank(bar_addr(&ctl->full[stage]), 0);
-                    if (leader) mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), 2u * (kATileBytes + kPairBTileBytes));
+                    if (leader)
+                        mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), 2u * (kATileBytes + kPairBTileBytes));
                     const int k = (p.kb_first + t.group * p.kb_group_stride + kb) * 64;
                     tma_load_2d_pair(sA + stage * kATileBytes, &tmA, fb, k, t.m * 256 + (int)rank * 128);
                     tma_load_2d_pair(sB + stage * kPairBTileBytes, &tmB, fb, k,
@@ -1551,7 +1551,8 @@ __global__ void __launch_bounds__(kStdThreads, 1)
             const StdTile t = tile_of(id);
             const int buf = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
-            const bool got = mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
+            const bool got =
+                mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
             if (!named_barrier_and(1, 128, got)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + (uint32_t)(buf * 256) + lane_off;
@@ -1588,12 +1589,14 @@ __global__ void __launch_bounds__(kStdThreads, 1)
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
                                                                  t.group * p.o_group_stride + tok * p.ldo + n);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     } else if constexpr (EPI == EPI_BF16) {
                         uint32_t w[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            w[i] = (uint32_t)f32_to_bf16_bits(v[2 * i]) | ((uint32_t)f32_to_bf16_bits(v[2 * i + 1]) << 16);
+                            w[i] = (uint32_t)f32_to_bf16_bits(v[2 * i]) |
+                                   ((uint32_t)f32_to_bf16_bits(v[2 * i + 1]) << 16);
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
                                                                t.group * p.o_group_stride + tok * p.ldo + n);
                         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -1623,7 +1626,8 @@ __global__ void __launch_bounds__(kStdThreads, 1)
         // (from both CTAs) have landed and been consumed
         const int64_t first = issued > S ? issued - S : 0;
         for (int64_t i = first; i < issued; ++i) {
-            const bool done = mbar_wait_drain(bar_addr(&ctl->empty[i % S]), (uint32_t)((i / S) & 1), drain_limit_ns(p.wait_limit_ns));
+            const bool done = mbar_wait_drain(bar_addr(&ctl->empty[i % S]), (uint32_t)((i / S) & 1),
+                                              drain_limit_ns(p.wait_limit_ns));
             if (!done) __nanosleep(200000);   // abort path: let in-flight copies land
         }
     }
