@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.oracle_mlp_forward.argtypes = [P, i64, i64, i64, P, P, P, i64, P, P, P, ci]
             L.oracle_shard_partial.restype = ci
             L.oracle_shard_partial.argtypes = [P, i64, i64, i64, P, P, ci, ci, P, i64, P, P, ci, ci]
+            L.oracle_shard_group_sum.restype = ci
+            L.oracle_shard_group_sum.argtypes = [P, i64, i64, i64, P, P, ci, ci, ci, P, i64, P, P, ci, ci]
             L.oracle_shard_sum.restype = None
             L.oracle_shard_sum.argtypes = [P, ci, ci, i64, i64, P]
             L.oracle_rank_major_to_logical.restype = ci
@@ -165,6 +167,23 @@ def shard_partial(x, w_gate_up, w_down, tp, rank, dtype=BF16, rows=None, nthread
     if rc != 0:
         raise ValueError("invalid shard geometry")
     return pf, pr
+
+
+def shard_group_sum(x, w_gate_up, w_down, tp, rank_first=0, rank_count=None, dtype=BF16, rows=None,
+                    nthreads=None):
+    """Sum of shards rank_first.. fp64 partials, rounded once -> (sum fp64 [n x H], rounded)."""
+    x = _u16(x); wgu = _u16(w_gate_up); wd = _u16(w_down)
+    T, H = x.shape
+    I = wgu.shape[0] // 2
+    rank_count = tp - rank_first if rank_count is None else rank_count
+    r, n = _rows(rows, T)
+    sf = np.empty((n, H), dtype=np.float64)
+    sr = np.empty((n, H), dtype=np.uint16 if dtype == BF16 else np.float32)
+    rc = lib().oracle_shard_group_sum(_p(x), T, H, I, _p(wgu), _p(wd), tp, rank_first, rank_count, _p(r), n,
+                                      _p(sf), _p(sr), dtype, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("invalid shard geometry")
+    return sf, sr
 
 
 def shard_sum(partials, dtype=BF16):

@@ -14,7 +14,9 @@
  *     x @ cat([gate, up]).T, times down.T);
  *   - the shard partial of rank r over intermediate slice [r*s, (r+1)*s), s = I/tp,
  *     and the sum of partials (same prhub section: per-rank slices of gate, up
- *     and of the down columns, then stack(partials).sum(0));
+ *     and of the down columns, then stack(partials).sum(0)), either of partials
+ *     already rounded to their storage dtype or of a group of shards' fp64
+ *     partials rounded once;
  *   - the merged q_a/kv_a projection stored as column shards whose gathered
  *     output is rank-major and is reordered to logical [q_a | kv_a]
  *     ("[II] TP-shard Kimi MLA latent projections", sections "Behavior" and
@@ -213,6 +215,36 @@ int oracle_shard_partial(const uint16_t *x, int64_t T, int64_t H, int64_t I,
     }
     free(acc);
     free(h);
+    return 0;
+}
+
+/* The summed partials of shards [rank_first, rank_first + rank_count) of tp: the
+ * reduce-scatter's sum (Kimi-K3 PR, section "Change"; prhub section "关键源码片段",
+ * stack(partials).sum(0)) taken over the shards' fp64 partials before any rounding,
+ * r ascending, then rounded once.  This is the sum a GEMM epilogue that reduces
+ * the partials itself produces: no partial is rounded to a storage dtype. */
+int oracle_shard_group_sum(const uint16_t *x, int64_t T, int64_t H, int64_t I,
+                           const uint16_t *w_gate_up, const uint16_t *w_down,
+                           int tp, int rank_first, int rank_count,
+                           const int64_t *rows, int64_t n_rows,
+                           double *out_f64, void *out_round, int dtype, int nthreads) {
+    if (tp <= 0 || I % tp != 0 || rank_first < 0 || rank_count < 1 || rank_first + rank_count > tp)
+        return -1;
+    double *sum = (double *)calloc((size_t)(n_rows * H), sizeof(double));
+    double *part = (double *)malloc(sizeof(double) * (size_t)(n_rows * H));
+    for (int r = rank_first; r < rank_first + rank_count; ++r) {
+        oracle_shard_partial(x, T, H, I, w_gate_up, w_down, tp, r, rows, n_rows, part, NULL, 0, nthreads);
+        for (int64_t e = 0; e < n_rows * H; ++e) sum[e] += part[e];
+    }
+    for (int64_t e = 0; e < n_rows * H; ++e) {
+        if (out_f64) out_f64[e] = sum[e];
+        if (out_round) {
+            if (dtype == 0) ((uint16_t *)out_round)[e] = oracle_f64_to_bf16_rne(sum[e]);
+            else ((float *)out_round)[e] = (float)sum[e];
+        }
+    }
+    free(part);
+    free(sum);
     return 0;
 }
 

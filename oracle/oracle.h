@@ -48,6 +48,15 @@ int oracle_shard_partial(const uint16_t *x, int64_t T, int64_t H, int64_t I,
 void oracle_shard_sum(const void *partials, int dtype, int n_parts, int64_t T, int64_t H,
                       uint16_t *out);
 
+/* out = round(sum_{r = rank_first .. rank_first + rank_count - 1} P_r), the fp64
+ * partials summed r ascending before any rounding; out_f64 (nullable) is the sum,
+ * out_round (nullable) its bf16 (dtype 0) or fp32 (dtype 1) rounding. */
+int oracle_shard_group_sum(const uint16_t *x, int64_t T, int64_t H, int64_t I,
+                           const uint16_t *w_gate_up, const uint16_t *w_down,
+                           int tp, int rank_first, int rank_count,
+                           const int64_t *rows, int64_t n_rows,
+                           double *out_f64, void *out_round, int dtype, int nthreads);
+
 /* Gathered (rank-major) column g  ->  logical column of [q_a | kv_a]. */
 int oracle_rank_major_to_logical(int64_t q_dim, int64_t kv_dim, int tp, int64_t *logical_of_gathered);
 

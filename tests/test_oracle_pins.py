@@ -347,6 +347,75 @@ def test_shard_geometry_rejected():
         oracle.rank_major_to_logical(1536, 576, 5)  # merged sizes not divisible
 
 
+# ----------------------------------------------------------------------------------
+# partials of a group of shards summed before any rounding (the fused reduce)
+# ----------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,H,I,tp,rf,rc,seed", [(2, 5, 4, 2, 0, 2, 11), (3, 6, 6, 3, 1, 2, 12),
+                                                 (2, 8, 8, 4, 1, 2, 13), (3, 4, 6, 3, 2, 1, 14)])
+def test_shard_group_sum_matches_exact_brute_force(T, H, I, tp, rf, rc, seed):
+    # exact rationals: h rounded exactly, then the sum over the group's intermediate
+    # columns [rf*s, (rf+rc)*s) only, rounded once (bf16) or to fp32
+    x = W.make_custom(seed, 0, (T, H), 1.5)
+    wgu = W.make_custom(seed, 1, (2 * I, H), 1.0)
+    wd = W.make_custom(seed, 2, (H, I), 1.0)
+    hb, h_tie, D = brute_force_mlp(x, wgu, wd)
+    assert (h_tie < 1e-9).sum() == 0
+    s = I // tp
+    j0, j1 = rf * s, (rf + rc) * s
+    sf, sb = oracle.shard_group_sum(x, wgu, wd, tp, rf, rc, oracle.BF16)
+    _, s32 = oracle.shard_group_sum(x, wgu, wd, tp, rf, rc, oracle.F32)
+    for t in range(T):
+        for n in range(H):
+            exact = sum(Fraction(float(hb[t, j])) * D[n][j] for j in range(j0, j1))
+            assert abs(float(exact) - sf[t, n]) <= 1e-13 * max(1.0, abs(float(exact)))
+            v, tie = round_bf16_exact(exact)
+            if tie > 1e-9:
+                assert oracle.bf16_to_f64(int(sb[t, n])) == float(v)
+            assert s32[t, n] == np.float32(float(exact))
+
+
+def test_shard_group_sum_of_all_shards_is_the_replicated_layer():
+    # the pages' invariant: summing every shard's partial gives the replicated output
+    T, H, I, tp = 6, 64, 48, 8
+    x = W.make_custom(22, 0, (T, H))
+    wgu = W.make_custom(22, 1, (2 * I, H), 1 / 8)
+    wd = W.make_custom(22, 2, (H, I), 1 / 7)
+    y, yf, _ = oracle.mlp_forward(x, wgu, wd)
+    sf, sb = oracle.shard_group_sum(x, wgu, wd, tp, 0, tp, oracle.BF16)
+    np.testing.assert_allclose(sf, yf, rtol=1e-12, atol=1e-13)
+    differ = sb != y
+    # only where the two fp64 sums straddle a bf16 rounding boundary
+    for t, n in zip(*np.nonzero(differ)):
+        _, tie = round_bf16_exact(Fraction(float(yf[t, n])))
+        assert tie < 1e-9
+
+
+def test_shard_group_sum_tiny_case_within_page_tolerance():
+    # the page's equivalence case at fp32: each rank's token rows of the summed
+    # partials are within the printed 1e-5 of the replicated layer
+    w = W.TINY_SHARDED
+    x = W.make_x(w)
+    wgu, wd = W.make_mlp_weights(w)
+    _, yf, _ = oracle.mlp_forward(x, wgu, wd)
+    _, s32 = oracle.shard_group_sum(x, wgu, wd, w.tp, 0, w.tp, oracle.F32)
+    g = read_golden("tiny_sharded_case.txt")
+    tpr = int(g["tokens_per_rank"][0])
+    for r in range(w.tp):
+        sl = slice(r * tpr, (r + 1) * tpr)
+        np.testing.assert_allclose(s32[sl].astype(np.float64), yf[sl], rtol=float(g["rtol"][0]),
+                                   atol=float(g["atol"][0]))
+
+
+def test_shard_group_geometry_rejected():
+    w = W.TINY_SHARDED
+    x = W.make_x(w)
+    wgu, wd = W.make_mlp_weights(w)
+    for tp, rf, rc in [(5, 0, 5), (4, 3, 2), (4, -1, 2), (4, 0, 0)]:
+        with pytest.raises(ValueError):
+            oracle.shard_group_sum(x, wgu, wd, tp, rf, rc)
+
+
 def test_feature_slice_concatenation_design_fails():
     """The rejected earlier design (output-dim sharding + all-gather of feature slices)
     under disjoint token shards must NOT match; with every rank holding the same tokens
