@@ -8,7 +8,10 @@ same number also given as microseconds per layer.  Weights are cycled over
 distinct copies (more bytes than L2), so no step reads its weights from L2.
 
 Extra lines in the same JSON object: the T = 8192 prefill layer (TFLOP/s), the
-TP8-sharded form (partials + shard_sum) and the merged MLA q_a/kv_a projection.
+TP8-sharded form (partials + shard_sum, and the partials summed inside the down
+projection), one rank's partial at TP4/TP8/TP16 and the merged MLA q_a/kv_a projection.
+`--only tp-sweep` prints instead the replicated-vs-sharded per-GPU time over token
+counts and tp (kernels measured, collectives modelled).
 
 `--impl reference` times the fp64 CPU oracle on the host cores instead.
 Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
@@ -366,6 +369,162 @@ def bench_tp8(w, K, Wm, layers):
     return s / K
 
 
+def bench_tp8_summed(w, K, Wm, layers):
+    """All shards' partials summed inside the down projection (mlp_swiglu_shard_forward):
+    no partial round trip, one [T x H] bf16 output."""
+    import torch
+    import moe_shared_expert_gb300 as mse
+    L = mse.lib()
+    T, H, I, tp = w.T, w.H, w.I, w.tp
+    x = dev_bf16(W.make_x(w))
+    wgu_b, wd_b = W.make_mlp_weights(w)
+    gus, wds = weight_copies(dev_bf16(wgu_b), dev_bf16(wd_b), layers)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    ws = mse.new_mlp_workspace(T, H, I)
+    sp = torch.cuda.current_stream().cuda_stream
+    pgu = [g.data_ptr() for g in gus]
+    pwd = [d.data_ptr() for d in wds]
+    bad = [0]
+
+    def step(i):
+        j = i % layers
+        bad[0] |= L.mlp_swiglu_shard_forward(x.data_ptr(), T, H, I, pgu[j], pwd[j], tp, 0, tp, out.data_ptr(), 0,
+                                             out.numel(), ws.data_ptr(), ws.numel(), sp)
+
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    s = time_loop(step, K, torch.cuda.current_stream())
+    if bad[0]:
+        raise RuntimeError("summed shard forward error status")
+    del gus, wds
+    torch.cuda.empty_cache()
+    return s / K
+
+
+class RankShapes:
+    """Decode weights (2 distinct copies, 528 MB) and tokens for per-rank timings: a step
+    of one rank r of a tp-way split reads that rank's slices only, so steps cycle through
+    the ranks and copies and no step finds its slice in L2."""
+
+    def __init__(self, max_T, copies=2):
+        import moe_shared_expert_gb300 as mse
+        w = W.DECODE_T64
+        self.H, self.I = w.H, w.I
+        wgu_b, wd_b = W.make_mlp_weights(w)
+        self.gus, self.wds = weight_copies(dev_bf16(wgu_b), dev_bf16(wd_b), copies)
+        self.copies = copies
+        self.x = dev_bf16(W.make_custom(77, 0, (max_T, self.H)))
+        self.ws = {}
+        self.mse = mse
+
+    def workspace(self, T):
+        if T not in self.ws:
+            self.ws.clear()
+            import torch
+            torch.cuda.empty_cache()
+            self.ws[T] = self.mse.new_mlp_workspace(T, self.H, self.I)
+        return self.ws[T]
+
+    def _time(self, step, K, Wm):
+        import torch
+        for i in range(Wm):
+            step(i)
+        torch.cuda.synchronize()
+        if K is None:      # size the loop to about 0.15 s
+            t = time_loop(step, 10, torch.cuda.current_stream()) / 10
+            K = int(max(20, min(4000, 0.15 / max(t, 1e-7))))
+        return time_loop(step, K, torch.cuda.current_stream()) / K
+
+    def rank_partial(self, T, tp, K=None, Wm=5):
+        """One rank's partial [T x H] bf16 over its 1/tp of the weights (T gathered tokens)."""
+        import torch
+        L = self.mse.lib()
+        H, I = self.H, self.I
+        out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        ws = self.workspace(T)
+        sp = torch.cuda.current_stream().cuda_stream
+        bad = [0]
+
+        def step(i):
+            r, c = i % tp, (i // tp) % self.copies
+            bad[0] |= L.mlp_swiglu_shard_partial(self.x.data_ptr(), T, H, I, self.gus[c].data_ptr(),
+                                                 self.wds[c].data_ptr(), tp, r, 1, out.data_ptr(), 0, out.numel(),
+                                                 ws.data_ptr(), ws.numel(), sp)
+
+        t = self._time(step, K, Wm)
+        if bad[0]:
+            raise RuntimeError("rank partial error status")
+        return t
+
+    def replicated(self, T, K=None, Wm=5):
+        """The full layer on T tokens (a replicated rank on its own tokens)."""
+        import torch
+        L = self.mse.lib()
+        H, I = self.H, self.I
+        out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        ws = self.workspace(T)
+        sp = torch.cuda.current_stream().cuda_stream
+        bad = [0]
+
+        def step(i):
+            c = i % self.copies
+            bad[0] |= L.mlp_swiglu_forward(self.x.data_ptr(), T, H, I, self.gus[c].data_ptr(),
+                                           self.wds[c].data_ptr(), out.data_ptr(), out.numel(), ws.data_ptr(),
+                                           ws.numel(), sp)
+
+        t = self._time(step, K, Wm)
+        if bad[0]:
+            raise RuntimeError("replicated error status")
+        return t
+
+
+def tp_sweep(args):
+    """Per-GPU time of the replicated and the TP-sharded MLP block under sequence
+    parallelism, over the group's token count T and tp.  Replicated: each rank runs the
+    full layer on its T/tp own tokens.  Sharded: each rank runs its 1/tp slice on all T
+    gathered tokens, plus an all-gather of the tokens and a reduce-scatter of the bf16
+    partials.  Kernel times are measured; the two collectives are MODELLED (this library
+    runs on one GPU): per collective  alpha + (tp-1)/tp * T*H*2 bytes / beta."""
+    import torch
+    torch.cuda.set_device(0)
+    from moe_shared_expert_gb300 import _build
+    _build.build()
+    import moe_shared_expert_gb300 as mse
+    mse.lib()
+    Ts = [int(v) for v in args.sweep_tokens.split(",")]
+    tps = [int(v) for v in args.sweep_tp.split(",")]
+    rs = RankShapes(max(Ts))
+    H, I = rs.H, rs.I
+    alpha, beta = args.coll_alpha_us * 1e-6, args.coll_link_gbs * 1e9
+    points = []
+    for tp in tps:
+        for T in Ts:
+            if T % tp:
+                continue
+            t_rep = rs.replicated(T // tp)
+            t_shard = rs.rank_partial(T, tp)
+            coll = 2 * (alpha + (tp - 1) / tp * T * H * 2 / beta)
+            points.append({"tp": tp, "T": T, "replicated_us": t_rep * 1e6, "sharded_kernel_us": t_shard * 1e6,
+                           "sharded_with_collectives_us": (t_shard + coll) * 1e6,
+                           "collectives_model_us": coll * 1e6})
+    cross = {}
+    for tp in tps:
+        pts = [p for p in points if p["tp"] == tp]
+        k = [p["T"] for p in pts if p["sharded_kernel_us"] >= p["replicated_us"]]
+        c = [p["T"] for p in pts if p["sharded_with_collectives_us"] >= p["replicated_us"]]
+        cross[str(tp)] = {"kernel_only_first_T_replicated_wins": min(k) if k else None,
+                          "with_modelled_collectives_first_T_replicated_wins": min(c) if c else None}
+    line = {"metric": "per-GPU µs of the MLP block: replicated vs TP-sharded under sequence parallelism",
+            "unit": "us", "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "tp_crossover_sweep", "H": H, "I": I, "tokens": Ts, "tp": tps,
+                       "weights": "decode weights, 2 copies cycled (and ranks cycled for the sharded slices)",
+                       "collective_model": {"alpha_us": args.coll_alpha_us, "link_GBps": args.coll_link_gbs,
+                                            "kind": "modelled, not measured"}},
+            "points": points, "crossover": cross}
+    print(json.dumps(line), flush=True)
+
+
 def bench_mla(w, K, Wm, copies=24):
     import torch
     import moe_shared_expert_gb300 as mse
@@ -470,6 +629,21 @@ def gpu_arm(args):
                                       "frac_of_hbm": b3 / s3 / 1e9 / peaks["hbm_gbs"],
                                       "partials_roundtrip_bytes": 2 * w3.tp * w3.T * w3.H * 2,
                                       "gpu_launches_per_step": 3}
+        s3b = bench_tp8_summed(w3, args.aux_steps, args.warmup, args.layers)
+        extra["tp8_summed_in_down_t128"] = {"us": s3b * 1e6, "tbps_algorithmic": b3 / s3b / 1e12,
+                                            "frac_of_hbm": b3 / s3b / 1e9 / peaks["hbm_gbs"],
+                                            "partials_roundtrip_bytes": 0, "gpu_launches_per_step": 2,
+                                            "entry": "mlp_swiglu_shard_forward"}
+        rs = RankShapes(64)
+        per_rank = {}
+        for tp in (4, 8, 16):
+            t = rs.rank_partial(64, tp, K=args.aux_steps, Wm=args.warmup)
+            b = mlp_bytes(64, w.H, w.I // tp)
+            per_rank[f"tp{tp}"] = {"us": t * 1e6, "slice": w.I // tp, "tbps_algorithmic": b / t / 1e12,
+                                   "frac_of_hbm": b / t / 1e9 / peaks["hbm_gbs"]}
+        extra["one_rank_partial_t64"] = per_rank
+        del rs
+        torch.cuda.empty_cache()
         w4 = W.MLA_MERGED
         s4 = bench_mla(w4, args.aux_steps, args.warmup)
         C = w4.q_dim + w4.kv_dim
@@ -602,7 +776,13 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--aux-steps", type=int, default=2000)
     ap.add_argument("--decode-only", action="store_true", help="same as --only decode")
-    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill"])
+    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill", "tp-sweep"])
+    ap.add_argument("--sweep-tokens", default="16,32,64,128,256,512,1024,2048")
+    ap.add_argument("--sweep-tp", default="4,8,16")
+    ap.add_argument("--coll-alpha-us", type=float, default=10.0,
+                    help="modelled fixed cost of one collective (tp-sweep)")
+    ap.add_argument("--coll-link-gbs", type=float, default=800.0,
+                    help="modelled per-GPU link bandwidth of one collective (tp-sweep)")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
@@ -615,6 +795,8 @@ def main():
         args.only = "decode"
     if args.impl == "reference":
         reference_arm(args)
+    elif args.only == "tp-sweep":
+        tp_sweep(args)
     else:
         gpu_arm(args)
 

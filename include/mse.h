@@ -87,20 +87,27 @@ typedef enum { MSE_PREFILL_AUTO = 0, MSE_PREFILL_SINGLE = 1, MSE_PREFILL_PAIR = 
 
 /* ---------------------------------------------------------------------------
  * Workspace sizing.  The workspace holds the bf16 intermediate h [T x I] and,
- * for the tensor-core path, fp32 split-K partial tiles and tile counters.
- * It must be 256-byte aligned and ZERO-FILLED before its first use; every call
- * that completes leaves the counter region zero again, so one workspace can be
- * reused by consecutive calls on one stream.  Calls that run concurrently
- * (different streams) need different workspaces.  After MSE_ERR_TIMEOUT the
- * caller must zero the workspace again.
+ * for the tensor-core path, fp32 split-K partial tiles and the sync words (tile
+ * counters and flags).  It must be 256-byte aligned and ZERO-FILLED before its
+ * first use.  The sync words sit at the END of the buffer (their size depends on
+ * H and I, or on q_dim + kv_dim, only); h and the partial tiles are laid out from
+ * its start.  Every call that completes leaves the sync words zero again, so a
+ * workspace of mlp_swiglu_workspace_bytes(T, H, I) bytes serves any sequence of
+ * calls on one stream with at most T tokens and the same H and I (likewise for
+ * the merged projection).  A call with another H or I needs a freshly zeroed
+ * workspace.  Calls that run concurrently (different streams) need different
+ * workspaces.  After MSE_ERR_TIMEOUT the caller must zero the workspace again.
+ * A call accepts any workspace at least as large as its own minimal need, which
+ * can be smaller than the size query's answer (the query covers all smaller T).
  * ------------------------------------------------------------------------- */
 
-/* Bytes needed by mlp_swiglu_forward and mlp_swiglu_shard_partial for T tokens
- * (the same size serves both; tp does not change it).  Returns 0 on invalid
- * arguments. */
+/* Bytes of a workspace that serves mlp_swiglu_forward, mlp_swiglu_shard_partial
+ * and mlp_swiglu_shard_forward for every token count up to T (tp does not change
+ * it).  Returns 0 on invalid arguments. */
 MSE_API size_t mlp_swiglu_workspace_bytes(int64_t T, int64_t H, int64_t I);
 
-/* Bytes needed by merged_proj_forward.  Returns 0 on invalid arguments. */
+/* Bytes of a workspace that serves merged_proj_forward for every token count up
+ * to T with the same q_dim + kv_dim.  Returns 0 on invalid arguments. */
 MSE_API size_t merged_proj_workspace_bytes(int64_t T, int64_t H, int64_t q_dim, int64_t kv_dim);
 
 /* ---------------------------------------------------------------------------
@@ -144,6 +151,51 @@ MSE_API mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_
                                     void *partials, mse_dtype partial_dtype,
                                     int64_t partials_capacity,
                                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * The partials of shards [rank_first, rank_first + rank_count) summed inside the
+ * down projection: a GEMM whose epilogue does the reduce-scatter's sum (Kimi-K3
+ * PR, section "Change": the block-end reduce-scatter sums across TP and restores
+ * the sequence sharding; prhub analysis of vllm PR #50656, section "关键源码片段":
+ * per-shard partials, then stack(partials).sum(0)).  No partial is rounded or
+ * stored: the down projection accumulates the group's intermediate columns
+ * [rank_first*s, (rank_first + rank_count)*s), s = I/tp, in fp32 (split across
+ * CTAs in ascending k order), and the sum is rounded once.
+ *
+ *   out   [T x H], out_dtype MSE_BF16 or MSE_F32, out_capacity >= T*H.
+ *         rank_count = tp: the whole TP group's reduced output; rank r's scatter
+ *         share is the row block [r*T/tp, (r+1)*T/tp) (a view; nothing is copied).
+ *         rank_count < tp: the group's pre-reduced partial, which a cross-GPU
+ *         reduce-scatter would sum with the other groups'.
+ *   Same inputs, workspace and stream rules as mlp_swiglu_shard_partial.
+ *
+ * Errors: MSE_ERR_NOT_DIVISIBLE if I % tp or H % tp; MSE_ERR_GEOMETRY if
+ * rank_first < 0, rank_count < 1, rank_first + rank_count > tp or
+ * out_capacity < T*H; MSE_ERR_INVALID_ARG for an unknown out_dtype.
+ * ------------------------------------------------------------------------- */
+MSE_API mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I,
+                                    const mse_bf16 *w_gate_up, const mse_bf16 *w_down,
+                                    int tp, int rank_first, int rank_count,
+                                    void *out, mse_dtype out_dtype, int64_t out_capacity,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Whether a dense or shared-expert MLP is to be TP-sharded under sequence
+ * parallelism rather than replicated on every rank (prhub analysis of vllm PR
+ * #50656, section "实现拆解", item 2; Kimi-K3 PR, sections "Change" and "Trade-off
+ * and why it is opt-in"): 1
+ * when all of
+ *   - enabled: the opt-in switch is on (it is off by default);
+ *   - use_sequence_parallel: the model runs with sequence parallelism;
+ *   - eligible: the call site may shard (shared experts only on the path whose
+ *     MoE block hands them the tokens directly; dense MLPs always);
+ *   - tp_size > 1, and hidden_size % tp_size == 0 and
+ *     intermediate_size % tp_size == 0;
+ * hold, else 0: the MLP stays replicated (the conservative fallback, never an
+ * error).  A pure host function: it touches no GPU and needs no device.
+ * ------------------------------------------------------------------------- */
+MSE_API int mse_shard_sequence_parallel_mlp(int enabled, int use_sequence_parallel, int eligible,
+                                            int tp_size, int64_t hidden_size, int64_t intermediate_size);
 
 /* ---------------------------------------------------------------------------
  * Sum of partials: the reduction half of the block-end reduce-scatter

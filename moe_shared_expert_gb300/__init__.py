@@ -6,9 +6,10 @@ streams) into pointers and sizes and turns status codes into exceptions.  There
 is no CPU or PyTorch fallback: if the library is missing, every call raises.
 
 Functions carry the C-ABI names:
-    mlp_swiglu_forward, mlp_swiglu_shard_partial, shard_sum,
-    merged_proj_forward, merged_proj_reorder
-plus the workspace queries, the device-error poll and the settings.
+    mlp_swiglu_forward, mlp_swiglu_shard_partial, mlp_swiglu_shard_forward, shard_sum,
+    merged_proj_forward, merged_proj_reorder, shard_sequence_parallel_mlp
+plus the workspace queries, the device-error poll and the settings, and
+``sequence_parallel_mlp``, which takes the sharding decision and makes the matching call.
 """
 from __future__ import annotations
 
@@ -20,6 +21,7 @@ from . import _build
 
 __all__ = [
     "MSEError", "lib", "library_path", "mlp_swiglu_forward", "mlp_swiglu_shard_partial", "shard_sum",
+    "mlp_swiglu_shard_forward", "shard_sequence_parallel_mlp", "sequence_parallel_mlp",
     "merged_proj_forward", "merged_proj_reorder", "mlp_swiglu_workspace_bytes", "merged_proj_workspace_bytes",
     "poll_device_error", "set_wait_limit_ns", "get_wait_limit_ns", "set_kernel_path", "selftest_wait_timeout",
     "set_phase_events", "set_prefill_kernel", "set_tuning", "BF16", "F32", "PATH_AUTO", "PATH_GENERIC", "PATH_TENSORCORE",
@@ -68,6 +70,8 @@ def lib() -> ctypes.CDLL:
                 "merged_proj_workspace_bytes": (sz, [i64, i64, i64, i64]),
                 "mlp_swiglu_forward": (ci, [P, i64, i64, i64, P, P, P, i64, P, sz, P]),
                 "mlp_swiglu_shard_partial": (ci, [P, i64, i64, i64, P, P, ci, ci, ci, P, ci, i64, P, sz, P]),
+                "mlp_swiglu_shard_forward": (ci, [P, i64, i64, i64, P, P, ci, ci, ci, P, ci, i64, P, sz, P]),
+                "mse_shard_sequence_parallel_mlp": (ci, [ci, ci, ci, ci, i64, i64]),
                 "shard_sum": (ci, [P, ci, ci, i64, i64, P, i64, P]),
                 "merged_proj_forward": (ci, [P, i64, i64, P, i64, i64, ci, P, P, i64, P, sz, P]),
                 "merged_proj_reorder": (ci, [P, P, i64, i64, i64, ci, i64, P]),
@@ -205,6 +209,59 @@ def mlp_swiglu_shard_partial(x, w_gate_up, w_down, tp, rank_first=0, rank_count=
                                         workspace.numel() * workspace.element_size(), _stream(stream))
     _check("mlp_swiglu_shard_partial", st)
     return partials
+
+
+def mlp_swiglu_shard_forward(x, w_gate_up, w_down, tp, rank_first=0, rank_count=None, out_dtype=None,
+                             out=None, workspace=None, stream=None):
+    """Sum [T, H] of the partials of shards rank_first.. of a tp-way intermediate split,
+    reduced inside the down projection (no partial is rounded or stored)."""
+    torch = _torch()
+    _need(x, "x", _bf16s(), 2)
+    _need(w_gate_up, "w_gate_up", _bf16s(), 2)
+    _need(w_down, "w_down", _bf16s(), 2)
+    T, H = x.shape
+    I = w_down.shape[1]
+    rank_count = tp - rank_first if rank_count is None else rank_count
+    code = _dtype_code(torch.bfloat16 if out_dtype is None else out_dtype)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32 if code == F32 else torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = new_mlp_workspace(T, H, I, x.device)
+    st = lib().mlp_swiglu_shard_forward(_ptr(x), T, H, I, _ptr(w_gate_up), _ptr(w_down), tp, rank_first,
+                                        rank_count, _ptr(out), code, out.numel(), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("mlp_swiglu_shard_forward", st)
+    return out
+
+
+def shard_sequence_parallel_mlp(enabled, use_sequence_parallel, eligible, tp_size, hidden_size,
+                                intermediate_size) -> bool:
+    """True when the MLP is to be TP-sharded under sequence parallelism, False when it
+    stays replicated (the library's host-side gate; no GPU needed)."""
+    return bool(lib().mse_shard_sequence_parallel_mlp(int(bool(enabled)), int(bool(use_sequence_parallel)),
+                                                      int(bool(eligible)), int(tp_size), int(hidden_size),
+                                                      int(intermediate_size)))
+
+
+def sequence_parallel_mlp(x, w_gate_up, w_down, tp, enabled, use_sequence_parallel=True, eligible=True,
+                          out=None, workspace=None, stream=None):
+    """The MLP block of a tp-rank sequence-parallel group on one GPU.
+
+    ``x`` [T, H] holds the group's tokens, rank r's own tokens being the row block
+    [r*T/tp, (r+1)*T/tp).  Returns (out [T, H] bf16, sharded); rank r's result is the same
+    row block of ``out``.  Sharded: every shard's partial over the gathered tokens, summed
+    in the down projection (mlp_swiglu_shard_forward).  Replicated: each rank's full MLP
+    on its own tokens, which for independent token rows is one mlp_swiglu_forward call."""
+    _need(x, "x", _bf16s(), 2)
+    T, H = x.shape
+    I = w_down.shape[1]
+    if tp < 1 or T % tp != 0:
+        raise ValueError(f"{T} tokens cannot be split into {tp} equal rank blocks")
+    shard = shard_sequence_parallel_mlp(enabled, use_sequence_parallel, eligible, tp, H, I)
+    if shard:
+        return mlp_swiglu_shard_forward(x, w_gate_up, w_down, tp, out=out, workspace=workspace,
+                                        stream=stream), True
+    return mlp_swiglu_forward(x, w_gate_up, w_down, y=out, workspace=workspace, stream=stream), False
 
 
 def shard_sum(partials, out=None, stream=None):

@@ -88,17 +88,25 @@ int pow2_at_least(int v) {
 
 // ----------------------------------------------------------------- workspace
 // h | split-K slots of the (first) gate_up pass | of the down pass | of the second gate_up
-// pass | counters of the gate_up tiles | counters of the down tiles | h-tile flags | exit
-// and published-tile counts.  The
-// region from the first counter to the end must be zero before a call and is left
-// zero by every call that completes.
+// pass ... and, at the END of the caller's buffer, the sync words: counters of the gate_up
+// tiles | counters of the down tiles | h-tile flags | exit and published-tile counts.  The
+// sync words must be zero before a call and every call that completes leaves them zero.
+// Their size depends on H and I only and they sit at the buffer's end whatever T is, while
+// h and the slots grow from its start: so a workspace sized for T tokens serves every call
+// with at most T tokens and the same H and I, in any order, and each call finds the sync
+// words the previous one left at zero (the T-dependent h and slot regions never reach
+// them).  Calls with token counts above the swap-AB range use no sync words but keep the
+// room for them, so they do not overwrite them either.
 struct MlpWs {
     size_t h_off = 0, slots_off = 0, slots_dn_off = 0, slots_gu2_off = 0, cnt_gu_off = 0, cnt_dn_off = 0,
-           flags_off = 0, exit_off = 0, total = 0;
+           flags_off = 0, exit_off = 0, sync_off = 0, sync_bytes = 0, total = 0;
 };
 
 constexpr int64_t kSwapAbMaxT = 256;   // token counts served by the swap-AB kernels
 
+size_t align_down(size_t v, size_t a) { return v / a * a; }
+
+// Minimal layout for (T, H, I): the sync words directly after the slots.
 MlpWs mlp_ws_layout(int64_t T, int64_t H, int64_t I) {
     MlpWs w;
     size_t off = 0;
@@ -113,21 +121,40 @@ MlpWs mlp_ws_layout(int64_t T, int64_t H, int64_t I) {
         off = align_up(off + slot_region, 256);
         w.slots_gu2_off = off;
         off = align_up(off + slot_region, 256);
-        w.cnt_gu_off = off;
-        off = align_up(off + (size_t)((I + 63) / 64) * 4, 256);
-        w.cnt_dn_off = off;
-        off = align_up(off + (size_t)((I + 63) / 64) * (size_t)((H + 127) / 128) * 4, 256);
-        w.flags_off = off;
-        off = align_up(off + (size_t)((I + 63) / 64) * 4, 256);
-        w.exit_off = off;   // exit count, then the published-tile counts of the two gate_up passes
-        off = align_up(off + 12, 256);
     }
+    w.sync_off = off;
+    w.cnt_gu_off = off;
+    off = align_up(off + (size_t)((I + 63) / 64) * 4, 256);
+    w.cnt_dn_off = off;
+    off = align_up(off + (size_t)((I + 63) / 64) * (size_t)((H + 127) / 128) * 4, 256);
+    w.flags_off = off;
+    off = align_up(off + (size_t)((I + 63) / 64) * 4, 256);
+    w.exit_off = off;   // exit count, then the published-tile counts of the two gate_up passes
+    off = align_up(off + 12, 256);
+    w.sync_bytes = off - w.sync_off;
     w.total = off;
     return w;
 }
 
+// The layout inside a caller buffer of workspace_bytes (>= the minimal total): the sync
+// words moved to the buffer's last 256-aligned sync_bytes.
+MlpWs mlp_ws_place(int64_t T, int64_t H, int64_t I, size_t workspace_bytes) {
+    MlpWs w = mlp_ws_layout(T, H, I);
+    if (workspace_bytes < w.total) return w;
+    const size_t base = align_down(workspace_bytes - w.sync_bytes, 256);
+    const size_t delta = base - w.sync_off;
+    w.sync_off += delta;
+    w.cnt_gu_off += delta;
+    w.cnt_dn_off += delta;
+    w.flags_off += delta;
+    w.exit_off += delta;
+    return w;
+}
+
+// merged projection: split-K slots from the start, the tile counters at the end of the
+// caller's buffer (their size depends on C only), as for the MLP workspace.
 struct MergedWs {
-    size_t slots_off = 0, cnt_off = 0, total = 0;
+    size_t slots_off = 0, cnt_off = 0, cnt_bytes = 0, total = 0;
 };
 
 MergedWs merged_ws_layout(int64_t T, int64_t C) {
@@ -137,10 +164,17 @@ MergedWs merged_ws_layout(int64_t T, int64_t C) {
         const int bn = round_up16(T);
         w.slots_off = off;
         off = align_up(off + (size_t)tc::kMaxGrid * 2 * 128 * (size_t)bn * 4, 256);
-        w.cnt_off = off;
-        off = align_up(off + (size_t)((C + 127) / 128) * 4, 256);
     }
+    w.cnt_off = off;
+    w.cnt_bytes = align_up((size_t)((C + 127) / 128) * 4, 256);
+    off += w.cnt_bytes;
     w.total = off;
+    return w;
+}
+
+MergedWs merged_ws_place(int64_t T, int64_t C, size_t workspace_bytes) {
+    MergedWs w = merged_ws_layout(T, C);
+    if (workspace_bytes >= w.total) w.cnt_off = align_down(workspace_bytes - w.cnt_bytes, 256);
     return w;
 }
 
@@ -613,17 +647,13 @@ void record(std::atomic<void *> &ev, cudaStream_t s) {
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
 
-// Byte range of the split-K tile counters inside an mlp workspace (they must be zero
-// before a call); bytes = 0 when the layout has none.
-void mlp_workspace_counter_range(int64_t T, int64_t H, int64_t I, size_t *off, size_t *bytes) {
-    const MlpWs L = mlp_ws_layout(T, H, I);
-    if (L.cnt_gu_off == 0) {
-        *off = 0;
-        *bytes = 0;
-        return;
-    }
-    *off = L.cnt_gu_off;
-    *bytes = L.total - L.cnt_gu_off;
+// Byte range of the sync words (tile counters, h flags, exit counts) inside an mlp
+// workspace of workspace_bytes (they must be zero before a call).
+void mlp_workspace_counter_range(int64_t T, int64_t H, int64_t I, size_t workspace_bytes, size_t *off,
+                                 size_t *bytes) {
+    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes);
+    *off = L.sync_off;
+    *bytes = L.sync_bytes;
 }
 
 }  // namespace mse
@@ -637,13 +667,18 @@ extern "C" {
 
 size_t mlp_swiglu_workspace_bytes(int64_t T, int64_t H, int64_t I) {
     if (T <= 0 || H <= 0 || I <= 0) return 0;
-    return mlp_ws_layout(T, H, I).total;
+    // the largest need of any call with at most T tokens (the split-K slots of the swap-AB
+    // range can outweigh h of a few hundred tokens more), so that the buffer serves them all
+    const size_t n = mlp_ws_layout(T, H, I).total;
+    const size_t m = mlp_ws_layout(T < kSwapAbMaxT ? T : kSwapAbMaxT, H, I).total;
+    return n > m ? n : m;
 }
 
 size_t merged_proj_workspace_bytes(int64_t T, int64_t H, int64_t q_dim, int64_t kv_dim) {
     if (T <= 0 || H <= 0 || q_dim < 0 || kv_dim < 0 || q_dim + kv_dim <= 0) return 0;
     const size_t n = merged_ws_layout(T, q_dim + kv_dim).total;
-    return n == 0 ? 256 : n;
+    const size_t m = merged_ws_layout(T < kSwapAbMaxT ? T : kSwapAbMaxT, q_dim + kv_dim).total;
+    return n > m ? n : m;
 }
 
 mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, const mse_bf16 *w_gate_up,
@@ -651,7 +686,7 @@ mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I
                               size_t workspace_bytes, void *stream) {
     if (!x || !w_gate_up || !w_down || !y || T <= 0 || H <= 0 || I <= 0) return MSE_ERR_INVALID_ARG;
     if (y_capacity < T * H) return MSE_ERR_GEOMETRY;
-    const MlpWs L = mlp_ws_layout(T, H, I);
+    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes);
     if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MSE_ERR_WORKSPACE;
     DeviceInfo *d = nullptr;
@@ -700,7 +735,7 @@ mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int
     if (I % tp != 0 || H % tp != 0) return MSE_ERR_NOT_DIVISIBLE;
     if (rank_first < 0 || rank_count < 1 || (int64_t)rank_first + rank_count > tp) return MSE_ERR_GEOMETRY;
     if (partials_capacity < (int64_t)rank_count * T * H) return MSE_ERR_GEOMETRY;
-    const MlpWs L = mlp_ws_layout(T, H, I);
+    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes);
     if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MSE_ERR_WORKSPACE;
     DeviceInfo *d = nullptr;
@@ -737,6 +772,57 @@ mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int
     return tc_down(*d, h, T, H, I, w_down, j0, sw, rank_count, partials, epi, ws, L, s);
 }
 
+mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, const mse_bf16 *w_gate_up,
+                                    const mse_bf16 *w_down, int tp, int rank_first, int rank_count, void *out,
+                                    mse_dtype out_dtype, int64_t out_capacity, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    if (!x || !w_gate_up || !w_down || !out || T <= 0 || H <= 0 || I <= 0 || tp <= 0)
+        return MSE_ERR_INVALID_ARG;
+    if (out_dtype != MSE_BF16 && out_dtype != MSE_F32) return MSE_ERR_INVALID_ARG;
+    if (I % tp != 0 || H % tp != 0) return MSE_ERR_NOT_DIVISIBLE;
+    if (rank_first < 0 || rank_count < 1 || (int64_t)rank_first + rank_count > tp) return MSE_ERR_GEOMETRY;
+    if (out_capacity < T * H) return MSE_ERR_GEOMETRY;
+    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes);
+    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MSE_ERR_WORKSPACE;
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    const int64_t sw = I / tp;
+    Path path;
+    if ((st = choose(mlp_tc_ok(x, H, I, sw, w_gate_up, w_down, out, workspace), &path)) != MSE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h_off);
+    // the group's intermediate columns form one contiguous range: one reduction over it
+    const int64_t j0 = (int64_t)rank_first * sw, width = (int64_t)rank_count * sw;
+
+    if (path == PATH_GENERIC) {
+        SimtGemmArgs a = {};
+        a.A = x; a.lda = H; a.B = w_gate_up + j0 * H; a.B2 = w_gate_up + (I + j0) * H; a.ldb = H;
+        a.M = T; a.N = width; a.K = H; a.groups = 1; a.out = h + j0; a.ldo = I; a.mode = SIMT_SWIGLU;
+        if ((st = from_cuda(launch_simt_gemm(a, s))) != MSE_OK) return st;
+        SimtGemmArgs b = {};
+        b.A = h + j0; b.lda = I;
+        b.B = w_down + j0; b.ldb = I;
+        b.M = T; b.N = H; b.K = width; b.groups = 1;
+        b.out = out; b.ldo = H;
+        b.mode = out_dtype == MSE_F32 ? SIMT_F32 : SIMT_BF16;
+        return from_cuda(launch_simt_gemm(b, s));
+    }
+    const int epi = out_dtype == MSE_F32 ? tc::EPI_F32 : tc::EPI_BF16;
+    if (one_launch_enabled(T))
+        return tc_mlp_one_launch(*d, x, T, H, I, w_gate_up, w_down, j0, width, width, 1, out, epi, ws, L, s);
+    if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s)) != MSE_OK) return st;
+    return tc_down(*d, h, T, H, I, w_down, j0, width, 1, out, epi, ws, L, s);
+}
+
+int mse_shard_sequence_parallel_mlp(int enabled, int use_sequence_parallel, int eligible, int tp_size,
+                                    int64_t hidden_size, int64_t intermediate_size) {
+    if (!enabled || !use_sequence_parallel || !eligible || tp_size <= 1) return 0;
+    return hidden_size % tp_size == 0 && intermediate_size % tp_size == 0 ? 1 : 0;
+}
+
 mse_status shard_sum(const void *partials, mse_dtype partial_dtype, int n_parts, int64_t T, int64_t H,
                      mse_bf16 *out, int64_t out_capacity, void *stream) {
     if (!partials || !out || n_parts <= 0 || T <= 0 || H <= 0) return MSE_ERR_INVALID_ARG;
@@ -758,7 +844,7 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
     if (q_dim % tp != 0 || kv_dim % tp != 0) return MSE_ERR_NOT_DIVISIBLE;
     const int64_t C = q_dim + kv_dim;
     if (out_capacity < T * C) return MSE_ERR_GEOMETRY;
-    const MergedWs L = merged_ws_layout(T, C);
+    const MergedWs L = merged_ws_place(T, C, workspace_bytes);
     if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MSE_ERR_WORKSPACE;
     DeviceInfo *d = nullptr;

@@ -10,7 +10,8 @@
 
 namespace mse {
 // defined in api.cu
-void mlp_workspace_counter_range(int64_t T, int64_t H, int64_t I, size_t *off, size_t *bytes);
+void mlp_workspace_counter_range(int64_t T, int64_t H, int64_t I, size_t workspace_bytes, size_t *off,
+                                 size_t *bytes);
 }  // namespace mse
 
 namespace {
@@ -61,7 +62,7 @@ MSE_API mse_status mlp_swiglu_forward_static_scratch(const mse_bf16 *x, int64_t 
     }
     // The array keeps the previous call's contents: the tile counters must start at zero.
     size_t off = 0, bytes = 0;
-    mse::mlp_workspace_counter_range(T, H, I, &off, &bytes);
+    mse::mlp_workspace_counter_range(T, H, I, kStaticScratchBytes, &off, &bytes);
     if (bytes > 0 &&
         cudaMemsetAsync(static_cast<unsigned char *>(scratch) + off, 0, bytes, static_cast<cudaStream_t>(stream)) !=
             cudaSuccess) {

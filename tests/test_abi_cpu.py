@@ -26,7 +26,8 @@ def declared_symbols():
 
 def test_header_declares_the_entry_points():
     names = set(declared_symbols())
-    for n in ["mlp_swiglu_forward", "mlp_swiglu_shard_partial", "shard_sum", "merged_proj_forward",
+    for n in ["mlp_swiglu_forward", "mlp_swiglu_shard_partial", "mlp_swiglu_shard_forward",
+              "mse_shard_sequence_parallel_mlp", "shard_sum", "merged_proj_forward",
               "merged_proj_reorder", "mlp_swiglu_workspace_bytes", "merged_proj_workspace_bytes",
               "mse_poll_device_error", "mse_status_string"]:
         assert n in names
@@ -52,6 +53,17 @@ def test_workspace_sizes(L):
     assert L.mlp_swiglu_workspace_bytes(8192, H, I) >= 8192 * I * 2
     assert L.merged_proj_workspace_bytes(128, 7168, 1536, 576) > 0
     assert L.merged_proj_workspace_bytes(128, 7168, -1, 576) == 0
+
+
+def test_workspace_size_covers_every_smaller_token_count(L):
+    # the size query is non-decreasing in T: a buffer sized for T serves every call with
+    # fewer tokens (the split-K tiles of T <= 256 outweigh h of a few hundred more tokens)
+    for H, I in [(7168, 6144), (384, 320), (2048, 1536)]:
+        sizes = [L.mlp_swiglu_workspace_bytes(T, H, I) for T in list(range(1, 400)) + [1024, 8192]]
+        assert all(a <= b for a, b in zip(sizes, sizes[1:])), (H, I)
+        assert all(n % 256 == 0 for n in sizes)
+    m = [L.merged_proj_workspace_bytes(T, 7168, 1536, 576) for T in range(1, 400)]
+    assert all(a <= b for a, b in zip(m, m[1:]))
 
 
 # Fake, never-dereferenced addresses: every call below fails validation before any
@@ -104,6 +116,25 @@ def test_shard_partial_validation(L):
     assert f(*args(8, 0, 8, full - 1)) == code("MSE_ERR_GEOMETRY")   # truncated partial buffer
     assert f(*args(8, 0, 8, full, 7)) == code("MSE_ERR_INVALID_ARG")  # bad dtype
     assert f(*args(0, 0, 1, full)) == code("MSE_ERR_INVALID_ARG")
+
+
+@no_gpu_only
+def test_shard_forward_validation(L):
+    f = L.mlp_swiglu_shard_forward
+    args = lambda tp, rf, rc, cap, dt=0: (FAKE, 128, 7168, 6144, FAKE, FAKE, tp, rf, rc, FAKE, dt, cap, FAKE,
+                                          GOOD_WS, None)
+    one = 128 * 7168
+    assert f(*args(5, 0, 5, one)) == code("MSE_ERR_NOT_DIVISIBLE")     # 6144 % 5 != 0
+    assert f(*args(3, 0, 3, one)) == code("MSE_ERR_NOT_DIVISIBLE")     # 7168 % 3 != 0
+    assert f(*args(8, 6, 3, one)) == code("MSE_ERR_GEOMETRY")
+    assert f(*args(8, -1, 2, one)) == code("MSE_ERR_GEOMETRY")
+    assert f(*args(8, 0, 0, one)) == code("MSE_ERR_GEOMETRY")
+    assert f(*args(8, 0, 8, one - 1)) == code("MSE_ERR_GEOMETRY")      # one [T x H] output, truncated
+    assert f(*args(8, 0, 8, one, 7)) == code("MSE_ERR_INVALID_ARG")
+    assert f(*args(0, 0, 1, one)) == code("MSE_ERR_INVALID_ARG")
+    a = list(args(8, 0, 8, one))
+    a[12] = FAKE + 8                                                  # misaligned workspace
+    assert f(*a) == code("MSE_ERR_WORKSPACE")
 
 
 @no_gpu_only

@@ -338,6 +338,38 @@ def test_workspace_reuse_across_shapes_and_calls():
     assert mse.poll_device_error() == 0
 
 
+def test_workspace_reuse_across_token_counts_wide_grid():
+    # Shapes whose split-K tiles occupy many CTAs' partial-tile slots: a 256-token call
+    # writes fp32 tiles far into the buffer, and each later call with fewer (or more than
+    # 256) tokens must still find its sync words zero.  Every call equals the same call
+    # on a fresh workspace bit for bit (same launches, deterministic sums).
+    H, I = 2048, 1536
+    _, wgu, wd = small_case(8, H, I, 1200)
+    dgu, dwd = to_dev(wgu), to_dev(wd)
+    ws = mse.new_mlp_workspace(300, H, I)
+    for T in [256, 64, 300, 7, 256, 130, 64, 1]:
+        x = to_dev(W.make_custom(1210 + T, 0, (T, H)))
+        y = mse.mlp_swiglu_forward(x, dgu, dwd, workspace=ws)
+        s = mse.mlp_swiglu_shard_forward(x, dgu, dwd, 4, rank_first=1, rank_count=2, workspace=ws)
+        y_fresh = mse.mlp_swiglu_forward(x, dgu, dwd)
+        s_fresh = mse.mlp_swiglu_shard_forward(x, dgu, dwd, 4, rank_first=1, rank_count=2)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_fresh), f"T={T}"
+        assert torch.equal(s, s_fresh), f"T={T} shard group"
+    assert mse.poll_device_error() == 0
+    # the merged projection's workspace in the same way
+    q, kv, tp = 1536, 576, 16
+    wm = to_dev(W.make_custom(1230, 4, (q + kv, H), 1 / 45))
+    wsm = mse.new_merged_workspace(256, H, q, kv)
+    for T in [256, 16, 200, 1]:
+        x = to_dev(W.make_custom(1240 + T, 0, (T, H)))
+        lo, _ = mse.merged_proj_forward(x, wm, q, kv, tp, workspace=wsm)
+        lo_fresh, _ = mse.merged_proj_forward(x, wm, q, kv, tp)
+        torch.cuda.synchronize()
+        assert torch.equal(lo, lo_fresh), f"merged T={T}"
+    assert mse.poll_device_error() == 0
+
+
 def test_timeout_selftest_reports_and_context_survives():
     mse.selftest_wait_timeout(2_000_000)          # 2 ms wait that nothing satisfies
     assert mse.STATUS[mse.poll_device_error()] == "MSE_ERR_TIMEOUT"

@@ -1,0 +1,213 @@
+"""The shards' partials summed inside the down projection (mlp_swiglu_shard_forward)
+and the sequence-parallel MLP block (sequence_parallel_mlp) against the fp64 oracle.
+
+The oracle's reading: the group's fp64 partials summed, ranks ascending, and rounded
+once (the reduce-scatter's sum with no partial rounded to a storage dtype).  Also:
+the TP4 and TP16 shard shapes of the 7168 x 6144 shared expert (slices of 1536 and
+384 intermediate columns), the shapes the pages' tuned GEMM table lists besides TP8.
+
+Criterion: |gpu - oracle| <= 0.02 + 0.02 |oracle| per element; bit-exact where the
+inputs make every sum exact.
+"""
+import contextlib
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests.helpers import assert_close, bits_f64, kernel_path, to_bits, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+mse = pytest.importorskip("moe_shared_expert_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from moe_shared_expert_gb300 import _build
+    _build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mse.lib()
+    yield
+    assert mse.poll_device_error() == 0
+
+
+@contextlib.contextmanager
+def one_launch(mode: int):
+    old = mse.set_tuning(mse.TUNE_ONE_LAUNCH, mode)
+    assert old >= 0
+    try:
+        yield
+    finally:
+        mse.set_tuning(mse.TUNE_ONE_LAUNCH, old)
+
+
+def case(T, H, I, seed):
+    x = W.make_custom(seed, 0, (T, H))
+    wgu = W.make_custom(seed, 1, (2 * I, H), 1 / math.sqrt(H))
+    wd = W.make_custom(seed, 2, (H, I), 1 / math.sqrt(I))
+    return x, wgu, wd
+
+
+def got_f64(t, dtype):
+    return bits_f64(to_bits(t)) if dtype == oracle.BF16 else t.cpu().numpy().astype(np.float64)
+
+
+def ref_f64(r, dtype):
+    return bits_f64(r) if dtype == oracle.BF16 else r.astype(np.float64)
+
+
+_decode = {}
+
+
+def decode_weights():
+    if not _decode:
+        w = W.DECODE_T64
+        wgu, wd = W.make_mlp_weights(w)
+        _decode.update(x=W.make_x(w), wgu=wgu, wd=wd, dgu=to_dev(wgu), dwd=to_dev(wd))
+    return _decode
+
+
+# ------------------------------------------------------------------ shapes and subsets
+@pytest.mark.parametrize("T,H,I,tp,rf,rc", [
+    (1, 384, 384, 3, 0, 3), (7, 768, 384, 3, 1, 2), (64, 1024, 768, 4, 0, 4), (65, 640, 512, 4, 1, 2),
+    (130, 512, 1024, 8, 3, 4), (256, 384, 768, 4, 2, 1), (257, 512, 512, 4, 0, 4), (300, 384, 768, 3, 1, 2)])
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.F32])
+def test_shard_forward_matches_oracle(T, H, I, tp, rf, rc, dtype):
+    x, wgu, wd = case(T, H, I, 9600 + T + H + I + rf)
+    td = torch.bfloat16 if dtype == oracle.BF16 else torch.float32
+    out = mse.mlp_swiglu_shard_forward(to_dev(x), to_dev(wgu), to_dev(wd), tp, rank_first=rf, rank_count=rc,
+                                       out_dtype=td)
+    torch.cuda.synchronize()
+    _, ref = oracle.shard_group_sum(x, wgu, wd, tp, rf, rc, dtype)
+    assert_close(got_f64(out, dtype), ref_f64(ref, dtype), f"T={T} ranks {rf}..{rf + rc - 1}")
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("rf,rc", [(0, 4), (1, 2), (3, 1)])
+def test_shard_forward_one_launch(mode, rf, rc):
+    # the one-launch layer over a column range that starts inside the intermediate dim
+    T, H, I, tp = 48, 768, 1024, 4
+    x, wgu, wd = case(T, H, I, 9700 + rf)
+    with one_launch(mode):
+        out = mse.mlp_swiglu_shard_forward(to_dev(x), to_dev(wgu), to_dev(wd), tp, rank_first=rf, rank_count=rc)
+        again = mse.mlp_swiglu_shard_forward(to_dev(x), to_dev(wgu), to_dev(wd), tp, rank_first=rf,
+                                             rank_count=rc)
+    torch.cuda.synchronize()
+    _, ref = oracle.shard_group_sum(x, wgu, wd, tp, rf, rc, oracle.BF16)
+    assert_close(bits_f64(to_bits(out)), bits_f64(ref), f"one launch mode {mode}")
+    assert torch.equal(out, again)
+
+
+@pytest.mark.parametrize("path", [mse.PATH_TENSORCORE, mse.PATH_GENERIC])
+@pytest.mark.parametrize("T", [18, 300])
+def test_shard_forward_bit_exact_on_integer_inputs(path, T):
+    # one-hot weights, integer inputs: each output is one h value or an exact zero, so
+    # the group's column range is checked bit for bit through the kernels
+    H, I, tp = 384, 192, 3
+    rng = np.random.default_rng(T + H + I)
+    x = W.f32_to_bf16_bits((4.0 * rng.integers(5, 11, size=(T, H))).astype(np.float32))
+    wgu = np.zeros((2 * I, H), dtype=np.uint16)
+    j = np.arange(I)
+    wgu[j, j % H] = 0x3F80
+    wgu[I + j, (7 * j + 3) % H] = 0x3F80
+    wd = np.zeros((H, I), dtype=np.uint16)
+    n = np.arange(H)
+    wd[n, (5 * n + 1) % I] = 0x3F80
+    with kernel_path(path):
+        for rf, rc in [(0, 3), (1, 1), (1, 2)]:
+            out = mse.mlp_swiglu_shard_forward(to_dev(x), to_dev(wgu), to_dev(wd), tp, rank_first=rf,
+                                               rank_count=rc)
+            torch.cuda.synchronize()
+            _, ref = oracle.shard_group_sum(x, wgu, wd, tp, rf, rc, oracle.BF16)
+            assert np.array_equal(to_bits(out), ref), f"ranks {rf}..{rf + rc - 1}"
+
+
+def test_shard_forward_unaligned_shape_takes_generic_path():
+    T, H, I, tp = 9, 100, 36, 4
+    x, wgu, wd = case(T, H, I, 9800)
+    out = mse.mlp_swiglu_shard_forward(to_dev(x), to_dev(wgu), to_dev(wd), tp, rank_first=1, rank_count=2)
+    torch.cuda.synchronize()
+    _, ref = oracle.shard_group_sum(x, wgu, wd, tp, 1, 2, oracle.BF16)
+    assert_close(bits_f64(to_bits(out)), bits_f64(ref), "generic")
+
+
+# ------------------------------------------------------------------ the TP8 workload
+def test_tp8_t128_summed_in_the_down_projection():
+    # 128 gathered tokens, 8 shards of 768 intermediate columns: the whole group's sum
+    w = W.TP8_EMULATED
+    wgu, wd = W.make_mlp_weights(w)
+    x = W.make_x(w)
+    dx, dgu, dwd = to_dev(x), to_dev(wgu), to_dev(wd)
+    ws = mse.new_mlp_workspace(w.T, w.H, w.I)
+    out = mse.mlp_swiglu_shard_forward(dx, dgu, dwd, w.tp, workspace=ws)
+    y = mse.mlp_swiglu_forward(dx, dgu, dwd, workspace=ws)
+    parts = mse.mlp_swiglu_shard_partial(dx, dgu, dwd, w.tp, workspace=ws)
+    red = mse.shard_sum(parts)
+    torch.cuda.synchronize()
+    # the same reduction over the same columns as the replicated layer: same launches, same bits
+    assert torch.equal(out, y)
+    tpr = w.T // w.tp
+    rows = np.array([0, tpr - 1, tpr, 3 * tpr + 5, w.T - tpr, w.T - 1])
+    _, ref = oracle.shard_group_sum(x, wgu, wd, w.tp, 0, w.tp, oracle.BF16, rows=rows)
+    r = assert_close(bits_f64(to_bits(out)[rows]), bits_f64(ref), "summed partials, sampled rows")
+    print(f"tp8 summed in the down projection: max err/tol {r:.3f}")
+    # against the unfused path (bf16 partials, then their sum): both within tolerance of the oracle
+    assert_close(bits_f64(to_bits(red)[rows]), bits_f64(ref), "partials then shard_sum")
+
+
+# ------------------------------------------------------------------ TP4 / TP16 shard shapes
+@pytest.mark.parametrize("tp,rank", [(4, 1), (4, 3), (16, 0), (16, 11)])
+def test_tp4_tp16_shard_partials_decode_weights(tp, rank):
+    d = decode_weights()
+    x = d["x"]
+    rows = np.array([0, 17, 63])
+    part = mse.mlp_swiglu_shard_partial(to_dev(x), d["dgu"], d["dwd"], tp, rank_first=rank, rank_count=1)
+    torch.cuda.synchronize()
+    _, pr = oracle.shard_partial(x, d["wgu"], d["wd"], tp, rank, oracle.BF16, rows=rows)
+    assert_close(bits_f64(to_bits(part[0])[rows]), bits_f64(pr), f"tp{tp} rank {rank} (s={6144 // tp})")
+
+
+@pytest.mark.parametrize("tp,rf,rc", [(4, 0, 4), (16, 4, 4), (16, 15, 1)])
+def test_tp4_tp16_summed_groups_decode_weights(tp, rf, rc):
+    d = decode_weights()
+    x = d["x"]
+    rows = np.array([1, 40, 62])
+    out = mse.mlp_swiglu_shard_forward(to_dev(x), d["dgu"], d["dwd"], tp, rank_first=rf, rank_count=rc,
+                                       out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _, ref = oracle.shard_group_sum(x, d["wgu"], d["wd"], tp, rf, rc, oracle.F32, rows=rows)
+    assert_close(out.cpu().numpy()[rows].astype(np.float64), ref.astype(np.float64), f"tp{tp} ranks {rf}+{rc}")
+
+
+# ------------------------------------------------------------------ the sequence-parallel block
+@pytest.mark.parametrize("enabled", [True, False])
+def test_sequence_parallel_mlp_block(enabled):
+    # disjoint token blocks per rank; sharded or replicated, each rank's rows match
+    # the replicated layer on its own tokens
+    T, H, I, tp = 96, 1024, 768, 4
+    x, wgu, wd = case(T, H, I, 9900)
+    out, sharded = mse.sequence_parallel_mlp(to_dev(x), to_dev(wgu), to_dev(wd), tp, enabled)
+    torch.cuda.synchronize()
+    assert sharded is enabled
+    tpr = T // tp
+    for r in range(tp):
+        own = np.arange(r * tpr, (r + 1) * tpr)
+        y_ref, _, _ = oracle.mlp_forward(x[own], wgu, wd)
+        assert_close(bits_f64(to_bits(out)[own]), bits_f64(y_ref), f"rank {r} rows")
+
+
+def test_sequence_parallel_mlp_gate_falls_back_and_checks_blocks():
+    T, H, I = 60, 640, 320        # 640 % 3 != 0; 640 and 320 both divide by 5
+    x, wgu, wd = case(T, H, I, 9950)
+    _, sharded = mse.sequence_parallel_mlp(to_dev(x), to_dev(wgu), to_dev(wd), 3, True)
+    assert sharded is False       # 640 % 3 != 0: replicated, no error
+    _, sharded = mse.sequence_parallel_mlp(to_dev(x), to_dev(wgu), to_dev(wd), 5, True)
+    assert sharded is True
+    with pytest.raises(ValueError):
+        mse.sequence_parallel_mlp(to_dev(x), to_dev(wgu), to_dev(wd), 8, True)   # 60 % 8 != 0
+    torch.cuda.synchronize()
