@@ -405,7 +405,12 @@ def bench_tp8_summed(w, K, Wm, layers):
 class RankShapes:
     """Decode weights (2 distinct copies, 528 MB) and tokens for per-rank timings: a step
     of one rank r of a tp-way split reads that rank's slices only, so steps cycle through
-    the ranks and copies and no step finds its slice in L2."""
+    the ranks and copies and no step finds its slice in L2.
+
+    Steps are captured in a CUDA graph (every rank and copy once) and the graph is
+    replayed: a rank's step is a few microseconds of device work, less than the host
+    needs to issue it, so an eager loop would time the host.  Decode serving replays
+    graphs in the same way."""
 
     def __init__(self, max_T, copies=2):
         import moe_shared_expert_gb300 as mse
@@ -426,15 +431,29 @@ class RankShapes:
             self.ws[T] = self.mse.new_mlp_workspace(T, self.H, self.I)
         return self.ws[T]
 
-    def _time(self, step, K, Wm):
+    def _time(self, step, n_steps, K, Wm, bad):
+        """Device seconds per step: steps 0..n_steps-1 captured once, replayed."""
         import torch
-        for i in range(Wm):
+        for i in range(max(Wm, n_steps)):      # eager warm-up (also sets kernel attributes)
             step(i)
         torch.cuda.synchronize()
-        if K is None:      # size the loop to about 0.15 s
-            t = time_loop(step, 10, torch.cuda.current_stream()) / 10
-            K = int(max(20, min(4000, 0.15 / max(t, 1e-7))))
-        return time_loop(step, K, torch.cuda.current_stream()) / K
+        side = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(n_steps):
+                step(i)
+        if bad[0]:
+            raise RuntimeError("error status while capturing")
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        if K is None:      # size the replay loop to about 0.15 s
+            t = time_loop(lambda i: g.replay(), 5, torch.cuda.current_stream()) / 5
+            K = int(max(10, min(4000, 0.15 / max(t, 1e-7))))
+        else:
+            K = max(1, K // n_steps)
+        t = time_loop(lambda i: g.replay(), K, torch.cuda.current_stream())
+        return t / (K * n_steps)
 
     def rank_partial(self, T, tp, K=None, Wm=5):
         """One rank's partial [T x H] bf16 over its 1/tp of the weights (T gathered tokens)."""
@@ -443,16 +462,16 @@ class RankShapes:
         H, I = self.H, self.I
         out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
         ws = self.workspace(T)
-        sp = torch.cuda.current_stream().cuda_stream
         bad = [0]
 
         def step(i):
             r, c = i % tp, (i // tp) % self.copies
+            sp = torch.cuda.current_stream().cuda_stream
             bad[0] |= L.mlp_swiglu_shard_partial(self.x.data_ptr(), T, H, I, self.gus[c].data_ptr(),
                                                  self.wds[c].data_ptr(), tp, r, 1, out.data_ptr(), 0, out.numel(),
                                                  ws.data_ptr(), ws.numel(), sp)
 
-        t = self._time(step, K, Wm)
+        t = self._time(step, tp * self.copies, K, Wm, bad)
         if bad[0]:
             raise RuntimeError("rank partial error status")
         return t
@@ -464,19 +483,32 @@ class RankShapes:
         H, I = self.H, self.I
         out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
         ws = self.workspace(T)
-        sp = torch.cuda.current_stream().cuda_stream
         bad = [0]
 
         def step(i):
             c = i % self.copies
+            sp = torch.cuda.current_stream().cuda_stream
             bad[0] |= L.mlp_swiglu_forward(self.x.data_ptr(), T, H, I, self.gus[c].data_ptr(),
                                            self.wds[c].data_ptr(), out.data_ptr(), out.numel(), ws.data_ptr(),
                                            ws.numel(), sp)
 
-        t = self._time(step, K, Wm)
+        t = self._time(step, 2 * self.copies, K, Wm, bad)
         if bad[0]:
             raise RuntimeError("replicated error status")
         return t
+
+
+def apply_tuning(spec: str) -> dict:
+    """Set library tuning keys from 'name=value,...' (names of the binding's TUNE_* constants)."""
+    import moe_shared_expert_gb300 as mse
+    done = {}
+    for item in filter(None, (t.strip() for t in spec.split(","))):
+        name, value = item.split("=")
+        key = getattr(mse, "TUNE_" + name.strip().upper())
+        if mse.set_tuning(key, int(value)) < 0:
+            raise ValueError(f"tuning {item} rejected")
+        done[name.strip().lower()] = int(value)
+    return done
 
 
 def tp_sweep(args):
@@ -492,6 +524,7 @@ def tp_sweep(args):
     _build.build()
     import moe_shared_expert_gb300 as mse
     mse.lib()
+    tuning = apply_tuning(args.tune)
     Ts = [int(v) for v in args.sweep_tokens.split(",")]
     tps = [int(v) for v in args.sweep_tp.split(",")]
     rs = RankShapes(max(Ts))
@@ -518,6 +551,7 @@ def tp_sweep(args):
     line = {"metric": "per-GPU µs of the MLP block: replicated vs TP-sharded under sequence parallelism",
             "unit": "us", "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "tp_crossover_sweep", "H": H, "I": I, "tokens": Ts, "tp": tps,
+                       "timing": "CUDA graph replay of every rank and weight copy", "tuning": tuning,
                        "weights": "decode weights, 2 copies cycled (and ranks cycled for the sharded slices)",
                        "collective_model": {"alpha_us": args.coll_alpha_us, "link_GBps": args.coll_link_gbs,
                                             "kind": "modelled, not measured"}},
@@ -585,6 +619,7 @@ def gpu_arm(args):
     mse.lib()
     if args.two_launch:
         mse.set_tuning(mse.TUNE_ONE_LAUNCH, 0)
+    tuning = apply_tuning(args.tune)
     peaks = load_peaks()
     clocks = ClockSampler(dist.local) if dist.rank == 0 else None
 
@@ -640,7 +675,7 @@ def gpu_arm(args):
             t = rs.rank_partial(64, tp, K=args.aux_steps, Wm=args.warmup)
             b = mlp_bytes(64, w.H, w.I // tp)
             per_rank[f"tp{tp}"] = {"us": t * 1e6, "slice": w.I // tp, "tbps_algorithmic": b / t / 1e12,
-                                   "frac_of_hbm": b / t / 1e9 / peaks["hbm_gbs"]}
+                                   "frac_of_hbm": b / t / 1e9 / peaks["hbm_gbs"], "timing": "CUDA graph replay"}
         extra["one_rank_partial_t64"] = per_rank
         del rs
         torch.cuda.empty_cache()
@@ -688,7 +723,8 @@ def gpu_arm(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "weights": "N(0,1/fan_in) bf16, seed 1",
                    "x": "N(0,1) bf16", "l2": f"inputs larger than L2: {args.layers} distinct weight copies "
-                   f"({args.layers * 264.2:.0f} MB) cycled across steps", "parallelism": f"replicas x{N}"},
+                   f"({args.layers * 264.2:.0f} MB) cycled across steps", "parallelism": f"replicas x{N}",
+                   **({"tuning": tuning} if tuning else {})},
         "clocks": clocks.summary(f"{w.name}.timed", "decode.all") if clocks else None,
         "e2e": {"value": N * bytes_step * r["e2e_K"] / e2e_s / 1e12 if r["e2e_K"] else None, "unit": UNIT,
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_K"]},
@@ -783,6 +819,8 @@ def main():
                     help="modelled fixed cost of one collective (tp-sweep)")
     ap.add_argument("--coll-link-gbs", type=float, default=800.0,
                     help="modelled per-GPU link bandwidth of one collective (tp-sweep)")
+    ap.add_argument("--tune", default="",
+                    help="library tuning for the run, e.g. one_launch=2,grid=144 (names of mse.TUNE_*)")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)

@@ -356,9 +356,10 @@ MSE_API int mse_set_tuning(int key, int value);
  * context usable.  Read the result with mse_poll_device_error(). */
 MSE_API mse_status mse_selftest_wait_timeout(uint64_t limit_ns, void *stream);
 
-/* Timing hook for profiling harnesses.  While set, every mlp_swiglu_forward call
- * records ev_begin before its first kernel, ev_mid between the gate_up and the
- * down kernel, and ev_end after the down kernel, on its stream (cudaEvent_t
+/* Timing hook for profiling harnesses.  While set, every mlp_swiglu_forward,
+ * mlp_swiglu_shard_partial and mlp_swiglu_shard_forward call on the tensor-core
+ * path records ev_begin before its first kernel, ev_mid between the gate_up and
+ * the down kernel, and ev_end after the down kernel, on its stream (cudaEvent_t
  * handles passed as void*; all three non-null, or all null to clear).  The
  * records separate the two kernels, so launches made while the hook is set do
  * not overlap them. Process-wide; not meant for concurrent callers. */

@@ -765,11 +765,18 @@ mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int
         return from_cuda(launch_simt_gemm(b, s));
     }
     const int epi = partial_dtype == MSE_F32 ? tc::EPI_F32 : tc::EPI_BF16;
-    if (one_launch_enabled(T))
-        return tc_mlp_one_launch(*d, x, T, H, I, w_gate_up, w_down, j0, width, sw, rank_count, partials, epi, ws, L,
-                                 s);
-    if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s)) != MSE_OK) return st;
-    return tc_down(*d, h, T, H, I, w_down, j0, sw, rank_count, partials, epi, ws, L, s);
+    record(g_ev_begin, s);
+    if (one_launch_enabled(T)) {
+        st = tc_mlp_one_launch(*d, x, T, H, I, w_gate_up, w_down, j0, width, sw, rank_count, partials, epi, ws, L, s);
+        if (st != MSE_OK) return st;
+        record(g_ev_mid, s);
+    } else {
+        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s)) != MSE_OK) return st;
+        record(g_ev_mid, s);
+        if ((st = tc_down(*d, h, T, H, I, w_down, j0, sw, rank_count, partials, epi, ws, L, s)) != MSE_OK) return st;
+    }
+    record(g_ev_end, s);
+    return MSE_OK;
 }
 
 mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, const mse_bf16 *w_gate_up,
@@ -811,10 +818,19 @@ mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int
         return from_cuda(launch_simt_gemm(b, s));
     }
     const int epi = out_dtype == MSE_F32 ? tc::EPI_F32 : tc::EPI_BF16;
-    if (one_launch_enabled(T))
-        return tc_mlp_one_launch(*d, x, T, H, I, w_gate_up, w_down, j0, width, width, 1, out, epi, ws, L, s);
-    if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s)) != MSE_OK) return st;
-    return tc_down(*d, h, T, H, I, w_down, j0, width, 1, out, epi, ws, L, s);
+    record(g_ev_begin, s);
+    if (one_launch_enabled(T)) {
+        if ((st = tc_mlp_one_launch(*d, x, T, H, I, w_gate_up, w_down, j0, width, width, 1, out, epi, ws, L, s)) !=
+            MSE_OK)
+            return st;
+        record(g_ev_mid, s);
+    } else {
+        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s)) != MSE_OK) return st;
+        record(g_ev_mid, s);
+        if ((st = tc_down(*d, h, T, H, I, w_down, j0, width, 1, out, epi, ws, L, s)) != MSE_OK) return st;
+    }
+    record(g_ev_end, s);
+    return MSE_OK;
 }
 
 int mse_shard_sequence_parallel_mlp(int enabled, int use_sequence_parallel, int eligible, int tp_size,

@@ -678,7 +678,7 @@ __device__ __forceinline__ void publish_h_tile(const SwapAbParams &p, int *hflag
 // hflags: publish each completed tile (gate_up passes of the fused layer).
 // PAIR: each CTA finishes its own 128-row half (m-tile 2 m' + rank) of the pair tile;
 // the parts of a split tile are the same halves of the pairs sharing it.
-template <int EPI, bool PAIR = false>
+template <int EPI, bool PAIR = false, bool COOP = false>
 __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring, uint32_t ring_base,
                                 uint32_t ring_bytes, int &gseg, uint32_t &fix_round, uint32_t tmem_base,
                                 bool ring_idle_at_end, int *hflags, int *hcount, volatile int *abort_flag) {
@@ -869,11 +869,13 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
         // Only the last CTA's part can be a non-final segment (the tile is that CTA's
         // first); it hands its part over and goes on.  All parts of the tile take the
         // same decision.
-        // (compiled into the merged-projection kernel only: its tiles are split about nine
-        // ways; the MLP kernels' tiles are split two to four ways, where the CTA arriving
-        // last finishing alone measured faster)
+        // (compiled into the merged-projection kernel, whose tiles are split about nine
+        // ways, and into the COOP kernels the host picks when some tile is split at least
+        // coop_finish ways, e.g. one shard's narrow gate_up slice; the replicated layer's
+        // tiles are split two to four ways, where the CTA arriving last finishing alone
+        // measured faster and even the untaken branch cost time)
         int n_fin = 0;   // parts that finish jointly; 0: the CTA arriving last finishes alone
-        if constexpr (EPI == EPI_MERGED) {
+        if constexpr (EPI == EPI_MERGED || COOP) {
             if (ring_idle_at_end && p.coop_finish > 0 && nseg >= p.coop_finish && nseg <= 128) {
                 n_fin = nseg - (sk.begin(c_last + 1) <= (tile + 1) * kbp ? 0 : 1);
                 if (ring_bytes / ((uint32_t)((bn + n_fin - 1) / n_fin) * 512u) < 2) n_fin = 0;
@@ -1065,7 +1067,7 @@ __device__ __forceinline__ void swapab_teardown(Ctrl *ctl, int S, int issued, ui
 // One stream-K pass: out = epilogue(A . B^T) over p's (group, m-tile, k-block) units.
 // PAIR: clusters of two CTAs take (group, pair of m-tiles, k-block) units; one M = 256
 // MMA per k-block covers both CTAs' weight rows, each CTA holding half of the tokens.
-template <int EPI, bool PAIR>
+template <int EPI, bool PAIR, bool COOP = false>
 __global__ void __launch_bounds__(kSwapAbThreads, 1)
     swapab_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const SwapAbParams p) {
@@ -1100,8 +1102,8 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
         pdl_wait();
         int gseg = 0;
         uint32_t fix_round = 0;
-        (void)swapab_epilogue<EPI, PAIR>(p, ctl, ring, base, (uint32_t)S * sm.stage_bytes, gseg, fix_round,
-                                         tmem_base, true, nullptr, nullptr, abort_flag);
+        (void)swapab_epilogue<EPI, PAIR, COOP>(p, ctl, ring, base, (uint32_t)S * sm.stage_bytes, gseg, fix_round,
+                                               tmem_base, true, nullptr, nullptr, abort_flag);
     }
     swapab_teardown<PAIR>(ctl, S, issued, tmem_base, p.tmem_cols, p.wait_limit_ns, clustered);
 }
@@ -1643,7 +1645,7 @@ __global__ void __launch_bounds__(kStdThreads, 1)
 }
 
 // Opt the kernel into the largest dynamic shared memory once per device.
-constexpr int kSmemAttrSlots = 32;   // one per kernel instantiation (slots 0..17 in use)
+constexpr int kSmemAttrSlots = 32;   // one per kernel instantiation (slots 0..20 in use)
 
 template <typename Kern>
 cudaError_t ensure_smem_attr(Kern kern, int slot) {
@@ -1673,6 +1675,18 @@ int swapab_stages_for(int bn, int kbs) {
 }
 int std_stages() { return 4; }
 
+// Largest number of CTAs any tile of a single-CTA stream-K launch is split between.
+static int swapab_max_parts(const SwapAbParams &p, int grid) {
+    const int64_t U = p.total_units, kbp = p.kb_per_tile;
+    if (U <= 0 || kbp <= 0 || grid <= 0) return 1;
+    const int64_t n_tiles = U / kbp;
+    auto owner = [&](int64_t u) { return ((u + 1) * grid - 1) / U; };
+    int worst = 1;
+    for (int64_t t = 0; t < n_tiles && t < 65536; ++t)
+        worst = std::max(worst, (int)(owner(t * kbp + kbp - 1) - owner(t * kbp) + 1));
+    return worst;
+}
+
 cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
                           bool pdl, bool pair, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -1701,6 +1715,18 @@ cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb,
     e = ensure_smem_attr(swapab_kernel<E, PR>, SLOT);                   \
     if (e != cudaSuccess) return e;                                     \
     return cudaLaunchKernelEx(&cfg, swapab_kernel<E, PR>, ta, tb, p);
+#define MSE_LAUNCH_SWAPAB_COOP(E, SLOT)                                 \
+    e = ensure_smem_attr(swapab_kernel<E, false, true>, SLOT);          \
+    if (e != cudaSuccess) return e;                                     \
+    return cudaLaunchKernelEx(&cfg, swapab_kernel<E, false, true>, ta, tb, p);
+    if (!pair && epi != EPI_MERGED && !p.cluster_finish && swapab_max_parts(p, grid) >= p.coop_finish &&
+        p.coop_finish > 0) {
+        switch (epi) {
+            case EPI_SWIGLU: MSE_LAUNCH_SWAPAB_COOP(EPI_SWIGLU, 18)
+            case EPI_BF16: MSE_LAUNCH_SWAPAB_COOP(EPI_BF16, 19)
+            default: MSE_LAUNCH_SWAPAB_COOP(EPI_F32, 20)
+        }
+    }
     if (!pair) {
         switch (epi) {
             case EPI_SWIGLU: MSE_LAUNCH_SWAPAB(EPI_SWIGLU, false, 0)
@@ -1716,6 +1742,7 @@ cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb,
         default: MSE_LAUNCH_SWAPAB(EPI_MERGED, true, 17)
     }
 #undef MSE_LAUNCH_SWAPAB
+#undef MSE_LAUNCH_SWAPAB_COOP
 }
 
 // Clusters of three single CTAs of the swap-AB kernel that can be resident at once.

@@ -136,6 +136,56 @@ def test_shard_forward_unaligned_shape_takes_generic_path():
     assert_close(bits_f64(to_bits(out)), bits_f64(ref), "generic")
 
 
+# ------------------------------------------------------------------ joint finish of narrow slices
+@contextlib.contextmanager
+def coop(threshold: int):
+    old = mse.set_tuning(mse.TUNE_COOP_FINISH, threshold)
+    assert old >= 0
+    try:
+        yield
+    finally:
+        mse.set_tuning(mse.TUNE_COOP_FINISH, old)
+
+
+@pytest.mark.parametrize("T", [1, 16, 33, 64, 130, 256])
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.F32])
+def test_one_shard_many_way_split_joint_finish(T, dtype):
+    # One shard of a narrow slice: two gate_up tiles of 64 columns over 64 k-blocks each,
+    # so every tile is split between dozens of CTAs and the kernels that finish such
+    # tiles jointly run (default threshold) or not (threshold 0).  Both sum the parts in
+    # the same order: results must agree bit for bit, and with the oracle.
+    H, I, tp, rank = 4096, 1024, 8, 5
+    x, wgu, wd = case(T, H, I, 9400 + T)
+    td = torch.bfloat16 if dtype == oracle.BF16 else torch.float32
+    dx, dgu, dwd = to_dev(x), to_dev(wgu), to_dev(wd)
+    with coop(6):
+        a = mse.mlp_swiglu_shard_partial(dx, dgu, dwd, tp, rank_first=rank, rank_count=1, partial_dtype=td)
+        ga = mse.mlp_swiglu_shard_forward(dx, dgu, dwd, tp, rank_first=rank, rank_count=1, out_dtype=td)
+    with coop(0):
+        b = mse.mlp_swiglu_shard_partial(dx, dgu, dwd, tp, rank_first=rank, rank_count=1, partial_dtype=td)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b), "joint finish differs from the finish by the last CTA"
+    assert torch.equal(a[0], ga)
+    _, pr = oracle.shard_partial(x, wgu, wd, tp, rank, dtype)
+    assert_close(got_f64(a[0], dtype), ref_f64(pr, dtype), f"T={T}")
+
+
+@pytest.mark.parametrize("tp", [4, 16])
+def test_joint_finish_h_matches_oracle(tp):
+    # the SiLU*mul epilogue finished in token slices: h of the shard's columns
+    T, H, I = 48, 2048, 1024
+    x, wgu, wd = case(T, H, I, 9450 + tp)
+    ws = mse.new_mlp_workspace(T, H, I)
+    s = I // tp
+    for rank in (0, tp - 1):
+        mse.mlp_swiglu_shard_partial(to_dev(x), to_dev(wgu), to_dev(wd), tp, rank_first=rank, rank_count=1,
+                                     workspace=ws)
+        torch.cuda.synchronize()
+        h = ws[: T * I * 2].view(torch.int16).view(T, I).cpu().numpy().view(np.uint16)
+        h_ref = oracle.swiglu_hidden(x, wgu, I, rank * s, (rank + 1) * s)
+        assert_close(bits_f64(h[:, rank * s:(rank + 1) * s]), bits_f64(h_ref), f"h tp{tp} rank {rank}")
+
+
 # ------------------------------------------------------------------ the TP8 workload
 def test_tp8_t128_summed_in_the_down_projection():
     # 128 gathered tokens, 8 shards of 768 intermediate columns: the whole group's sum
