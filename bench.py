@@ -431,12 +431,16 @@ class RankShapes:
             self.ws[T] = self.mse.new_mlp_workspace(T, self.H, self.I)
         return self.ws[T]
 
-    def _time(self, step, n_steps, K, Wm, bad):
-        """Device seconds per step: steps 0..n_steps-1 captured once, replayed."""
+    def _time(self, step, n_steps, K, Wm, bad, graph=True):
+        """Device seconds per step: steps 0..n_steps-1 captured once, replayed (or, with
+        graph=False, K eager steps)."""
         import torch
         for i in range(max(Wm, n_steps)):      # eager warm-up (also sets kernel attributes)
             step(i)
         torch.cuda.synchronize()
+        if not graph:
+            K = K or 200
+            return time_loop(step, K, torch.cuda.current_stream()) / K
         side = torch.cuda.Stream()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=side):
@@ -455,7 +459,7 @@ class RankShapes:
         t = time_loop(lambda i: g.replay(), K, torch.cuda.current_stream())
         return t / (K * n_steps)
 
-    def rank_partial(self, T, tp, K=None, Wm=5):
+    def rank_partial(self, T, tp, K=None, Wm=5, graph=True):
         """One rank's partial [T x H] bf16 over its 1/tp of the weights (T gathered tokens)."""
         import torch
         L = self.mse.lib()
@@ -471,7 +475,7 @@ class RankShapes:
                                                  self.wds[c].data_ptr(), tp, r, 1, out.data_ptr(), 0, out.numel(),
                                                  ws.data_ptr(), ws.numel(), sp)
 
-        t = self._time(step, tp * self.copies, K, Wm, bad)
+        t = self._time(step, tp * self.copies, K, Wm, bad, graph)
         if bad[0]:
             raise RuntimeError("rank partial error status")
         return t
@@ -509,6 +513,28 @@ def apply_tuning(spec: str) -> dict:
             raise ValueError(f"tuning {item} rejected")
         done[name.strip().lower()] = int(value)
     return done
+
+
+def rank_bench(args):
+    """One rank's partial alone (first of --sweep-tokens / --sweep-tp), eager launches:
+    the small command that profiles of the per-rank kernels are taken on."""
+    import torch
+    torch.cuda.set_device(0)
+    from moe_shared_expert_gb300 import _build
+    _build.build()
+    import moe_shared_expert_gb300 as mse
+    mse.lib()
+    tuning = apply_tuning(args.tune)
+    T = int(args.sweep_tokens.split(",")[0])
+    tp = int(args.sweep_tp.split(",")[0])
+    rs = RankShapes(T)
+    t = rs.rank_partial(T, tp, K=args.steps, Wm=args.warmup, graph=False)
+    b = mlp_bytes(T, rs.H, rs.I // tp)
+    print(json.dumps({"metric": "one rank's shard partial", "value": t * 1e6, "unit": "us", "n_gpus": 1,
+                      "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": f"rank_partial_tp{tp}_t{T}", "T": T, "tp": tp, "slice": rs.I // tp,
+                                 "timing": "eager launches", "tuning": tuning},
+                      "tbps_algorithmic": b / t / 1e12, "gpu_launches": 2 * args.steps}), flush=True)
 
 
 def tp_sweep(args):
@@ -812,7 +838,7 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--aux-steps", type=int, default=2000)
     ap.add_argument("--decode-only", action="store_true", help="same as --only decode")
-    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill", "tp-sweep"])
+    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill", "tp-sweep", "rank"])
     ap.add_argument("--sweep-tokens", default="16,32,64,128,256,512,1024,2048")
     ap.add_argument("--sweep-tp", default="4,8,16")
     ap.add_argument("--coll-alpha-us", type=float, default=10.0,
@@ -835,6 +861,8 @@ def main():
         reference_arm(args)
     elif args.only == "tp-sweep":
         tp_sweep(args)
+    elif args.only == "rank":
+        rank_bench(args)
     else:
         gpu_arm(args)
 
