@@ -355,7 +355,9 @@ struct SwapAbShape {
     int grid;
     int b_box_rows;   // token rows of one B copy (each CTA's half for pairs)
 };
-SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups, int kbp, bool down = false) {
+// narrow: an MLP launch whose CTAs may be fewer than the SMs when its work is small (see below).
+SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups, int kbp, bool down = false,
+                         bool narrow = false) {
     SwapAbShape r;
     const int pmin = g_tune_pair_min_t.load();
     if (pmin > 0 && T >= pmin) {
@@ -380,6 +382,15 @@ SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups,
     r.p.n_mtiles = n_real;
     r.p.n_mtiles_real = n_real;
     r.grid = swapab_grid(d, r.p.total_units, kbp, down ? g_tune_grid_down.load() : 0);
+    // Small work (one shard's narrow slice): at least 16 k-blocks per CTA, but never fewer
+    // CTAs than half of the SMs.  Such launches are bound by their split-K tails and
+    // stragglers, not by bytes, and fewer CTAs split each tile into fewer parts (one rank's
+    // TP8 / TP16 step measured 1-3 us faster on 76-120 CTAs than on 152).  Not applied when
+    // a grid is set through the tuning keys.
+    if (narrow && g_tune_grid.load() == 0 && (!down || g_tune_grid_down.load() == 0)) {
+        const int cap = std::max((r.p.total_units + 15) / 16, std::min(d.sm_count, tc::kMaxGrid) / 2);
+        if (cap < r.grid) r.grid = cap;
+    }
     r.b_box_rows = r.p.bn;
     // clusters of three when three CTAs cover two tiles exactly (every tile in two parts)
     if (g_tune_cluster_finish.load() != 0 && r.grid % 3 == 0 &&
@@ -423,7 +434,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
     mse_status st;
     if (T <= kSwapAbMaxT) {
         const int kbp = (int)(H / 64);
-        SwapAbShape sh = swapab_shape(d, T, (int)(width / 64), 1, kbp);
+        SwapAbShape sh = swapab_shape(d, T, (int)(width / 64), 1, kbp, false, true);
         tc::SwapAbParams &p = sh.p;
         if ((st = map_2d(&ta, w_gate_up, 2 * I, H, H, 64)) != MSE_OK) return st;
         if ((st = map_2d(&tb, x, T, H, H, sh.b_box_rows)) != MSE_OK) return st;
@@ -485,7 +496,7 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
     mse_status st;
     if (T <= kSwapAbMaxT) {
         const int kbp = (int)(s_width / 64);
-        SwapAbShape sh = swapab_shape(d, T, (int)((H + 127) / 128), groups, kbp, true);
+        SwapAbShape sh = swapab_shape(d, T, (int)((H + 127) / 128), groups, kbp, true, true);
         tc::SwapAbParams &p = sh.p;
         if ((st = map_2d(&ta, w_down, H, I, I, 128)) != MSE_OK) return st;
         if ((st = map_2d(&tb, h, T, I, I, sh.b_box_rows)) != MSE_OK) return st;
