@@ -537,6 +537,25 @@ def rank_bench(args):
                       "tbps_algorithmic": b / t / 1e12, "gpu_launches": 2 * args.steps}), flush=True)
 
 
+def collectives_model_s(T, H, tp, alpha_s, beta_Bps):
+    """Modelled time of the block's two collectives (all-gather of the tokens, reduce-scatter
+    of the bf16 partials): each alpha + (tp-1)/tp * T*H*2 bytes / beta."""
+    return 2 * (alpha_s + (tp - 1) / tp * T * H * 2 / beta_Bps)
+
+
+def crossovers(points, tps):
+    """First group size T at which the replicated block is at least as fast, kernels only and
+    with the modelled collectives (None: sharding faster at every T measured)."""
+    out = {}
+    for tp in tps:
+        pts = sorted((p for p in points if p["tp"] == tp), key=lambda p: p["T"])
+        k = [p["T"] for p in pts if p["sharded_kernel_us"] >= p["replicated_us"]]
+        c = [p["T"] for p in pts if p["sharded_with_collectives_us"] >= p["replicated_us"]]
+        out[str(tp)] = {"kernel_only_first_T_replicated_wins": min(k) if k else None,
+                        "with_modelled_collectives_first_T_replicated_wins": min(c) if c else None}
+    return out
+
+
 def tp_sweep(args):
     """Per-GPU time of the replicated and the TP-sharded MLP block under sequence
     parallelism, over the group's token count T and tp.  Replicated: each rank runs the
@@ -563,17 +582,11 @@ def tp_sweep(args):
                 continue
             t_rep = rs.replicated(T // tp)
             t_shard = rs.rank_partial(T, tp)
-            coll = 2 * (alpha + (tp - 1) / tp * T * H * 2 / beta)
+            coll = collectives_model_s(T, H, tp, alpha, beta)
             points.append({"tp": tp, "T": T, "replicated_us": t_rep * 1e6, "sharded_kernel_us": t_shard * 1e6,
                            "sharded_with_collectives_us": (t_shard + coll) * 1e6,
                            "collectives_model_us": coll * 1e6})
-    cross = {}
-    for tp in tps:
-        pts = [p for p in points if p["tp"] == tp]
-        k = [p["T"] for p in pts if p["sharded_kernel_us"] >= p["replicated_us"]]
-        c = [p["T"] for p in pts if p["sharded_with_collectives_us"] >= p["replicated_us"]]
-        cross[str(tp)] = {"kernel_only_first_T_replicated_wins": min(k) if k else None,
-                          "with_modelled_collectives_first_T_replicated_wins": min(c) if c else None}
+    cross = crossovers(points, tps)
     line = {"metric": "per-GPU µs of the MLP block: replicated vs TP-sharded under sequence parallelism",
             "unit": "us", "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "tp_crossover_sweep", "H": H, "I": I, "tokens": Ts, "tp": tps,
