@@ -305,7 +305,11 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         is fetched in runs of 128 x value contiguous bytes (1..4, default 2)
  *   MSE_TUNE_STAGES       shared-memory pipeline depth (0 = as many as fit, default)
  *   MSE_TUNE_CACHE_HINTS  1 = weights evict-first / tokens evict-last in L2 (default), 0 = none
- *   MSE_TUNE_GRID         CTAs of the stream-K grid (0 = one per SM, default; at most 160)
+ *   MSE_TUNE_GRID         CTAs of the stream-K grid (at most 160).  0 (default) = chosen per shape:
+ *                         among 90-100% of the SMs the count that splits tiles into the fewest
+ *                         parts when that is at most three, else one per SM; MLP launches with
+ *                         little work (one shard's narrow slice) then at most one CTA per 16
+ *                         k-blocks, but not fewer than half of the SMs
  *   MSE_TUNE_SPIN_WAIT    1 = pipeline waits poll (mbarrier.test_wait) instead of suspending
  *   MSE_TUNE_ONE_LAUNCH   decode token counts (T <= 256): 0 = gate_up + SiluAndMul and the down
  *                         projection as two launches (default: with programmatic dependent
@@ -317,12 +321,14 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         starts while the previous one in the stream drains and fetches its
  *                         first weight tiles before waiting for it (default); 0 = plain
  *                         stream order
- *   MSE_TUNE_COOP_FINISH  merged projection at decode token counts: a tile whose reduction is
- *                         split between at least this many CTAs (0..128; 0 = never) is
- *                         finished jointly by the CTAs for which it is the final segment: each
- *                         waits (bounded) for all parts, then sums and writes one slice of the
- *                         tile's token columns.  Other split tiles are finished by the CTA
- *                         arriving last.  Default 6
+ *   MSE_TUNE_COOP_FINISH  decode token counts: a tile whose reduction is split between at least
+ *                         this many CTAs (0..128; 0 = never) is finished jointly by the CTAs for
+ *                         which it is the final segment: each waits (bounded) for all parts,
+ *                         then sums and writes one slice of the tile's token columns.  Other
+ *                         split tiles are finished by the CTA arriving last.  Applies to the
+ *                         merged projection and to MLP launches with some tile split this many
+ *                         ways (one shard's narrow gate_up slice); same results bit for bit.
+ *                         Default 6
  *   MSE_TUNE_PAIR_MIN_T   token counts from which the decode-size kernels run as CTA pairs: one
  *                         256-row weight tile per pair (one M = 256 MMA over both CTAs), each
  *                         CTA holding half of the token rows, so that more weight bytes are in
