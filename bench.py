@@ -243,6 +243,29 @@ def time_loop(fn, K, stream):
     return s.elapsed_time(e) / 1e3   # seconds
 
 
+def time_chunks(fn, K, stream, n_chunks=20):
+    """time_loop in n_chunks consecutive chunks (an event between chunks, none between the
+    steps of a chunk): (total seconds, seconds per step of each chunk)."""
+    import torch
+    n_chunks = max(1, min(n_chunks, K))
+    bounds = [K * c // n_chunks for c in range(n_chunks + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_chunks + 1)]
+    evs[0].record(stream)
+    for c in range(n_chunks):
+        for i in range(bounds[c], bounds[c + 1]):
+            fn(i)
+        evs[c + 1].record(stream)
+    evs[-1].synchronize()
+    total = evs[0].elapsed_time(evs[-1]) / 1e3
+    per = [evs[c].elapsed_time(evs[c + 1]) / 1e3 / (bounds[c + 1] - bounds[c]) for c in range(n_chunks)]
+    return total, per
+
+
+def percentiles(v, qs=(10, 50, 90)):
+    s = sorted(v)
+    return [s[min(len(s) - 1, max(0, int(round(q / 100 * (len(s) - 1)))))] for q in qs]
+
+
 def one_launch_active() -> bool:
     import moe_shared_expert_gb300 as mse
     old = mse.set_tuning(mse.TUNE_ONE_LAUNCH, 1)
@@ -280,7 +303,7 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    dev_s = time_loop(step, K, stream)
+    dev_s, chunk_s = time_chunks(step, K, stream)
     torch.cuda.synchronize()
     dist.barrier()
     t1 = time.time()
@@ -330,7 +353,7 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
         raise RuntimeError("error status in e2e loop")
     del gus, wds
     torch.cuda.empty_cache()
-    return {"dev_s": dev_s, "K": K, "e2e_s": e2e_s, "e2e_K": n_e2e,
+    return {"dev_s": dev_s, "K": K, "e2e_s": e2e_s, "e2e_K": n_e2e, "chunk_s": chunk_s,
             "gate_up_ms": statistics.mean(gate_up_ms), "down_ms": statistics.mean(down_ms),
             "layer_ms": statistics.mean(layer_ms),
             "gate_up_ms_median": statistics.median(gate_up_ms), "h2d": T * H * 2, "d2h": T * H * 2}
@@ -773,6 +796,8 @@ def gpu_arm(args):
                      "kernel": k_name, "kernel_ms": k_ms, "algorithmic_bytes": k_bytes,
                      "peak_kind": f"HBM copy ({peaks['source']})"},
         "step_frac_of_hbm": bytes_step / (dev_s / K) / 1e9 / peaks["hbm_gbs"],
+        "us_per_layer_p10_p50_p90": [v * 1e6 for v in percentiles(r["chunk_s"])],
+        "us_per_layer_spread": f"per-step time of {len(r['chunk_s'])} consecutive chunks of the timed loop",
     }
     if launches == 2 * K:
         line["down_kernel_ms"] = r["down_ms"]

@@ -69,3 +69,9 @@ def test_apply_tuning_parses_sets_and_rejects():
     finally:
         mse.set_tuning(mse.TUNE_GRID, old)
         mse.set_tuning(mse.TUNE_ONE_LAUNCH, 0)
+
+
+def test_percentiles_nearest_rank():
+    assert bench.percentiles([5, 1, 3, 2, 4]) == [1, 3, 5]
+    assert bench.percentiles([7.0]) == [7.0, 7.0, 7.0]
+    assert bench.percentiles(list(range(21))) == [2, 10, 18]
