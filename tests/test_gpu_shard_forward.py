@@ -170,6 +170,32 @@ def test_one_shard_many_way_split_joint_finish(T, dtype):
     assert_close(got_f64(a[0], dtype), ref_f64(pr, dtype), f"T={T}")
 
 
+@pytest.mark.parametrize("T", [16, 64, 130])
+def test_down_projection_joint_finish_bf16_and_f32(T):
+    # Two 128-row down tiles over long reductions (64 and 32 k-blocks): each tile is split
+    # between dozens of CTAs, so the down kernels with the joint finish write the bf16
+    # output and the fp32 partials in token slices.  Bit-identical to the finish by the
+    # last CTA (threshold 0), and within tolerance of the oracle.
+    H, I = 256, 4096
+    x, wgu, wd = case(T, H, I, 9460 + T)
+    dx, dgu, dwd = to_dev(x), to_dev(wgu), to_dev(wd)
+    with coop(6):
+        y = mse.mlp_swiglu_forward(dx, dgu, dwd)
+        p32 = mse.mlp_swiglu_shard_partial(dx, dgu, dwd, 2, rank_first=1, rank_count=1,
+                                           partial_dtype=torch.float32)
+    with coop(0):
+        y0 = mse.mlp_swiglu_forward(dx, dgu, dwd)
+        p32_0 = mse.mlp_swiglu_shard_partial(dx, dgu, dwd, 2, rank_first=1, rank_count=1,
+                                             partial_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y0)
+    assert torch.equal(p32, p32_0)
+    y_ref, _, _ = oracle.mlp_forward(x, wgu, wd)
+    assert_close(bits_f64(to_bits(y)), bits_f64(y_ref), f"y T={T}")
+    _, pr = oracle.shard_partial(x, wgu, wd, 2, 1, oracle.F32)
+    assert_close(p32[0].cpu().numpy().astype(np.float64), pr.astype(np.float64), f"fp32 partial T={T}")
+
+
 @pytest.mark.parametrize("tp", [4, 16])
 def test_joint_finish_h_matches_oracle(tp):
     # the SiLU*mul epilogue finished in token slices: h of the shard's columns
