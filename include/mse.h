@@ -110,6 +110,19 @@ MSE_API size_t mlp_swiglu_workspace_bytes(int64_t T, int64_t H, int64_t I);
  * to T with the same q_dim + kv_dim.  Returns 0 on invalid arguments. */
 MSE_API size_t merged_proj_workspace_bytes(int64_t T, int64_t H, int64_t q_dim, int64_t kv_dim);
 
+/* Byte range [*offset, *offset + *bytes) of the sync words (tile counters and
+ * flags) inside a workspace of workspace_bytes for calls with at most T tokens
+ * and this H and I.  Only this range must be zero before a call: after
+ * MSE_ERR_TIMEOUT, zeroing it is enough to reuse the workspace.  Returns
+ * MSE_ERR_WORKSPACE when workspace_bytes is below the call's minimal need,
+ * MSE_ERR_INVALID_ARG on invalid sizes or null pointers.  Host only. */
+MSE_API mse_status mlp_swiglu_workspace_sync_range(int64_t T, int64_t H, int64_t I, size_t workspace_bytes,
+                                                   size_t *offset, size_t *bytes);
+
+/* The same for a merged-projection workspace (the tile counters). */
+MSE_API mse_status merged_proj_workspace_sync_range(int64_t T, int64_t H, int64_t q_dim, int64_t kv_dim,
+                                                    size_t workspace_bytes, size_t *offset, size_t *bytes);
+
 /* ---------------------------------------------------------------------------
  * Replicated SwiGLU MLP ("[Kimi-K3] Add option to shard the shared expert
  * instead of replicating", section "Change": gate_up projection, SiluAndMul,

@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
             sig = {
                 "mlp_swiglu_workspace_bytes": (sz, [i64, i64, i64]),
                 "merged_proj_workspace_bytes": (sz, [i64, i64, i64, i64]),
+                "mlp_swiglu_workspace_sync_range": (ci, [i64, i64, i64, sz, P, P]),
+                "merged_proj_workspace_sync_range": (ci, [i64, i64, i64, i64, sz, P, P]),
                 "mlp_swiglu_forward": (ci, [P, i64, i64, i64, P, P, P, i64, P, sz, P]),
                 "mlp_swiglu_shard_partial": (ci, [P, i64, i64, i64, P, P, ci, ci, ci, P, ci, i64, P, sz, P]),
                 "mlp_swiglu_shard_forward": (ci, [P, i64, i64, i64, P, P, ci, ci, ci, P, ci, i64, P, sz, P]),
@@ -160,6 +162,23 @@ def mlp_swiglu_workspace_bytes(T: int, H: int, I: int) -> int:
 
 def merged_proj_workspace_bytes(T: int, H: int, q_dim: int, kv_dim: int) -> int:
     return int(lib().merged_proj_workspace_bytes(T, H, q_dim, kv_dim))
+
+
+def mlp_swiglu_workspace_sync_range(T: int, H: int, I: int, workspace_bytes: int) -> tuple[int, int]:
+    """(offset, bytes) of the sync words inside an MLP workspace of workspace_bytes."""
+    off, n = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("mlp_swiglu_workspace_sync_range",
+           lib().mlp_swiglu_workspace_sync_range(T, H, I, workspace_bytes, ctypes.byref(off), ctypes.byref(n)))
+    return int(off.value), int(n.value)
+
+
+def merged_proj_workspace_sync_range(T: int, H: int, q_dim: int, kv_dim: int, workspace_bytes: int) -> tuple[int, int]:
+    """(offset, bytes) of the tile counters inside a merged-projection workspace."""
+    off, n = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("merged_proj_workspace_sync_range",
+           lib().merged_proj_workspace_sync_range(T, H, q_dim, kv_dim, workspace_bytes, ctypes.byref(off),
+                                                  ctypes.byref(n)))
+    return int(off.value), int(n.value)
 
 
 def new_mlp_workspace(T: int, H: int, I: int, device="cuda"):

@@ -692,6 +692,27 @@ size_t merged_proj_workspace_bytes(int64_t T, int64_t H, int64_t q_dim, int64_t 
     return n > m ? n : m;
 }
 
+mse_status mlp_swiglu_workspace_sync_range(int64_t T, int64_t H, int64_t I, size_t workspace_bytes, size_t *offset,
+                                          size_t *bytes) {
+    if (T <= 0 || H <= 0 || I <= 0 || !offset || !bytes) return MSE_ERR_INVALID_ARG;
+    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes);
+    if (workspace_bytes < L.total) return MSE_ERR_WORKSPACE;
+    *offset = L.sync_off;
+    *bytes = L.sync_bytes;
+    return MSE_OK;
+}
+
+mse_status merged_proj_workspace_sync_range(int64_t T, int64_t H, int64_t q_dim, int64_t kv_dim,
+                                           size_t workspace_bytes, size_t *offset, size_t *bytes) {
+    if (T <= 0 || H <= 0 || q_dim < 0 || kv_dim < 0 || q_dim + kv_dim <= 0 || !offset || !bytes)
+        return MSE_ERR_INVALID_ARG;
+    const MergedWs L = merged_ws_place(T, q_dim + kv_dim, workspace_bytes);
+    if (workspace_bytes < L.total) return MSE_ERR_WORKSPACE;
+    *offset = L.cnt_off;
+    *bytes = L.cnt_bytes;
+    return MSE_OK;
+}
+
 mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, const mse_bf16 *w_gate_up,
                               const mse_bf16 *w_down, mse_bf16 *y, int64_t y_capacity, void *workspace,
                               size_t workspace_bytes, void *stream) {

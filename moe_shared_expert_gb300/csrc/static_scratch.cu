@@ -25,6 +25,8 @@ constexpr size_t kStaticScratchBytes = (size_t)32 << 20;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_addr[kMaxDevices];   // device address of the array, per device
+bool g_checked[kMaxDevices];         // compute capability read for this device
+bool g_supported[kMaxDevices];       // compute capability 10.3 (the only code this library holds)
 
 }  // namespace
 
@@ -48,8 +50,21 @@ MSE_API mse_status mlp_swiglu_forward_static_scratch(const mse_bf16 *x, int64_t 
     void *scratch = nullptr;
     {
         // Set-up, once per device, with that device current: the array's name is
-        // only a host-side stand-in, so its device address is looked up here.
+        // only a host-side stand-in, so its device address is looked up here.  The
+        // device is checked first: on a device without sm_103a code the lookup would
+        // fail (or load the module) instead of reporting the unsupported device.
         std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_checked[dev]) {
+            int major = 0, minor = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+                cudaGetLastError();
+                return MSE_ERR_CUDA;
+            }
+            g_supported[dev] = major == 10 && minor == 3;
+            g_checked[dev] = true;
+        }
+        if (!g_supported[dev]) return MSE_ERR_UNSUPPORTED_DEVICE;
         if (!g_scratch_addr[dev]) {
             void *p = nullptr;
             if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {

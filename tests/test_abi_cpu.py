@@ -66,6 +66,28 @@ def test_workspace_size_covers_every_smaller_token_count(L):
     assert all(a <= b for a, b in zip(m, m[1:]))
 
 
+def test_sync_range_sits_at_the_end_of_the_buffer(L):
+    # the sync words are the workspace's last, 256-aligned bytes whatever T is, and their
+    # size depends on H and I only: a buffer sized for T serves every smaller call
+    for H, I in [(7168, 6144), (384, 320), (2048, 1536)]:
+        n = L.mlp_swiglu_workspace_bytes(256, H, I)
+        ranges = set()
+        for T in (1, 16, 64, 65, 200, 256):
+            off, b = mse.mlp_swiglu_workspace_sync_range(T, H, I, n)
+            assert off % 256 == 0 and b > 0 and off + b <= n and n - (off + b) < 256
+            # room for the counters of every gate_up tile, every down tile and every h flag
+            assert b >= 4 * ((I // 64) + (I // 64) * (H // 128) + (I // 64) + 3)
+            ranges.add((off, b))
+        assert len(ranges) == 1, (H, I, ranges)
+    # a buffer below the call's minimal need is rejected
+    n = L.mlp_swiglu_workspace_bytes(64, 7168, 6144)
+    with pytest.raises(mse.MSEError):
+        mse.mlp_swiglu_workspace_sync_range(64, 7168, 6144, n - 256)
+    n = L.merged_proj_workspace_bytes(128, 7168, 1536, 576)
+    off, b = mse.merged_proj_workspace_sync_range(128, 7168, 1536, 576, n)
+    assert off + b == n and b >= 4 * 17
+
+
 # Fake, never-dereferenced addresses: every call below fails validation before any
 # CUDA call.  As a second guard they are not run where a CUDA device is visible.
 FAKE = 0x10000
