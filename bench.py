@@ -44,6 +44,13 @@ UNIT = "TB/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+# GB300 vendor figures, reported beside the measured denominators: HBM3e 7.9 TB/s,
+# dense bf16 2.25 PFLOP/s; and the tensor pipe's own rate, 152 SMs x 8192 dense bf16
+# FLOP per SM per clock, scaled by the SM clock sampled during the run.
+SPEC_HBM_GBS = 7900.0
+SPEC_BF16_TFLOPS = 2250.0
+N_SMS = 152
+BF16_FLOP_PER_SM_CLK = 8192
 
 
 # ------------------------------------------------------------------------------------------
@@ -231,10 +238,27 @@ def weight_copies(wgu0, wd0, n):
     return gus, wds
 
 
-def time_loop(fn, K, stream):
+# A device-side spin enqueued just before the start event, so that the host has queued
+# the first steps before the timed region begins (the start event then records when
+# the spin ends and the first step follows at once).  It is outside the timed region.
+HOLD_CYCLES = 400_000   # about 0.2 ms at 2 GHz
+
+
+def hold_device(stream):
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HOLD_CYCLES)
+
+
+def time_loop(fn, K, stream, hold=True):
+    """Device seconds of K steps: one event pair around all of them, no event between
+    steps (an event between two kernels would cut the programmatic-dependent-launch
+    overlap of consecutive layers)."""
     import torch
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
+    if hold:
+        hold_device(stream)
     s.record(stream)
     for i in range(K):
         fn(i)
@@ -245,11 +269,13 @@ def time_loop(fn, K, stream):
 
 def time_chunks(fn, K, stream, n_chunks=20):
     """time_loop in n_chunks consecutive chunks (an event between chunks, none between the
-    steps of a chunk): (total seconds, seconds per step of each chunk)."""
+    steps of a chunk): (total seconds, seconds per step of each chunk).  Used only for the
+    spread of per-step times, in a pass of its own with at least 50 steps per chunk."""
     import torch
     n_chunks = max(1, min(n_chunks, K))
     bounds = [K * c // n_chunks for c in range(n_chunks + 1)]
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_chunks + 1)]
+    hold_device(stream)
     evs[0].record(stream)
     for c in range(n_chunks):
         for i in range(bounds[c], bounds[c + 1]):
@@ -273,7 +299,7 @@ def one_launch_active() -> bool:
     return old == 1
 
 
-def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=None):
+def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=None, spread_steps=2000):
     """Replicated shared-expert layer: returns dict with device time, e2e time and phase times."""
     import torch
     import moe_shared_expert_gb300 as mse
@@ -303,7 +329,7 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    dev_s, chunk_s = time_chunks(step, K, stream)
+    dev_s = time_loop(step, K, stream)
     torch.cuda.synchronize()
     dist.barrier()
     t1 = time.time()
@@ -314,6 +340,11 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
     st = mse.poll_device_error()
     if st:
         raise RuntimeError(f"device error {mse.STATUS.get(st)}")
+
+    # spread of the per-step time: a separate pass of 20 chunks of >= 50 steps each
+    # (the headline above has no event inside its loop)
+    n_spread = 20 * max(50, spread_steps // 20) if spread_steps else 0
+    chunk_s = time_chunks(step, n_spread, stream)[1] if n_spread else []
 
     # per-kernel durations: CUDA events recorded by the library between its two kernels
     n_ph = min(phase_steps, K)
@@ -347,13 +378,20 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
         e2e_step(i)
     torch.cuda.synchronize()
     dist.barrier()
-    e2e_s = time_loop(e2e_step, n_e2e, stream)
-    torch.cuda.synchronize()
+    e2e_s, e2e_host_s = 0.0, 0.0
+    if n_e2e:
+        # host wall clock from the first call to the final synchronize (host launch and
+        # synchronisation costs included), and the stream's own events beside it
+        torch.cuda.synchronize()
+        h0 = time.perf_counter()
+        e2e_s = time_loop(e2e_step, n_e2e, stream, hold=False)
+        torch.cuda.synchronize()
+        e2e_host_s = time.perf_counter() - h0
     if bad[0]:
         raise RuntimeError("error status in e2e loop")
     del gus, wds
     torch.cuda.empty_cache()
-    return {"dev_s": dev_s, "K": K, "e2e_s": e2e_s, "e2e_K": n_e2e, "chunk_s": chunk_s,
+    return {"dev_s": dev_s, "K": K, "e2e_s": e2e_s, "e2e_host_s": e2e_host_s, "e2e_K": n_e2e, "chunk_s": chunk_s,
             "gate_up_ms": statistics.mean(gate_up_ms), "down_ms": statistics.mean(down_ms),
             "layer_ms": statistics.mean(layer_ms),
             "gate_up_ms_median": statistics.median(gate_up_ms), "h2d": T * H * 2, "d2h": T * H * 2}
@@ -579,6 +617,24 @@ def crossovers(points, tps):
     return out
 
 
+def crossover_sensitivity(points, tps, H, alphas_us=(5.0, 10.0, 20.0), betas_gbs=(400.0, 800.0, 1600.0)):
+    """The crossover (first T at which the replicated block is at least as fast as the
+    sharded one with its two modelled collectives) for each collective model (alpha,
+    beta), from the same measured kernel times: {tp: {"a{alpha}_b{beta}": T or None}}."""
+    out = {}
+    for tp in tps:
+        pts = sorted((p for p in points if p["tp"] == tp), key=lambda p: p["T"])
+        row = {}
+        for a in alphas_us:
+            for b in betas_gbs:
+                c = [p["T"] for p in pts
+                     if (p["sharded_kernel_us"] * 1e-6 + collectives_model_s(p["T"], H, tp, a * 1e-6, b * 1e9))
+                     >= p["replicated_us"] * 1e-6]
+                row[f"a{a:g}us_b{b:g}GBps"] = min(c) if c else None
+        out[str(tp)] = row
+    return out
+
+
 def tp_sweep(args):
     """Per-GPU time of the replicated and the TP-sharded MLP block under sequence
     parallelism, over the group's token count T and tp.  Replicated: each rank runs the
@@ -617,7 +673,11 @@ def tp_sweep(args):
                        "weights": "decode weights, 2 copies cycled (and ranks cycled for the sharded slices)",
                        "collective_model": {"alpha_us": args.coll_alpha_us, "link_GBps": args.coll_link_gbs,
                                             "kind": "modelled, not measured"}},
-            "points": points, "crossover": cross}
+            "points": points, "crossover": cross,
+            "crossover_sensitivity": {
+                "what": "first T at which replication wins, per collective model alpha (us) x beta (GB/s), "
+                        "from the same measured kernel times",
+                "by_tp": crossover_sensitivity(points, tps, H)}}
     print(json.dumps(line), flush=True)
 
 
@@ -668,6 +728,18 @@ def cpu_oracle_baseline(w, max_rows=None):
                       f"{dt:.2f} s wall on {threads} threads"}
 
 
+def decode_config(w, layers, n_gpus):
+    """The workload description shared by the GPU arm and the reference arm."""
+    return {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "weights": "N(0,1/fan_in) bf16, seed 1",
+            "x": "N(0,1) bf16", "l2": f"inputs larger than L2: {layers} distinct weight copies "
+            f"({layers * 264.2:.0f} MB) cycled across steps", "parallelism": f"replicas x{n_gpus}"}
+
+
+def tensor_peak_at_clock(sm_mhz):
+    """Dense bf16 tensor-pipe rate of the whole GPU at the given SM clock (TFLOP/s)."""
+    return N_SMS * BF16_FLOP_PER_SM_CLK * sm_mhz * 1e6 / 1e12 if sm_mhz else None
+
+
 def gpu_arm(args):
     import torch
     dist = Dist()
@@ -703,19 +775,29 @@ def gpu_arm(args):
             wp = dataclasses.replace(wp, T=args.prefill_tokens, name=f"prefill_t{args.prefill_tokens}")
         t_p0 = time.time()
         rp = bench_mlp(wp, args.prefill_steps, max(3, min(args.warmup, 5)), 2, dist, clocks=clocks,
-                       phase_steps=min(10, args.prefill_steps), e2e_steps=0)
+                       phase_steps=min(10, args.prefill_steps), e2e_steps=0, spread_steps=0)
         if clocks:
             clocks.mark("prefill.all", t_p0, time.time())
         ps = dist.max(rp["dev_s"]) / args.prefill_steps
         gu_fl = gate_up_flops(wp.T, wp.H, wp.I)
         ach = gu_fl / (rp["gate_up_ms"] * 1e-3) / 1e12
+        layer_tf = mlp_flops(wp.T, wp.H, wp.I) / ps / 1e12
+        pclk = clocks.summary(f"{wp.name}.timed", "prefill.all") if clocks else None
+        clk_peak = tensor_peak_at_clock(pclk.get("sm_mhz") if pclk else None)
+        pkey = "pair_gate_up_prefill" if args.prefill_tokens >= 512 else "std_gate_up_prefill"
         extra[wp.name] = {
-            "ms_per_layer": ps * 1e3, "tflops": mlp_flops(wp.T, wp.H, wp.I) / ps / 1e12,
-            "frac_of_bf16_peak": mlp_flops(wp.T, wp.H, wp.I) / ps / 1e12 / peaks["bf16_tflops_sustained"],
+            "ms_per_layer": ps * 1e3, "tflops": layer_tf,
+            "frac_of_bf16_peak_sustained": layer_tf / peaks["bf16_tflops_sustained"],
+            "frac_of_bf16_peak_burst": layer_tf / peaks["bf16_tflops"],
+            "frac_of_bf16_spec_2250": layer_tf / SPEC_BF16_TFLOPS,
+            "frac_of_tensor_pipe_at_sampled_clock": layer_tf / clk_peak if clk_peak else None,
             "gate_up_ms": rp["gate_up_ms"], "down_ms": rp["down_ms"],
             "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": ach / peaks["bf16_tflops"], "traffic": profiled_traffic("std_gate_up_prefill"),
-                         "peak_kind": f"burst bf16 ({peaks['source']})"},
+                         "frac": ach / peaks["bf16_tflops"], "traffic": profiled_traffic(pkey),
+                         "peak_kind": f"burst bf16 ({peaks['source']})",
+                         "frac_of_spec_2250": ach / SPEC_BF16_TFLOPS,
+                         "frac_of_tensor_pipe_at_sampled_clock": ach / clk_peak if clk_peak else None},
+            "clocks": pclk,
             "gpu_launches": 2 * args.prefill_steps,
         }
     if args.only == "all":
@@ -779,26 +861,32 @@ def gpu_arm(args):
         k_name = "swapab_kernel<EPI_SWIGLU> (gate_up + SiLU*mul)"
         k_key = "swapab_gate_up_decode"
     ach = k_bytes / (k_ms * 1e-3) / 1e9
+    e2e_host_s = dist.max(r["e2e_host_s"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": N, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms, "us_per_layer": ms * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "weights": "N(0,1/fan_in) bf16, seed 1",
-                   "x": "N(0,1) bf16", "l2": f"inputs larger than L2: {args.layers} distinct weight copies "
-                   f"({args.layers * 264.2:.0f} MB) cycled across steps", "parallelism": f"replicas x{N}",
-                   **({"tuning": tuning} if tuning else {})},
+        "config": {**decode_config(w, args.layers, N), **({"tuning": tuning} if tuning else {})},
+        "timing": "one CUDA event pair around all timed steps on the launching stream (no event between steps)",
         "clocks": clocks.summary(f"{w.name}.timed", "decode.all") if clocks else None,
-        "e2e": {"value": N * bytes_step * r["e2e_K"] / e2e_s / 1e12 if r["e2e_K"] else None, "unit": UNIT,
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_K"]},
+        "e2e": {"value": N * bytes_step * r["e2e_K"] / e2e_host_s / 1e12 if r["e2e_K"] else None, "unit": UNIT,
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_K"],
+                "us_per_layer_host_clock": e2e_host_s / r["e2e_K"] * 1e6 if r["e2e_K"] else None,
+                "us_per_layer_stream_events": e2e_s / r["e2e_K"] * 1e6 if r["e2e_K"] else None,
+                "timing": "host wall clock from the first call to the final synchronize; stream events beside it"},
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": ach / peaks["hbm_gbs"], "traffic": profiled_traffic(k_key),
                      "kernel": k_name, "kernel_ms": k_ms, "algorithmic_bytes": k_bytes,
-                     "peak_kind": f"HBM copy ({peaks['source']})"},
+                     "peak_kind": f"HBM copy ({peaks['source']})",
+                     "frac_of_spec_7900": ach / SPEC_HBM_GBS},
         "step_frac_of_hbm": bytes_step / (dev_s / K) / 1e9 / peaks["hbm_gbs"],
-        "us_per_layer_p10_p50_p90": [v * 1e6 for v in percentiles(r["chunk_s"])],
-        "us_per_layer_spread": f"per-step time of {len(r['chunk_s'])} consecutive chunks of the timed loop",
+        "step_frac_of_hbm_spec_7900": bytes_step / (dev_s / K) / 1e9 / SPEC_HBM_GBS,
     }
+    if r["chunk_s"]:
+        line["us_per_layer_p10_p50_p90"] = [v * 1e6 for v in percentiles(r["chunk_s"])]
+        line["us_per_layer_spread"] = (f"per-step time of {len(r['chunk_s'])} consecutive chunks of a separate "
+                                       f"pass after the timed region")
     if launches == 2 * K:
         line["down_kernel_ms"] = r["down_ms"]
     if extra:
@@ -859,7 +947,7 @@ def reference_arm(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I},
+        "config": decode_config(w, args.layers, dist.world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

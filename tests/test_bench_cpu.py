@@ -75,3 +75,32 @@ def test_percentiles_nearest_rank():
     assert bench.percentiles([5, 1, 3, 2, 4]) == [1, 3, 5]
     assert bench.percentiles([7.0]) == [7.0, 7.0, 7.0]
     assert bench.percentiles(list(range(21))) == [2, 10, 18]
+
+
+def test_crossover_sensitivity_moves_with_the_collective_model():
+    # replicated 50 us at every T; sharded kernels 20 us.  A cheaper collective model can
+    # only move the crossover to a larger T (or away), a dearer one to a smaller T.
+    pts = [{"tp": 8, "T": T, "replicated_us": 50.0, "sharded_kernel_us": 20.0} for T in (16, 64, 256, 1024, 4096)]
+    c = bench.crossover_sensitivity(pts, [8], H, alphas_us=(0.0, 10.0, 20.0), betas_gbs=(400.0, 1600.0))["8"]
+    # alpha 20 us: 2 x 20 us + 20 us of kernel = 60 us > 50 at any T
+    assert c["a20us_b400GBps"] == 16 and c["a20us_b1600GBps"] == 16
+    # alpha 0, beta 1600 GB/s: 20 us + 2 * 7/8 * T * H * 2 / 1.6e12 >= 50 us from T = 4096 on
+    assert c["a0us_b1600GBps"] == 4096
+    order = [c[f"a{a:g}us_b{b:g}GBps"] or 10 ** 9 for a in (0.0, 10.0, 20.0) for b in (1600.0,)]
+    assert order == sorted(order, reverse=True)
+    # the model is the one the sweep uses
+    T = 1024
+    assert (20e-6 + bench.collectives_model_s(T, H, 8, 10e-6, 400e9) >= 50e-6) == (c["a10us_b400GBps"] <= T)
+
+
+def test_decode_config_is_shared_by_both_arms():
+    import workloads as W
+    a = bench.decode_config(W.DECODE_T64, 4, 1)
+    assert a["workload"] == "decode_t64" and a["T"] == 64 and "1057 MB" in a["l2"]
+    assert a == bench.decode_config(W.DECODE_T64, 4, 1)
+
+
+def test_tensor_peak_at_clock():
+    # 152 SMs x 8192 dense bf16 FLOP per clock at 2070 MHz
+    assert bench.tensor_peak_at_clock(2070) == pytest.approx(152 * 8192 * 2.07e9 / 1e12)
+    assert bench.tensor_peak_at_clock(None) is None
