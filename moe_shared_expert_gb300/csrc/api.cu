@@ -269,6 +269,17 @@ mse_status map_gate_up_halves(CUtensorMap *m, const void *w, int64_t H, int64_t 
     return make_map(m, w, 3, dims, strides, box);
 }
 
+// W_gate_up [2I x H] viewed as (k, row r < 16, gate/up, 16-row block b): one box of
+// 64 k x 16 rows x 2 halves x 4 blocks is the 128-row operand of a decode-size gate_up tile
+// of 64 j, in which rows 32b .. 32b+15 are gate rows and rows 32b+16 .. 32b+31 the up rows of
+// the same j, so that a warp's 32 accumulator lanes hold both factors of 16 j.
+mse_status map_gate_up_interleaved(CUtensorMap *m, const void *w, int64_t H, int64_t I) {
+    const uint64_t dims[4] = {(uint64_t)H, 16, 2, (uint64_t)(I / 16)};
+    const uint64_t strides[3] = {(uint64_t)H * 2, (uint64_t)I * H * 2, (uint64_t)16 * H * 2};
+    const uint32_t box[4] = {64, 16, 2, 4};
+    return make_map(m, w, 4, dims, strides, box);
+}
+
 // ----------------------------------------------------------------- launch helpers
 // pair: the CTA-pair kernel, whose CTAs each hold half of the token rows
 tc::SwapAbParams swapab_base(int64_t T, int total_units, bool pair = false) {
@@ -436,14 +447,13 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         const int kbp = (int)(H / 64);
         SwapAbShape sh = swapab_shape(d, T, (int)(width / 64), 1, kbp, false, true);
         tc::SwapAbParams &p = sh.p;
-        if ((st = map_2d(&ta, w_gate_up, 2 * I, H, H, 64)) != MSE_OK) return st;
+        if ((st = map_gate_up_interleaved(&ta, w_gate_up, H, I)) != MSE_OK) return st;
         if ((st = map_2d(&tb, x, T, H, H, sh.b_box_rows)) != MSE_OK) return st;
         p.n_groups = 1;
         p.kb_per_tile = kbp;
         p.kb_first = 0;
         p.kb_group_stride = 0;
         p.a_row_base = (int)j_begin;
-        p.a_up_offset = (int)I;
         p.m_valid = 2 * width;
         p.out = h;
         p.ldo = I;
@@ -574,7 +584,7 @@ mse_status tc_mlp_one_launch(const DeviceInfo &d, const uint16_t *x, int64_t T, 
     tc::SwapAbParams &p1 = fp.ph[2];
     p0 = swapab_base(T, n0a * kbp0);
     p1 = swapab_base(T, groups * n1 * (two ? kbp1 / 2 : kbp1));
-    if ((st = map_2d(&ta0, w_gate_up, 2 * I, H, H, 64)) != MSE_OK) return st;
+    if ((st = map_gate_up_interleaved(&ta0, w_gate_up, H, I)) != MSE_OK) return st;
     if ((st = map_2d(&tb0, x, T, H, H, p0.bn)) != MSE_OK) return st;
     if ((st = map_2d(&ta1, w_down, H, I, I, 128)) != MSE_OK) return st;
     if ((st = map_2d(&tb1, h, T, I, I, p1.bn)) != MSE_OK) return st;
@@ -582,7 +592,6 @@ mse_status tc_mlp_one_launch(const DeviceInfo &d, const uint16_t *x, int64_t T, 
     p0.n_groups = 1;
     p0.kb_per_tile = kbp0;
     p0.a_row_base = (int)j0;
-    p0.a_up_offset = (int)I;
     p0.m_valid = 2 * width;
     p0.out = h;
     p0.ldo = I;

@@ -41,7 +41,6 @@ struct Ctrl {
     uint32_t tmem_base;
     int abort_flag;
     int fin_flag;
-    float xbuf[4][16][32];   // swap-AB SwiGLU epilogue: g/u exchange between lane quarters
     int seg_slot[128];       // swap-AB split-K finisher: slot index of each part of the tile
 };
 
@@ -82,25 +81,24 @@ __device__ __forceinline__ void swapab_epilogue_chunk(const SwapAbParams &p, Ctr
     // independent chains interleave); the stores are unpredicated when the whole
     // chunk is inside T.
     if constexpr (EPI == EPI_SWIGLU) {
-        // Rows 0-63 are gate rows j = j0 + r, rows 64-127 the up rows of the same j, so
-        // quarter q (gate) pairs with quarter q ^ 2 (up).  The gate warp computes tokens
-        // 0-7 of the chunk and the up warp tokens 8-15, each reading its partner's half
-        // from shared memory.
+        // Rows 32q .. 32q+15 are the gate rows of j = j0 + 16q + (lane & 15), rows 32q+16 ..
+        // 32q+31 the up rows of the same j, so lane l < 16 pairs with lane l + 16 of the same
+        // warp.  The gate lane computes tokens 0-7 of the chunk and the up lane tokens 8-15,
+        // each taking its partner's half by a register shuffle.
+        (void)ctl;
+        const bool is_gate = lane < 16;
+        float other[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ctl->xbuf[q][i][lane] = v[i];
-        named_barrier_sync(1, 128);
-        const bool is_gate = q < 2;
-        const int pq = q ^ 2;
-        const int64_t j = (int64_t)p.a_row_base + (int64_t)m * 64 + 32 * (q & 1) + lane;
+        for (int i = 0; i < 8; ++i) other[i] = __shfl_xor_sync(0xffffffffu, is_gate ? v[8 + i] : v[i], 16);
+        const int64_t j = (int64_t)p.a_row_base + (int64_t)m * 64 + 16 * q + (lane & 15);
         const int t0 = c * 16 + (is_gate ? 0 : 8);
         uint16_t hv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float g = is_gate ? v[i] : ctl->xbuf[pq][8 + i][lane];
-            const float u = is_gate ? ctl->xbuf[pq][i][lane] : v[8 + i];
+            const float g = is_gate ? v[i] : other[i];
+            const float u = is_gate ? other[i] : v[8 + i];
             hv[i] = f32_to_bf16_bits(silu_f32(g) * u);
         }
-        named_barrier_sync(1, 128);   // xbuf is rewritten by the next chunk
         uint16_t *h = static_cast<uint16_t *>(p.out) + (int64_t)t0 * p.ldo + j;
         if (t0 + 8 <= p.T) {
 #pragma unroll
@@ -164,8 +162,9 @@ __device__ __forceinline__ void swapab_epilogue_smem(const SwapAbParams &p, cons
                                                      int tid, int t0, int t1) {
     if (t1 > p.T) t1 = p.T;
     if constexpr (EPI == EPI_SWIGLU) {
-        // rows 0-63: g of j = j0 + r; rows 64-127: u of the same j
+        // j = j0 + jr: its gate row is 32 (jr / 16) + jr % 16, its up row 16 further
         const int jr = tid & 63;
+        const int gr = 32 * (jr >> 4) + (jr & 15);
         uint16_t *h = static_cast<uint16_t *>(p.out) + (int64_t)p.a_row_base + (int64_t)m * 64 + jr;
         int t = t0 + (tid >> 6);
         for (; t + 6 < t1; t += 8) {   // 4 tokens per step, computed before storing
@@ -173,14 +172,14 @@ __device__ __forceinline__ void swapab_epilogue_smem(const SwapAbParams &p, cons
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const float *c = tilebuf + (t + 2 * r - t0) * 128;
-                hv[r] = f32_to_bf16_bits(silu_f32(c[jr]) * c[64 + jr]);
+                hv[r] = f32_to_bf16_bits(silu_f32(c[gr]) * c[gr + 16]);
             }
 #pragma unroll
             for (int r = 0; r < 4; ++r) h[(int64_t)(t + 2 * r) * p.ldo] = hv[r];
         }
         for (; t < t1; t += 2) {
             const float *c = tilebuf + (t - t0) * 128;
-            h[(int64_t)t * p.ldo] = f32_to_bf16_bits(silu_f32(c[jr]) * c[64 + jr]);
+            h[(int64_t)t * p.ldo] = f32_to_bf16_bits(silu_f32(c[gr]) * c[gr + 16]);
         }
     } else {
         const int64_t n = (int64_t)m * 128 + tid;
@@ -374,10 +373,16 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
             const int k = kglob(w, i) * 64;
             const uint32_t dst = sm.a(st) + (uint32_t)i * kATileBytes;
             if constexpr (EPI == EPI_SWIGLU) {
-                // rows 0-63: gate rows j0..j0+63; rows 64-127: the up rows of the same j
-                const int j0 = p.a_row_base + mreal(w.m) * 64;
-                tma2d(dst, tmA, fb, k, j0, pol_w, hints);
-                tma2d(dst + 8192u, tmA, fb, k, p.a_up_offset + j0, pol_w, hints);
+                // one box of the (k, row, gate/up, 16-row block) view of W_gate_up: rows
+                // 32b .. 32b+15 are the gate rows of j = j0 + 16b .., rows 32b+16 .. 32b+31
+                // the up rows of the same j (b = 0..3)
+                const int jb0 = (p.a_row_base + mreal(w.m) * 64) / 16;
+                if constexpr (PAIR) {
+                    tma_load_4d_pair_hint(dst, tmA, fb, k, 0, 0, jb0, pol_w);
+                } else {
+                    if (hints) tma_load_4d(dst, tmA, fb, k, 0, 0, jb0, pol_w);
+                    else tma_load_4d_nohint(dst, tmA, fb, k, 0, 0, jb0);
+                }
             } else {
                 tma2d(dst, tmA, fb, k, mreal(w.m) * 128, pol_w, hints);
             }

@@ -28,8 +28,10 @@ struct SwapAbParams {
     int bn;                // MMA N (tokens, padded to a multiple of 16), <= 256
     int stages;            // smem pipeline depth
     int tmem_cols;         // allocated TMEM columns (power of two >= 2*bn)
-    int a_row_base;        // SWIGLU: first intermediate index j of tile 0 (multiple of 64)
-    int a_up_offset;       // SWIGLU: row offset of the up half in W_gate_up (= I)
+    int a_row_base;        // SWIGLU: first intermediate index j of tile 0 (multiple of 64); the
+                           // weight operand is W_gate_up viewed as (k, row, gate/up, 16-row
+                           // block), so that rows 32b .. 32b+15 of a tile are gate rows and
+                           // rows 32b+16 .. 32b+31 the up rows of the same j
     int kbs;               // consecutive k-blocks per pipeline stage (each weight row is fetched
                            // kbs x 128 contiguous bytes at a time; DRAM row-buffer locality)
     int cache_hints;       // 1: weights evict_first, tokens evict_last in L2; 0: no hints
