@@ -362,36 +362,54 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
     down_ms = [e[1].elapsed_time(e[2]) for e in evs]
     layer_ms = [e[0].elapsed_time(e[2]) for e in evs]
 
-    # end to end through the public API with host buffers
-    n_e2e = e2e_steps if e2e_steps is not None else min(K, 2000)
+    # end to end through the public API with host buffers: mlp_swiglu_forward_host reads x
+    # from and writes y to page-locked host memory every step (a copy kernel and the
+    # layer's kernels, all chained by programmatic dependent launch)
+    # at least 200 steps, so that start-up and the final synchronisation do not dominate
+    n_e2e = e2e_steps if e2e_steps is not None else min(max(K, 200), 2000)
     xh = torch.from_numpy(W.make_x(w).view(np.int16)).view(torch.bfloat16).pin_memory()
     yh = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty_like(x)
+    hws = mse.new_host_workspace(T, H, I)
+    pxh, pyh, phws, hwsb = xh.data_ptr(), yh.data_ptr(), hws.data_ptr(), hws.numel()
 
     def e2e_step(i):
+        j = i % layers
+        bad[0] |= L.mlp_swiglu_forward_host(pxh, T, H, I, pgu[j], pwd[j], pyh, cap, phws, hwsb, sp)
+
+    xd = torch.empty_like(x)
+
+    def e2e_torch_step(i):   # the same with torch's host<->device copies around the device call
         j = i % layers
         xd.copy_(xh, non_blocking=True)
         bad[0] |= L.mlp_swiglu_forward(xd.data_ptr(), T, H, I, pgu[j], pwd[j], py, cap, pws, wsb, sp)
         yh.copy_(y, non_blocking=True)
 
-    for i in range(min(Wm, 10)):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    dist.barrier()
-    e2e_s, e2e_host_s = 0.0, 0.0
-    if n_e2e:
+    def host_timed(fn, n):
         # host wall clock from the first call to the final synchronize (host launch and
         # synchronisation costs included), and the stream's own events beside it
         torch.cuda.synchronize()
         h0 = time.perf_counter()
-        e2e_s = time_loop(e2e_step, n_e2e, stream, hold=False)
+        ev = time_loop(fn, n, stream, hold=False)
         torch.cuda.synchronize()
-        e2e_host_s = time.perf_counter() - h0
+        return ev, time.perf_counter() - h0
+
+    for i in range(min(Wm, 10)):
+        e2e_step(i)
+        e2e_torch_step(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e2e_s = e2e_host_s = e2e_torch_host_s = 0.0
+    if n_e2e:
+        e2e_s, e2e_host_s = host_timed(e2e_step, n_e2e)
+        _, e2e_torch_host_s = host_timed(e2e_torch_step, n_e2e)
+        if not torch.equal(yh.cuda(), y):
+            raise RuntimeError("host-buffer output differs from the device output")
     if bad[0]:
         raise RuntimeError("error status in e2e loop")
     del gus, wds
     torch.cuda.empty_cache()
     return {"dev_s": dev_s, "K": K, "e2e_s": e2e_s, "e2e_host_s": e2e_host_s, "e2e_K": n_e2e, "chunk_s": chunk_s,
+            "e2e_torch_host_s": e2e_torch_host_s,
             "gate_up_ms": statistics.mean(gate_up_ms), "down_ms": statistics.mean(down_ms),
             "layer_ms": statistics.mean(layer_ms),
             "gate_up_ms_median": statistics.median(gate_up_ms), "h2d": T * H * 2, "d2h": T * H * 2}
@@ -873,6 +891,9 @@ def gpu_arm(args):
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_K"],
                 "us_per_layer_host_clock": e2e_host_s / r["e2e_K"] * 1e6 if r["e2e_K"] else None,
                 "us_per_layer_stream_events": e2e_s / r["e2e_K"] * 1e6 if r["e2e_K"] else None,
+                "us_per_layer_torch_copies_host_clock":
+                    r["e2e_torch_host_s"] / r["e2e_K"] * 1e6 if r["e2e_K"] else None,
+                "entry": "mlp_swiglu_forward_host (x read from and y written to page-locked host memory)",
                 "timing": "host wall clock from the first call to the final synchronize; stream events beside it"},
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",

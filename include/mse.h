@@ -293,6 +293,38 @@ MSE_API mse_status mlp_swiglu_forward_static_scratch(const mse_bf16 *x, int64_t 
                                                      mse_bf16 *y, int64_t y_capacity, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * The replicated SwiGLU MLP with its activations in host memory: the same layer as
+ * mlp_swiglu_forward ("[Kimi-K3] Add option to shard the shared expert instead of
+ * replicating", section "Change"), for callers whose tokens arrive in, and whose output
+ * goes back to, page-locked host memory.
+ *
+ *   x_host  [T x H] bf16, page-locked host memory mapped into the device's address space
+ *           (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped); on systems
+ *           whose GPU reaches pageable host memory (cudaDevAttrPageableMemoryAccess, e.g.
+ *           Grace-based ones) any host memory
+ *   y_host  [T x H] bf16, the same kind of memory, y_capacity >= T*H elements
+ *   w_gate_up, w_down  device memory, as for mlp_swiglu_forward
+ *   workspace  device memory of mlp_swiglu_host_workspace_bytes(T, H, I) bytes, 256-byte
+ *           aligned, zero before first use: a device copy of x, then the workspace of
+ *           mlp_swiglu_forward (same rules for reuse)
+ *
+ * Three kernels on `stream`, each launched with programmatic dependent launch, so that
+ * none of them cuts the overlap of consecutive calls: a copy of x into the workspace, and
+ * the two kernels of the layer, the down projection writing y straight into y_host.  The
+ * copy reads x while the previous work on the stream still runs, unless x overlaps the
+ * y_host of the previous call of this entry point on the same stream (layers chained
+ * through host memory): then it reads after that work is complete.  y_host holds the result once the stream has reached
+ * the end of the call (e.g. after cudaStreamSynchronize); the host must not modify x or
+ * read y before then.  MSE_ERR_INVALID_ARG if a host pointer is not mapped page-locked
+ * memory or the two buffers overlap.
+ * ------------------------------------------------------------------------- */
+MSE_API size_t mlp_swiglu_host_workspace_bytes(int64_t T, int64_t H, int64_t I);
+MSE_API mse_status mlp_swiglu_forward_host(const mse_bf16 *x_host, int64_t T, int64_t H, int64_t I,
+                                           const mse_bf16 *w_gate_up, const mse_bf16 *w_down, mse_bf16 *y_host,
+                                           int64_t y_capacity, void *workspace, size_t workspace_bytes,
+                                           void *stream);
+
+/* ---------------------------------------------------------------------------
  * Errors raised on the device and process-wide settings.
  * ------------------------------------------------------------------------- */
 

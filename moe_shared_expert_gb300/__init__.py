@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
                 "merged_proj_forward": (ci, [P, i64, i64, P, i64, i64, ci, P, P, i64, P, sz, P]),
                 "merged_proj_reorder": (ci, [P, P, i64, i64, i64, ci, i64, P]),
                 "mlp_swiglu_forward_static_scratch": (ci, [P, i64, i64, i64, P, P, P, i64, P]),
+                "mlp_swiglu_host_workspace_bytes": (sz, [i64, i64, i64]),
+                "mlp_swiglu_forward_host": (ci, [P, i64, i64, i64, P, P, P, i64, P, sz, P]),
                 "mse_poll_device_error": (ci, [P]),
                 "mse_set_wait_limit_ns": (None, [u64]),
                 "mse_get_wait_limit_ns": (u64, []),
@@ -186,6 +188,11 @@ def new_mlp_workspace(T: int, H: int, I: int, device="cuda"):
     return _workspace(mlp_swiglu_workspace_bytes(T, H, I), device)
 
 
+def new_host_workspace(T: int, H: int, I: int, device="cuda"):
+    """A zero-filled workspace for mlp_swiglu_forward_host."""
+    return _workspace(mlp_swiglu_host_workspace_bytes(T, H, I), device)
+
+
 def new_merged_workspace(T: int, H: int, q_dim: int, kv_dim: int, device="cuda"):
     return _workspace(merged_proj_workspace_bytes(T, H, q_dim, kv_dim), device)
 
@@ -207,6 +214,32 @@ def mlp_swiglu_forward(x, w_gate_up, w_down, y=None, workspace=None, stream=None
                                   _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check("mlp_swiglu_forward", st)
     return y
+
+
+def mlp_swiglu_host_workspace_bytes(T: int, H: int, I: int) -> int:
+    return int(lib().mlp_swiglu_host_workspace_bytes(T, H, I))
+
+
+def mlp_swiglu_forward_host(x_host, w_gate_up, w_down, y_host=None, workspace=None, stream=None):
+    """The layer with x and y in page-locked host memory (pinned CPU tensors); y_host holds
+    the result once the stream has reached the end of the call."""
+    torch = _torch()
+    if x_host.is_cuda or x_host.dtype not in _bf16s() or x_host.dim() != 2 or not x_host.is_contiguous() \
+            or not x_host.is_pinned():
+        raise ValueError("x_host: need a contiguous 2-d pinned CPU bf16 tensor")
+    _need(w_gate_up, "w_gate_up", _bf16s(), 2)
+    _need(w_down, "w_down", _bf16s(), 2)
+    T, H = x_host.shape
+    I = w_down.shape[1]
+    if y_host is None:
+        y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    if workspace is None:
+        workspace = new_host_workspace(T, H, I, w_down.device)
+    st = lib().mlp_swiglu_forward_host(_ptr(x_host), T, H, I, _ptr(w_gate_up), _ptr(w_down), _ptr(y_host),
+                                       y_host.numel(), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    _check("mlp_swiglu_forward_host", st)
+    return y_host
 
 
 def mlp_swiglu_shard_partial(x, w_gate_up, w_down, tp, rank_first=0, rank_count=None, partial_dtype=None,

@@ -683,6 +683,39 @@ using namespace mse;
 // =============================================================================
 // exported C ABI
 // =============================================================================
+namespace mse {
+namespace {
+// The host range that the last mlp_swiglu_forward_host call on each stream writes (its
+// y).  A call whose x overlaps it must not read x before that call's kernels are done;
+// any other host range may be read while the previous work on the stream still runs
+// (kernels of other libraries do not start this library's kernels early, and copies
+// complete before a kernel after them starts).  Recorded in call order, so also right
+// for calls captured into a CUDA graph.
+struct HostOutput {
+    void *stream;
+    uintptr_t lo, hi;
+};
+std::mutex g_hostout_mu;
+HostOutput g_hostout[64];
+int g_hostout_n = 0;
+
+bool host_range_overlaps_last_output(void *stream, uintptr_t lo, uintptr_t hi) {
+    std::lock_guard<std::mutex> lk(g_hostout_mu);
+    for (int i = 0; i < g_hostout_n; ++i)
+        if (g_hostout[i].stream == stream) return lo < g_hostout[i].hi && g_hostout[i].lo < hi;
+    return false;
+}
+
+void record_host_output(void *stream, uintptr_t lo, uintptr_t hi) {
+    std::lock_guard<std::mutex> lk(g_hostout_mu);
+    for (int i = 0; i < g_hostout_n; ++i)
+        if (g_hostout[i].stream == stream) { g_hostout[i].lo = lo; g_hostout[i].hi = hi; return; }
+    if (g_hostout_n == 64) g_hostout_n = 0;   // forget the oldest streams (only makes copies wait)
+    g_hostout[g_hostout_n++] = {stream, lo, hi};
+}
+}  // namespace
+}  // namespace mse
+
 extern "C" {
 
 size_t mlp_swiglu_workspace_bytes(int64_t T, int64_t H, int64_t I) {
@@ -872,6 +905,48 @@ mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int
     }
     record(g_ev_end, s);
     return MSE_OK;
+}
+
+size_t mlp_swiglu_host_workspace_bytes(int64_t T, int64_t H, int64_t I) {
+    const size_t n = mlp_swiglu_workspace_bytes(T, H, I);
+    if (n == 0) return 0;
+    return align_up((size_t)T * (size_t)H * 2, 256) + n;
+}
+
+mse_status mlp_swiglu_forward_host(const mse_bf16 *x_host, int64_t T, int64_t H, int64_t I,
+                                   const mse_bf16 *w_gate_up, const mse_bf16 *w_down, mse_bf16 *y_host,
+                                   int64_t y_capacity, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!x_host || !w_gate_up || !w_down || !y_host || T <= 0 || H <= 0 || I <= 0) return MSE_ERR_INVALID_ARG;
+    if (y_capacity < T * H) return MSE_ERR_GEOMETRY;
+    const size_t act = align_up((size_t)T * (size_t)H * 2, 256);
+    if (!workspace || workspace_bytes < act || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MSE_ERR_WORKSPACE;
+    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes - act);
+    if (workspace_bytes - act < L.total) return MSE_ERR_WORKSPACE;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x_host), ya = reinterpret_cast<uintptr_t>(y_host);
+    const uintptr_t nb = (uintptr_t)(T * H * 2);
+    if (xa < ya + nb && ya < xa + nb) return MSE_ERR_INVALID_ARG;   // x and y overlap
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    // the device's view of the caller's page-locked buffers
+    void *xh = nullptr, *yh = nullptr;
+    if (cudaHostGetDevicePointer(&xh, const_cast<mse_bf16 *>(x_host), 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&yh, y_host, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return MSE_ERR_INVALID_ARG;
+    }
+    char *ws = static_cast<char *>(workspace);
+    mse_bf16 *xd = reinterpret_cast<mse_bf16 *>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // x may be read before the previous work on the stream is done unless the previous call
+    // of this entry point on the stream writes it
+    const bool early = !host_range_overlaps_last_output(stream, xa, xa + nb);
+    record_host_output(stream, ya, ya + nb);
+    if ((st = from_cuda(launch_copy_in(xh, xd, T * H * 2, early, d->sm_count, s))) != MSE_OK) return st;
+    // the down projection writes y straight into the caller's host buffer
+    return mlp_swiglu_forward(xd, T, H, I, w_gate_up, w_down, static_cast<mse_bf16 *>(yh), y_capacity, ws + act,
+                              workspace_bytes - act, stream);
 }
 
 int mse_shard_sequence_parallel_mlp(int enabled, int use_sequence_parallel, int eligible, int tp_size,

@@ -102,6 +102,44 @@ __global__ void __launch_bounds__(256) reorder_kernel(const uint16_t *__restrict
     }
 }
 
+// Copy of activations from host memory (device-mapped) to device memory, launched with
+// programmatic dependent launch.  It waits for the previous kernel before writing (the
+// destination may still be read by it).  With `early`, each thread reads its first
+// kCopyPer 16-byte words before that wait (the caller knows that the previous work on
+// the stream does not write the source); else it reads after the wait too.
+constexpr int kCopyPer = 4;
+
+__global__ void __launch_bounds__(256) copy_in_vec(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n,
+                                                   int early) {
+    pdl_launch_dependents();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint4 v[kCopyPer];
+    if (early) {
+#pragma unroll
+        for (int k = 0; k < kCopyPer; ++k)
+            if (i0 + k * stride < n) v[k] = src[i0 + k * stride];
+    }
+    pdl_wait();
+    if (!early) {
+#pragma unroll
+        for (int k = 0; k < kCopyPer; ++k)
+            if (i0 + k * stride < n) v[k] = src[i0 + k * stride];
+    }
+#pragma unroll
+    for (int k = 0; k < kCopyPer; ++k)
+        if (i0 + k * stride < n) dst[i0 + k * stride] = v[k];
+    for (int64_t i = i0 + kCopyPer * stride; i < n; i += stride) dst[i] = src[i];
+}
+
+__global__ void __launch_bounds__(256) copy_in_bytes(const unsigned char *__restrict__ src,
+                                                     unsigned char *__restrict__ dst, int64_t n) {
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
 // One CTA waits on a barrier that nothing arrives on, bounded by limit_ns.
 __global__ void wait_selftest_kernel(uint64_t limit_ns, uint32_t *err) {
     __shared__ __align__(8) uint64_t bar;
@@ -160,6 +198,21 @@ cudaError_t launch_reorder(const uint16_t *rm, uint16_t *logical, int64_t T, int
     if (total <= 0) return cudaSuccess;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
     return launch_ew(reorder_kernel, blocks, pdl, s, rm, logical, T, C, q_dim, q_dim / tp, kv_dim / tp);
+}
+
+cudaError_t launch_copy_in(const void *src, void *dst, int64_t bytes, bool early, int sm_count, cudaStream_t s) {
+    if (bytes <= 0) return cudaSuccess;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src), b = reinterpret_cast<uintptr_t>(dst);
+    if (a % 16 == 0 && b % 16 == 0 && bytes % 16 == 0) {
+        const int64_t n = bytes / 16;
+        const int per = 256 * kCopyPer;
+        const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + per - 1) / per, (int64_t)sm_count * 4));
+        return launch_ew(copy_in_vec, blocks, true, s, static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n,
+                         early ? 1 : 0);
+    }
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((bytes + 255) / 256, (int64_t)sm_count * 4));
+    return launch_ew(copy_in_bytes, blocks, true, s, static_cast<const unsigned char *>(src),
+                     static_cast<unsigned char *>(dst), bytes);
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *err, cudaStream_t s) {

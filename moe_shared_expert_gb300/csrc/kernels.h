@@ -35,5 +35,8 @@ cudaError_t launch_shard_sum(const void *partials, int dtype_f32, int n_parts, i
 cudaError_t launch_reorder(const uint16_t *rm, uint16_t *logical, int64_t T, int64_t q_dim, int64_t kv_dim, int tp,
                            bool pdl, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *err, cudaStream_t s);
+// Copy of activations from host (device-mapped) to device memory, with programmatic
+// dependent launch; `early`: the source is read before waiting for the previous kernel.
+cudaError_t launch_copy_in(const void *src, void *dst, int64_t bytes, bool early, int sm_count, cudaStream_t s);
 
 }  // namespace mse

@@ -123,6 +123,18 @@ def test_forward_validation(L):
 
 
 @no_gpu_only
+def test_forward_host_validation(L):
+    f = L.mlp_swiglu_forward_host
+    n = L.mlp_swiglu_host_workspace_bytes(64, 7168, 6144)
+    assert n == L.mlp_swiglu_workspace_bytes(64, 7168, 6144) + 64 * 7168 * 2   # + the device copy of x
+    assert f(None, 64, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168, FAKE, n, None) == code("MSE_ERR_INVALID_ARG")
+    assert f(FAKE, 64, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168 - 1, FAKE, n, None) == code("MSE_ERR_GEOMETRY")
+    assert f(FAKE, 64, 7168, 6144, FAKE, FAKE, FAKE * 16, 64 * 7168, FAKE, n - 256, None) == code("MSE_ERR_WORKSPACE")
+    # x and y overlap (checked before any CUDA call)
+    assert f(FAKE, 64, 7168, 6144, FAKE, FAKE, FAKE + 64, 64 * 7168, FAKE, n, None) == code("MSE_ERR_INVALID_ARG")
+
+
+@no_gpu_only
 def test_shard_partial_validation(L):
     f = L.mlp_swiglu_shard_partial
     args = lambda tp, rf, rc, cap, dt=0: (FAKE, 128, 7168, 6144, FAKE, FAKE, tp, rf, rc, FAKE, dt, cap, FAKE,
