@@ -781,7 +781,7 @@ def gpu_arm(args):
         r = None
     else:
         t_w0 = time.time()
-        r = bench_mlp(w, args.steps, args.warmup, args.layers, dist, clocks=clocks)
+        r = bench_mlp(w, args.steps, args.warmup, args.layers, dist, clocks=clocks, spread_steps=args.spread_steps)
         dev_s = dist.max(r["dev_s"])
         e2e_s = dist.max(r["e2e_s"])
         if clocks:
@@ -995,6 +995,8 @@ def main():
     ap.add_argument("--tune", default="",
                     help="library tuning for the run, e.g. one_launch=2,grid=144 (names of mse.TUNE_*)")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
+    ap.add_argument("--spread-steps", type=int, default=2000,
+                    help="steps of the separate pass that gives the p10/p50/p90 spread (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--two-launch", action="store_true",
