@@ -384,6 +384,13 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         (gate_up at 64 tokens on 144 CTAs), launch clusters of three and finish
  *                         each two-part tile inside its cluster (same results bit for bit;
  *                         measured within 0.1 us); 0 = through L2 only (default)
+ *   MSE_TUNE_L2_PREFETCH  decode token counts: 64-wide k-blocks of weight tiles beyond the
+ *                         pipeline that a CTA prefetches into L2 before waiting for the previous
+ *                         kernel, if it was not placed on an SM idle at launch: such CTAs start
+ *                         while the previous kernel's split-K tail leaves HBM underused.  Applied
+ *                         to launches of at most 64 tokens with at least 32 k-blocks per CTA
+ *                         (default 8: the decode layer measured 54.2 against 54.35 us with none,
+ *                         56.0 with 16; 0 = none)
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -397,7 +404,8 @@ typedef enum {
     MSE_TUNE_COOP_FINISH = 9,
     MSE_TUNE_PAIR_MIN_T = 10,
     MSE_TUNE_GRID_DOWN = 11,
-    MSE_TUNE_CLUSTER_FINISH = 12
+    MSE_TUNE_CLUSTER_FINISH = 12,
+    MSE_TUNE_L2_PREFETCH = 14
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

@@ -410,6 +410,22 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
             load_a(a, n, st);
             a.advance(n);
         }
+        if (!PAIR && p.l2_prefetch_kb > 0 && (int)blockIdx.x >= p.l2_prefetch_from) {
+            // the next weight tiles into L2 while the previous kernel finishes
+            int left = p.l2_prefetch_kb;
+            while (left > 0 && !a.done()) {
+                const int n = a.count(KBS) < left ? a.count(KBS) : left;
+                for (int i = 0; i < n; ++i) {
+                    const int k = kglob(a, i) * 64;
+                    if constexpr (EPI == EPI_SWIGLU)
+                        tma_prefetch_l2_4d(tmA, k, 0, 0, (p.a_row_base + a.m * 64) / 16);
+                    else
+                        tma_prefetch_l2_2d(tmA, k, a.m * 128);
+                }
+                a.advance(n);
+                left -= n;
+            }
+        }
         pdl_wait();
         for (int t = 0; t < st; ++t) {
             const int n = w.count(KBS);

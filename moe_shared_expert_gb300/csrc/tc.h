@@ -41,6 +41,10 @@ struct SwapAbParams {
     int coop_finish;       // > 0: a tile split into at least this many parts, in the CTAs' final
                            // segments, is finished jointly (each part's CTA sums one slice of
                            // token columns) when the ring is idle; 0: never
+    int l2_prefetch_kb;    // k-blocks of weight tiles beyond the ring prefetched into L2 before the
+                           // wait for the previous kernel, by CTAs with blockIdx >= l2_prefetch_from
+    int l2_prefetch_from;  // (CTAs dispatched after the SMs that were idle at launch: they start
+                           // while the previous kernel's tail leaves HBM underused)
     int T;                 // valid tokens
     int64_t m_valid;       // valid output features (A rows) for masking
     void *out; int64_t ldo; int64_t o_group_stride;
