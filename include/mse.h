@@ -79,9 +79,10 @@ typedef enum { MSE_BF16 = 0, MSE_F32 = 1 } mse_dtype;
  *                MSE_ERR_UNSUPPORTED_SHAPE. */
 typedef enum { MSE_PATH_AUTO = 0, MSE_PATH_GENERIC = 1, MSE_PATH_TENSORCORE = 2 } mse_kernel_path;
 
-/* Tensor-core kernel for prefill-sized token counts (T > 256), process-wide.
- *   AUTO:   CTA-pair kernel (two SMs share one 256 x 256 tile) for T >= 512,
- *           single-CTA 128 x 256 kernel below.
+/* Tensor-core kernel for the token counts the decode-size kernels do not serve
+ * (MSE_TUNE_SWAPAB_MAX_T), process-wide.
+ *   AUTO:   CTA-pair kernel (two SMs share one 256 x 256 tile) up to 256 tokens and from
+ *           512 on, single-CTA 128 x 256 kernel between.
  *   SINGLE: always the single-CTA kernel.   PAIR: always the CTA-pair kernel. */
 typedef enum { MSE_PREFILL_AUTO = 0, MSE_PREFILL_SINGLE = 1, MSE_PREFILL_PAIR = 2 } mse_prefill_kernel;
 
@@ -391,6 +392,11 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         to launches of at most 64 tokens with at least 32 k-blocks per CTA
  *                         (default 8: the decode layer measured 54.2 against 54.35 us with none,
  *                         56.0 with 16; 0 = none)
+ *   MSE_TUNE_SWAPAB_MAX_T launches over at least 4096 weight rows (the full layer) take the
+ *                         decode-size (swap-AB) kernels up to this token count and the prefill
+ *                         kernels above it (0 .. 256, default 176: at 192-256 tokens the full
+ *                         layer measured 73 us on the CTA-pair kernel against 82-93 us); narrower
+ *                         launches take the swap-AB kernels up to 256 tokens
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -405,7 +411,8 @@ typedef enum {
     MSE_TUNE_PAIR_MIN_T = 10,
     MSE_TUNE_GRID_DOWN = 11,
     MSE_TUNE_CLUSTER_FINISH = 12,
-    MSE_TUNE_L2_PREFETCH = 14
+    MSE_TUNE_L2_PREFETCH = 14,
+    MSE_TUNE_SWAPAB_MAX_T = 15
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

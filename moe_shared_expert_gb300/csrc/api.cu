@@ -21,7 +21,7 @@ std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
     g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
     g_tune_coop_finish{6}, g_tune_pair_min_t{0}, g_tune_grid_down{0}, g_tune_cluster_finish{0},
-    g_tune_l2_prefetch{8};
+    g_tune_l2_prefetch{8}, g_tune_swapab_max_t{176};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -103,7 +103,7 @@ struct MlpWs {
            flags_off = 0, exit_off = 0, sync_off = 0, sync_bytes = 0, total = 0;
 };
 
-constexpr int64_t kSwapAbMaxT = 256;   // token counts served by the swap-AB kernels
+constexpr int64_t kSwapAbMaxT = 256;   // token counts the swap-AB kernels can serve (workspace layout)
 
 size_t align_down(size_t v, size_t a) { return v / a * a; }
 
@@ -306,6 +306,18 @@ tc::SwapAbParams swapab_base(int64_t T, int total_units, bool pair = false) {
 
 bool use_pdl() { return g_tune_pdl.load() != 0; }
 
+// Whether a launch of T tokens over `rows` weight rows takes the swap-AB kernels (else the
+// prefill kernels).  Up to 256 tokens (the split-K slots the workspace layout provides),
+// except that launches over at least 4096 weight rows switch at MSE_TUNE_SWAPAB_MAX_T
+// (default 176): the full layer measured 82-93 us at 192-256 tokens on the swap-AB kernels,
+// whose ring holds two stages there, and 73 us on the CTA-pair prefill kernel (68.5 against
+// 72.8 us at 160 tokens).  Narrow launches (a shard's slice) would leave most SMs idle on
+// the prefill kernels.
+bool use_swapab(int64_t T, int64_t rows) {
+    if (T > kSwapAbMaxT) return false;
+    return rows < 4096 || T <= g_tune_swapab_max_t.load();
+}
+
 // Stream-K grid for `units` units of `kbp` per tile.  Among CTA counts from 90% of the
 // SMs up to all of them, the largest one that minimises the largest number of CTAs any
 // tile is split between, if that is at most three: each extra part lengthens the tile's
@@ -430,11 +442,15 @@ tc::StdParams std_base(int64_t T) {
     return p;
 }
 
+// Prefill-kernel choice (MSE_PREFILL_AUTO): the CTA pair up to 256 tokens (one 256-token
+// tile: the full layer measured 73 us against 89 on single CTAs at 192-256 tokens) and from
+// 512 on; single CTAs between (at 320 tokens 90 against 103 us for the pair, whose second
+// token tile is mostly padding).
 bool use_pair(int64_t T) {
     const int k = g_prefill.load();
     if (k == MSE_PREFILL_SINGLE) return false;
     if (k == MSE_PREFILL_PAIR) return true;
-    return T >= 512;
+    return T <= 256 || T >= 512;
 }
 
 int pair_clusters(const DeviceInfo &d, int64_t n_tiles) {
@@ -453,7 +469,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
                       const MlpWs &L, cudaStream_t s) {
     CUtensorMap ta, tb;
     mse_status st;
-    if (T <= kSwapAbMaxT) {
+    if (use_swapab(T, 2 * width)) {
         const int kbp = (int)(H / 64);
         SwapAbShape sh = swapab_shape(d, T, (int)(width / 64), 1, kbp, false, true);
         tc::SwapAbParams &p = sh.p;
@@ -514,7 +530,8 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
                    cudaStream_t s) {
     CUtensorMap ta, tb;
     mse_status st;
-    if (T <= kSwapAbMaxT) {
+    // the same choice as the layer's gate_up launch (its rows: 2 x the intermediate columns)
+    if (use_swapab(T, 2 * (int64_t)groups * s_width)) {
         const int kbp = (int)(s_width / 64);
         SwapAbShape sh = swapab_shape(d, T, (int)((H + 127) / 128), groups, kbp, true, true);
         tc::SwapAbParams &p = sh.p;
@@ -1005,7 +1022,7 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
     }
     CUtensorMap ta, tb;
     char *ws = static_cast<char *>(workspace);
-    if (T <= kSwapAbMaxT) {
+    if (use_swapab(T, C)) {
         const int kbp = (int)(H / 64);
         SwapAbShape sh = swapab_shape(*d, T, (int)((C + 127) / 128), 1, kbp);
         tc::SwapAbParams &p = sh.p;
@@ -1122,6 +1139,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_GRID_DOWN: slot = &g_tune_grid_down; ok = value >= 0 && value <= tc::kMaxGrid; break;
         case MSE_TUNE_CLUSTER_FINISH: slot = &g_tune_cluster_finish; ok = value == 0 || value == 1; break;
         case MSE_TUNE_L2_PREFETCH: slot = &g_tune_l2_prefetch; ok = value >= 0 && value <= 256; break;
+        case MSE_TUNE_SWAPAB_MAX_T: slot = &g_tune_swapab_max_t; ok = value >= 0 && value <= kSwapAbMaxT; break;
         default: return -1;
     }
     if (!ok) return -1;

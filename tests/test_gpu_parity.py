@@ -247,6 +247,26 @@ def test_ragged_tokens(T, path):
     assert_close(bits_f64(y), bits_f64(y_ref), f"y T={T}")
 
 
+@pytest.mark.parametrize("T", [192, 256])
+@pytest.mark.parametrize("swapab_max_t", [176, 256])
+def test_near_ridge_tokens_decode_weights(T, swapab_max_t):
+    # 129-256 tokens on the Kimi-K3 shapes: the CTA-pair prefill kernels (default above 176
+    # tokens for the full layer) and the swap-AB kernels (forced), every row against the oracle
+    w = W.DECODE_T64
+    wgu, wd = W.make_mlp_weights(w)
+    x = W.make_custom(1800 + T, 0, (T, w.H))
+    old = mse.set_tuning(mse.TUNE_SWAPAB_MAX_T, swapab_max_t)
+    try:
+        with kernel_path(mse.PATH_TENSORCORE):
+            y, h = run_forward(x, wgu, wd)
+    finally:
+        mse.set_tuning(mse.TUNE_SWAPAB_MAX_T, old)
+    y_ref, _, h_ref = oracle.mlp_forward(x, wgu, wd)
+    assert_close(bits_f64(h), bits_f64(h_ref), f"h T={T}")
+    r = assert_close(bits_f64(y), bits_f64(y_ref), f"y T={T}")
+    print(f"T={T} swap-AB up to {swapab_max_t}: max err/tol {r:.3f}")
+
+
 @pytest.mark.parametrize("T", [257, 300, 512, 700, 1000])
 @pytest.mark.parametrize("kind", [mse.PREFILL_SINGLE, mse.PREFILL_PAIR])
 def test_prefill_kernels_ragged(T, kind):
