@@ -394,8 +394,8 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         56.0 with 16; 0 = none)
  *   MSE_TUNE_SWAPAB_MAX_T launches over at least 4096 weight rows (the full layer) take the
  *                         decode-size (swap-AB) kernels up to this token count and the prefill
- *                         kernels above it (0 .. 256, default 176: at 192-256 tokens the full
- *                         layer measured 73 us on the CTA-pair kernel against 82-93 us); narrower
+ *                         kernels above it (0 .. 256, default 160: at 176-256 tokens the full
+ *                         layer measured 73 us on the CTA-pair kernel against 80-93 us); narrower
  *                         launches take the swap-AB kernels up to 256 tokens
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */

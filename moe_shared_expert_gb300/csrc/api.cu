@@ -21,7 +21,7 @@ std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
     g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
     g_tune_coop_finish{6}, g_tune_pair_min_t{0}, g_tune_grid_down{0}, g_tune_cluster_finish{0},
-    g_tune_l2_prefetch{8}, g_tune_swapab_max_t{176};
+    g_tune_l2_prefetch{8}, g_tune_swapab_max_t{160};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -309,10 +309,10 @@ bool use_pdl() { return g_tune_pdl.load() != 0; }
 // Whether a launch of T tokens over `rows` weight rows takes the swap-AB kernels (else the
 // prefill kernels).  Up to 256 tokens (the split-K slots the workspace layout provides),
 // except that launches over at least 4096 weight rows switch at MSE_TUNE_SWAPAB_MAX_T
-// (default 176): the full layer measured 82-93 us at 192-256 tokens on the swap-AB kernels,
-// whose ring holds two stages there, and 73 us on the CTA-pair prefill kernel (68.5 against
-// 72.8 us at 160 tokens).  Narrow launches (a shard's slice) would leave most SMs idle on
-// the prefill kernels.
+// (default 160): the full layer measured 80-93 us at 176-256 tokens on the swap-AB kernels,
+// whose ring holds two stages there, and 72.6-73.2 us on the CTA-pair prefill kernel (68.3
+// against 72.8 us at 160 tokens).  Narrow launches (a shard's slice) would leave most SMs
+// idle on the prefill kernels.
 bool use_swapab(int64_t T, int64_t rows) {
     if (T > kSwapAbMaxT) return false;
     return rows < 4096 || T <= g_tune_swapab_max_t.load();
