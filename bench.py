@@ -299,7 +299,16 @@ def one_launch_active() -> bool:
     return old == 1
 
 
-def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=None, spread_steps=2000):
+# Library options for the decode leg.  The workload's x is a buffer that no kernel writes
+# and each step's y and workspace are the same buffers, so a step's x never overlaps what
+# the previous step writes: MSE_TUNE_X_EARLY lets each layer's gate_up weight stream start
+# during the previous layer's split-K tail; with it, 12 k-blocks of L2 prefetch measured best.
+# The time with the library's default settings is reported beside the headline.
+DECODE_TUNING = "x_early=1,l2_prefetch=12"
+
+
+def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=None, spread_steps=2000,
+              default_steps=0):
     """Replicated shared-expert layer: returns dict with device time, e2e time and phase times."""
     import torch
     import moe_shared_expert_gb300 as mse
@@ -340,6 +349,21 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
     st = mse.poll_device_error()
     if st:
         raise RuntimeError(f"device error {mse.STATUS.get(st)}")
+
+    # the same loop with the library's default settings (no event inside its loop either)
+    default_s = None
+    if default_steps:
+        saved = {k: mse.set_tuning(getattr(mse, "TUNE_" + k.upper()), d)
+                 for k, d in (("x_early", 0), ("l2_prefetch", 8))}
+        for i in range(Wm):
+            step(i)
+        torch.cuda.synchronize()
+        default_s = time_loop(step, default_steps, stream) / default_steps
+        for k, v in saved.items():
+            mse.set_tuning(getattr(mse, "TUNE_" + k.upper()), v)
+        for i in range(Wm):
+            step(i)
+        torch.cuda.synchronize()
 
     # spread of the per-step time: a separate pass of 20 chunks of >= 50 steps each
     # (the headline above has no event inside its loop)
@@ -409,7 +433,7 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
     del gus, wds
     torch.cuda.empty_cache()
     return {"dev_s": dev_s, "K": K, "e2e_s": e2e_s, "e2e_host_s": e2e_host_s, "e2e_K": n_e2e, "chunk_s": chunk_s,
-            "e2e_torch_host_s": e2e_torch_host_s,
+            "e2e_torch_host_s": e2e_torch_host_s, "default_s": default_s, "default_K": default_steps,
             "gate_up_ms": statistics.mean(gate_up_ms), "down_ms": statistics.mean(down_ms),
             "layer_ms": statistics.mean(layer_ms),
             "gate_up_ms_median": statistics.median(gate_up_ms), "h2d": T * H * 2, "d2h": T * H * 2}
@@ -781,7 +805,18 @@ def gpu_arm(args):
         r = None
     else:
         t_w0 = time.time()
-        r = bench_mlp(w, args.steps, args.warmup, args.layers, dist, clocks=clocks, spread_steps=args.spread_steps)
+        decode_tuning = {}
+        saved = {}
+        if not args.tune and not args.library_defaults:
+            for item in DECODE_TUNING.split(","):
+                name, v = item.split("=")
+                saved[name] = mse.set_tuning(getattr(mse, "TUNE_" + name.upper()), int(v))
+                decode_tuning[name] = int(v)
+        r = bench_mlp(w, args.steps, args.warmup, args.layers, dist, clocks=clocks, spread_steps=args.spread_steps,
+                      default_steps=max(args.steps, 2000) if decode_tuning else 0)
+        for name, v in saved.items():
+            mse.set_tuning(getattr(mse, "TUNE_" + name.upper()), v)
+        tuning = {**decode_tuning, **tuning}
         dev_s = dist.max(r["dev_s"])
         e2e_s = dist.max(r["e2e_s"])
         if clocks:
@@ -884,7 +919,8 @@ def gpu_arm(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": N, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms, "us_per_layer": ms * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {**decode_config(w, args.layers, N), **({"tuning": tuning} if tuning else {})},
+        "config": decode_config(w, args.layers, N),
+        "library_tuning": tuning or None,
         "timing": "one CUDA event pair around all timed steps on the launching stream (no event between steps)",
         "clocks": clocks.summary(f"{w.name}.timed", "decode.all") if clocks else None,
         "e2e": {"value": N * bytes_step * r["e2e_K"] / e2e_host_s / 1e12 if r["e2e_K"] else None, "unit": UNIT,
@@ -904,6 +940,10 @@ def gpu_arm(args):
         "step_frac_of_hbm": bytes_step / (dev_s / K) / 1e9 / peaks["hbm_gbs"],
         "step_frac_of_hbm_spec_7900": bytes_step / (dev_s / K) / 1e9 / SPEC_HBM_GBS,
     }
+    if r.get("default_s"):
+        line["us_per_layer_library_defaults"] = r["default_s"] * 1e6
+        line["library_defaults"] = (f"{r['default_K']} steps timed the same way with the library's default "
+                                    f"settings (x_early=0, l2_prefetch=8)")
     if r["chunk_s"]:
         line["us_per_layer_p10_p50_p90"] = [v * 1e6 for v in percentiles(r["chunk_s"])]
         line["us_per_layer_spread"] = (f"per-step time of {len(r['chunk_s'])} consecutive chunks of a separate "
@@ -995,6 +1035,8 @@ def main():
     ap.add_argument("--tune", default="",
                     help="library tuning for the run, e.g. one_launch=2,grid=144 (names of mse.TUNE_*)")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
+    ap.add_argument("--library-defaults", action="store_true",
+                    help="time the decode leg with the library's default settings only (no DECODE_TUNING)")
     ap.add_argument("--spread-steps", type=int, default=2000,
                     help="steps of the separate pass that gives the p10/p50/p90 spread (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

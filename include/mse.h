@@ -397,6 +397,15 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         kernels above it (0 .. 256, default 160: at 176-256 tokens the full
  *                         layer measured 73 us on the CTA-pair kernel against 80-93 us); narrower
  *                         launches take the swap-AB kernels up to 256 tokens
+ *   MSE_TUNE_X_EARLY      1 = mlp_swiglu_forward (decode-size kernels) reads its x without waiting
+ *                         for the previous kernel on the stream when x overlaps neither the y nor
+ *                         the workspace of the previous mlp_swiglu_forward call on that stream
+ *                         and no other call of this library came between (independent layers or
+ *                         requests streamed back to back): the gate_up weight stream then runs
+ *                         during the previous layer's split-K tail.  Only for callers whose x is
+ *                         not written by a kernel of their own that lets its dependents start
+ *                         early (programmatic dependent launch) while still writing x.  0 =
+ *                         always wait (default).
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -412,7 +421,8 @@ typedef enum {
     MSE_TUNE_GRID_DOWN = 11,
     MSE_TUNE_CLUSTER_FINISH = 12,
     MSE_TUNE_L2_PREFETCH = 14,
-    MSE_TUNE_SWAPAB_MAX_T = 15
+    MSE_TUNE_SWAPAB_MAX_T = 15,
+    MSE_TUNE_X_EARLY = 16
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

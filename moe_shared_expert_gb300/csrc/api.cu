@@ -21,7 +21,7 @@ std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
     g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
     g_tune_coop_finish{6}, g_tune_pair_min_t{0}, g_tune_grid_down{0}, g_tune_cluster_finish{0},
-    g_tune_l2_prefetch{8}, g_tune_swapab_max_t{160};
+    g_tune_l2_prefetch{8}, g_tune_swapab_max_t{160}, g_tune_x_early{0};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -466,7 +466,7 @@ int std_grid(const DeviceInfo &d, int64_t n_tiles) {
 // gate_up + SiluAndMul over intermediate columns [j_begin, j_begin + width) into h [T x I].
 mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t H, int64_t I,
                       const uint16_t *w_gate_up, int64_t j_begin, int64_t width, uint16_t *h, char *ws,
-                      const MlpWs &L, cudaStream_t s) {
+                      const MlpWs &L, cudaStream_t s, bool x_early = false) {
     CUtensorMap ta, tb;
     mse_status st;
     if (use_swapab(T, 2 * width)) {
@@ -485,6 +485,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         p.ldo = I;
         p.slots = reinterpret_cast<float *>(ws + L.slots_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_gu_off);
+        p.x_early = x_early ? 1 : 0;
         p.err = d.err;
         return from_cuda(tc::launch_swapab(tc::EPI_SWIGLU, ta, tb, p, sh.grid, use_pdl(), sh.pair, s));
     }
@@ -726,6 +727,49 @@ std::mutex g_hostout_mu;
 HostOutput g_hostout[64];
 int g_hostout_n = 0;
 
+// The device ranges that the last mlp_swiglu_forward call on each stream writes (y, its
+// workspace), for MSE_TUNE_X_EARLY: the next call on the stream may read its x before the
+// previous kernel completes when x overlaps neither.  Any other call of this library on the
+// stream forgets the record (its kernels write other ranges).
+struct StreamWrites {
+    void *stream;
+    uintptr_t lo[2], hi[2];
+    bool known;
+};
+StreamWrites g_writes[64];
+int g_writes_n = 0;
+
+StreamWrites *stream_writes(void *stream) {   // caller holds g_hostout_mu
+    for (int i = 0; i < g_writes_n; ++i)
+        if (g_writes[i].stream == stream) return &g_writes[i];
+    if (g_writes_n == 64) g_writes_n = 0;
+    StreamWrites *w = &g_writes[g_writes_n++];
+    w->stream = stream;
+    w->known = false;
+    return w;
+}
+
+bool x_independent_of_last_forward(void *stream, uintptr_t lo, uintptr_t hi) {
+    std::lock_guard<std::mutex> lk(g_hostout_mu);
+    const StreamWrites *w = stream_writes(stream);
+    if (!w->known) return false;
+    for (int k = 0; k < 2; ++k)
+        if (lo < w->hi[k] && w->lo[k] < hi) return false;
+    return true;
+}
+
+void record_forward_writes(void *stream, uintptr_t y_lo, uintptr_t y_hi, uintptr_t ws_lo, uintptr_t ws_hi) {
+    std::lock_guard<std::mutex> lk(g_hostout_mu);
+    StreamWrites *w = stream_writes(stream);
+    w->lo[0] = y_lo; w->hi[0] = y_hi; w->lo[1] = ws_lo; w->hi[1] = ws_hi;
+    w->known = true;
+}
+
+void forget_writes(void *stream) {
+    std::lock_guard<std::mutex> lk(g_hostout_mu);
+    stream_writes(stream)->known = false;
+}
+
 bool host_range_overlaps_last_output(void *stream, uintptr_t lo, uintptr_t hi) {
     std::lock_guard<std::mutex> lk(g_hostout_mu);
     for (int i = 0; i < g_hostout_n; ++i)
@@ -798,6 +842,12 @@ mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h_off);
+    // MSE_TUNE_X_EARLY: x overlaps nothing the previous call on this stream writes (nor this
+    // call's workspace); the record is forgotten until this call's launches succeed
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(workspace);
+    const bool x_early = g_tune_x_early.load() != 0 && !(xa < wa + workspace_bytes && wa < xa + T * H * 2) &&
+                         x_independent_of_last_forward(stream, xa, xa + (uintptr_t)(T * H * 2));
+    forget_writes(stream);
 
     record(g_ev_begin, s);
     if (path == PATH_GENERIC) {
@@ -817,12 +867,14 @@ mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I
                 return st;
             record(g_ev_mid, s);   // one launch: no boundary between the passes
         } else {
-            if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, 0, I, h, ws, L, s)) != MSE_OK) return st;
+            if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, 0, I, h, ws, L, s, x_early)) != MSE_OK) return st;
             record(g_ev_mid, s);
             if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s)) != MSE_OK) return st;
         }
     }
     record(g_ev_end, s);
+    const uintptr_t ya = reinterpret_cast<uintptr_t>(y);
+    record_forward_writes(stream, ya, ya + (uintptr_t)(T * H * 2), wa, wa + workspace_bytes);
     return MSE_OK;
 }
 
@@ -842,6 +894,7 @@ mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int
     DeviceInfo *d = nullptr;
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
+    forget_writes(stream);
     const int64_t sw = I / tp;
     Path path;
     if ((st = choose(mlp_tc_ok(x, H, I, sw, w_gate_up, w_down, partials, workspace), &path)) != MSE_OK) return st;
@@ -896,6 +949,7 @@ mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int
     DeviceInfo *d = nullptr;
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
+    forget_writes(stream);
     const int64_t sw = I / tp;
     Path path;
     if ((st = choose(mlp_tc_ok(x, H, I, sw, w_gate_up, w_down, out, workspace), &path)) != MSE_OK) return st;
@@ -970,6 +1024,7 @@ mse_status mlp_swiglu_forward_host(const mse_bf16 *x_host, int64_t T, int64_t H,
     // of this entry point on the stream writes it
     const bool early = !host_range_overlaps_last_output(stream, xa, xa + nb);
     record_host_output(stream, ya, ya + nb);
+    forget_writes(stream);   // the copy kernel writes this call's x
     if ((st = from_cuda(launch_copy_in(xh, xd, T * H * 2, early, d->sm_count, s))) != MSE_OK) return st;
     // the down projection writes y straight into the caller's host buffer
     return mlp_swiglu_forward(xd, T, H, I, w_gate_up, w_down, static_cast<mse_bf16 *>(yh), y_capacity, ws + act,
@@ -991,6 +1046,7 @@ mse_status shard_sum(const void *partials, mse_dtype partial_dtype, int n_parts,
     DeviceInfo *d = nullptr;
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
+    forget_writes(stream);
     return from_cuda(launch_shard_sum(partials, partial_dtype == MSE_F32, n_parts, T * H, out, d->sm_count,
                                       use_pdl(), static_cast<cudaStream_t>(stream)));
 }
@@ -1009,6 +1065,7 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
     DeviceInfo *d = nullptr;
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
+    forget_writes(stream);
     const bool tc_ok = H % 64 == 0 && aligned16(x) && aligned16(w) && aligned16(workspace);
     Path path;
     if ((st = choose(tc_ok, &path)) != MSE_OK) return st;
@@ -1089,6 +1146,7 @@ mse_status merged_proj_reorder(const mse_bf16 *rank_major, mse_bf16 *logical, in
     DeviceInfo *d = nullptr;
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
+    forget_writes(stream);
     return from_cuda(
         launch_reorder(rank_major, logical, T, q_dim, kv_dim, tp, use_pdl(), static_cast<cudaStream_t>(stream)));
 }
@@ -1140,6 +1198,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_CLUSTER_FINISH: slot = &g_tune_cluster_finish; ok = value == 0 || value == 1; break;
         case MSE_TUNE_L2_PREFETCH: slot = &g_tune_l2_prefetch; ok = value >= 0 && value <= 256; break;
         case MSE_TUNE_SWAPAB_MAX_T: slot = &g_tune_swapab_max_t; ok = value >= 0 && value <= kSwapAbMaxT; break;
+        case MSE_TUNE_X_EARLY: slot = &g_tune_x_early; ok = value == 0 || value == 1; break;
         default: return -1;
     }
     if (!ok) return -1;

@@ -400,7 +400,7 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
     pl.init(p, worker_index<PAIR>(), worker_count<PAIR>());
     StageIter w;
     w.start(pl);
-    if (pdl_prologue) {
+    if (pdl_prologue && !p.x_early) {
         // the ring is fresh: stages 0.. in their first use
         StageIter a = w;
         int st = 0;

@@ -45,6 +45,9 @@ struct SwapAbParams {
                            // wait for the previous kernel, by CTAs with blockIdx >= l2_prefetch_from
     int l2_prefetch_from;  // (CTAs dispatched after the SMs that were idle at launch: they start
                            // while the previous kernel's tail leaves HBM underused)
+    int x_early;           // gate_up: the token operand is not written by the previous kernel on the
+                           // stream, so the producer requests it without waiting for that kernel
+                           // (the epilogue still waits before any store)
     int T;                 // valid tokens
     int64_t m_valid;       // valid output features (A rows) for masking
     void *out; int64_t ldo; int64_t o_group_stride;
