@@ -302,9 +302,12 @@ def one_launch_active() -> bool:
 # Library options for the decode leg.  The workload's x is a buffer that no kernel writes
 # and each step's y and workspace are the same buffers, so a step's x never overlaps what
 # the previous step writes: MSE_TUNE_X_EARLY lets each layer's gate_up weight stream start
-# during the previous layer's split-K tail; with it, 12 k-blocks of L2 prefetch measured best.
-# The time with the library's default settings is reported beside the headline.
-DECODE_TUNING = "x_early=1,l2_prefetch=12"
+# during the previous layer's split-K tail; with it, 12 k-blocks of L2 prefetch measured best,
+# and MSE_TUNE_DOWN_FLAGS (the down kernel starts on each h block as soon as the gate_up
+# kernel publishes it) took the layer from 53.6 to 50.2 us.  The time with the library's
+# default settings is reported beside the headline.
+DECODE_TUNING = "x_early=1,l2_prefetch=12,down_flags=1"
+LIBRARY_DEFAULTS = (("x_early", 0), ("l2_prefetch", 8), ("down_flags", 0))
 
 
 def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=None, spread_steps=2000,
@@ -354,7 +357,7 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
     default_s = None
     if default_steps:
         saved = {k: mse.set_tuning(getattr(mse, "TUNE_" + k.upper()), d)
-                 for k, d in (("x_early", 0), ("l2_prefetch", 8))}
+                 for k, d in LIBRARY_DEFAULTS}
         for i in range(Wm):
             step(i)
         torch.cuda.synchronize()
@@ -943,7 +946,7 @@ def gpu_arm(args):
     if r.get("default_s"):
         line["us_per_layer_library_defaults"] = r["default_s"] * 1e6
         line["library_defaults"] = (f"{r['default_K']} steps timed the same way with the library's default "
-                                    f"settings (x_early=0, l2_prefetch=8)")
+                                    f"settings ({', '.join(f'{k}={v}' for k, v in LIBRARY_DEFAULTS)})")
     if r["chunk_s"]:
         line["us_per_layer_p10_p50_p90"] = [v * 1e6 for v in percentiles(r["chunk_s"])]
         line["us_per_layer_spread"] = (f"per-step time of {len(r['chunk_s'])} consecutive chunks of a separate "

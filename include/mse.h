@@ -406,6 +406,11 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         not written by a kernel of their own that lets its dependents start
  *                         early (programmatic dependent launch) while still writing x.  0 =
  *                         always wait (default).
+ *   MSE_TUNE_DOWN_FLAGS   decode token counts, two launches per layer: 1 = the gate_up kernel sets
+ *                         a flag per finished 64-column block of h, and each CTA of the down
+ *                         kernel, instead of waiting for the gate_up grid to complete, waits
+ *                         until the flags of every h block it reads are set (its epilogue still
+ *                         waits for the gate_up grid before any store); 0 = off (default)
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -422,7 +427,8 @@ typedef enum {
     MSE_TUNE_CLUSTER_FINISH = 12,
     MSE_TUNE_L2_PREFETCH = 14,
     MSE_TUNE_SWAPAB_MAX_T = 15,
-    MSE_TUNE_X_EARLY = 16
+    MSE_TUNE_X_EARLY = 16,
+    MSE_TUNE_DOWN_FLAGS = 17
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

@@ -21,7 +21,7 @@ std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
     g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
     g_tune_coop_finish{6}, g_tune_pair_min_t{0}, g_tune_grid_down{0}, g_tune_cluster_finish{0},
-    g_tune_l2_prefetch{8}, g_tune_swapab_max_t{160}, g_tune_x_early{0};
+    g_tune_l2_prefetch{8}, g_tune_swapab_max_t{160}, g_tune_x_early{0}, g_tune_down_flags{0};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -464,9 +464,16 @@ int std_grid(const DeviceInfo &d, int64_t n_tiles) {
 }
 
 // gate_up + SiluAndMul over intermediate columns [j_begin, j_begin + width) into h [T x I].
+// Whether the two swap-AB launches of a decode-size layer hand h over by per-block flags
+// (MSE_TUNE_DOWN_FLAGS): both launches single-CTA and the gate_up launch without cluster
+// finish (every other way of finishing a gate_up tile publishes it: the CTA that owns it
+// whole, the last of its parts to arrive, or the last of its joint finishers).  Returns the
+// epoch the flags of this call carry, or 0 for no flags.
+int down_flags_epoch(const DeviceInfo &d, int64_t T, int64_t H, int64_t width, int64_t s_width, int groups);
+
 mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t H, int64_t I,
                       const uint16_t *w_gate_up, int64_t j_begin, int64_t width, uint16_t *h, char *ws,
-                      const MlpWs &L, cudaStream_t s, bool x_early = false) {
+                      const MlpWs &L, cudaStream_t s, bool x_early = false, int flags = 0) {
     CUtensorMap ta, tb;
     mse_status st;
     if (use_swapab(T, 2 * width)) {
@@ -486,6 +493,10 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         p.slots = reinterpret_cast<float *>(ws + L.slots_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_gu_off);
         p.x_early = x_early ? 1 : 0;
+        if (flags) {
+            p.hflags = reinterpret_cast<int *>(ws + L.flags_off);
+            p.hflag_epoch = flags;
+        }
         p.err = d.err;
         return from_cuda(tc::launch_swapab(tc::EPI_SWIGLU, ta, tb, p, sh.grid, use_pdl(), sh.pair, s));
     }
@@ -528,7 +539,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
 // intermediate columns starting at column kcol0 + g * s_width.
 mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H, int64_t I, const uint16_t *w_down,
                    int64_t kcol0, int64_t s_width, int groups, void *out, int epi, char *ws, const MlpWs &L,
-                   cudaStream_t s) {
+                   cudaStream_t s, int flags = 0) {
     CUtensorMap ta, tb;
     mse_status st;
     // the same choice as the layer's gate_up launch (its rows: 2 x the intermediate columns)
@@ -548,6 +559,13 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
         p.o_group_stride = T * H;
         p.slots = reinterpret_cast<float *>(ws + L.slots_dn_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_dn_off);
+        if (flags) {
+            p.hflags = reinterpret_cast<int *>(ws + L.flags_off);
+            p.exit_count = reinterpret_cast<int *>(ws + L.exit_off);
+            p.hflag_first = (int)(kcol0 / 64);
+            p.hflag_n = (int)((int64_t)groups * s_width / 64);
+            p.hflag_epoch = flags;
+        }
         p.err = d.err;
         return from_cuda(tc::launch_swapab(epi, ta, tb, p, sh.grid, use_pdl(), sh.pair, s));
     }
@@ -664,6 +682,18 @@ mse_status tc_mlp_one_launch(const DeviceInfo &d, const uint16_t *x, int64_t T, 
 }
 
 bool one_launch_enabled(int64_t T) { return T <= kSwapAbMaxT && g_tune_one_launch.load() != 0; }
+
+std::atomic<uint32_t> g_epoch{0};
+
+int down_flags_epoch(const DeviceInfo &d, int64_t T, int64_t H, int64_t width, int64_t s_width, int groups) {
+    if (g_tune_down_flags.load() == 0 || !use_pdl() || !use_swapab(T, 2 * width)) return 0;
+    SwapAbShape gu = swapab_shape(d, T, (int)(width / 64), 1, (int)(H / 64), false, true);
+    if (gu.pair || gu.p.cluster_finish) return 0;
+    const SwapAbShape dn = swapab_shape(d, T, (int)((H + 127) / 128), groups, (int)(s_width / 64), true, true);
+    if (dn.pair) return 0;
+    // positive, and different from the previous call's
+    return (int)(g_epoch.fetch_add(1) % 0x7ffffffeu) + 1;
+}
 
 // ----------------------------------------------------------------- path choice
 enum Path { PATH_GENERIC, PATH_TC };
@@ -867,9 +897,10 @@ mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I
                 return st;
             record(g_ev_mid, s);   // one launch: no boundary between the passes
         } else {
-            if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, 0, I, h, ws, L, s, x_early)) != MSE_OK) return st;
+            const int fl = down_flags_epoch(*d, T, H, I, I, 1);
+            if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, 0, I, h, ws, L, s, x_early, fl)) != MSE_OK) return st;
             record(g_ev_mid, s);
-            if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s)) != MSE_OK) return st;
+            if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s, fl)) != MSE_OK) return st;
         }
     }
     record(g_ev_end, s);
@@ -925,9 +956,11 @@ mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int
         if (st != MSE_OK) return st;
         record(g_ev_mid, s);
     } else {
-        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s)) != MSE_OK) return st;
+        const int fl = down_flags_epoch(*d, T, H, width, sw, rank_count);
+        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s, false, fl)) != MSE_OK) return st;
         record(g_ev_mid, s);
-        if ((st = tc_down(*d, h, T, H, I, w_down, j0, sw, rank_count, partials, epi, ws, L, s)) != MSE_OK) return st;
+        if ((st = tc_down(*d, h, T, H, I, w_down, j0, sw, rank_count, partials, epi, ws, L, s, fl)) != MSE_OK)
+            return st;
     }
     record(g_ev_end, s);
     return MSE_OK;
@@ -980,9 +1013,10 @@ mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int
             return st;
         record(g_ev_mid, s);
     } else {
-        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s)) != MSE_OK) return st;
+        const int fl = down_flags_epoch(*d, T, H, width, width, 1);
+        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s, false, fl)) != MSE_OK) return st;
         record(g_ev_mid, s);
-        if ((st = tc_down(*d, h, T, H, I, w_down, j0, width, 1, out, epi, ws, L, s)) != MSE_OK) return st;
+        if ((st = tc_down(*d, h, T, H, I, w_down, j0, width, 1, out, epi, ws, L, s, fl)) != MSE_OK) return st;
     }
     record(g_ev_end, s);
     return MSE_OK;
@@ -1199,6 +1233,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_L2_PREFETCH: slot = &g_tune_l2_prefetch; ok = value >= 0 && value <= 256; break;
         case MSE_TUNE_SWAPAB_MAX_T: slot = &g_tune_swapab_max_t; ok = value >= 0 && value <= kSwapAbMaxT; break;
         case MSE_TUNE_X_EARLY: slot = &g_tune_x_early; ok = value == 0 || value == 1; break;
+        case MSE_TUNE_DOWN_FLAGS: slot = &g_tune_down_flags; ok = value == 0 || value == 1; break;
         default: return -1;
     }
     if (!ok) return -1;

@@ -38,6 +38,7 @@ struct Ctrl {
     uint64_t fixbar;         // swap-AB finisher: bulk copies of partial tiles into shared memory
     uint64_t go_bar;         // swap-AB cluster finish: the receiving CTA's ring is free
     uint64_t recv_bar;       // swap-AB cluster finish: the sending CTA's part has landed
+    uint64_t hready_bar;     // swap-AB down with h flags: every h block the CTA reads is published
     uint32_t tmem_base;
     int abort_flag;
     int fin_flag;
@@ -426,11 +427,23 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
                 left -= n;
             }
         }
-        pdl_wait();
+        bool flags_ok = true;
+        if (EPI != EPI_SWIGLU && p.hflags) {
+            // the epilogue warps poll the flags of every h block this CTA reads (no wait for
+            // the gate_up grid to complete) and arrive here once all are published
+            flags_ok = mbar_wait_bounded(bar_addr(&ctl->hready_bar), 0u, abort_flag, p.wait_limit_ns, p.err);
+            fence_proxy_async_global();   // h was written through the generic proxy
+        } else {
+            pdl_wait();
+        }
         for (int t = 0; t < st; ++t) {
             const int n = w.count(KBS);
             load_b(w, n, t);
             w.advance(n);
+        }
+        if (!flags_ok) {
+            issued += st;
+            return false;
         }
         issued += st;
         r.stage = st == S ? 0 : st;
@@ -684,12 +697,13 @@ __device__ bool finish_cols_smem(const SwapAbParams &p, Ctrl *ctl, float *ring, 
 // Publication of a finished gate_up tile (m) for readers of h in the same launch: every
 // epilogue thread's h stores, then GPU-scope releases of the tile's flag and of the
 // pass's count of published tiles.
-__device__ __forceinline__ void publish_h_tile(const SwapAbParams &p, int *hflags, int *hcount, int m) {
+__device__ __forceinline__ void publish_h_tile(const SwapAbParams &p, int *hflags, int *hcount, int m,
+                                               int epoch = 1) {
     fence_proxy_async_global();
     named_barrier_sync(1, 128);
     if (threadIdx.x == 64) {
-        st_release_gpu(hflags + p.a_row_base / 64 + m, 1);
-        red_add_release_gpu(hcount, 1);
+        st_release_gpu(hflags + p.a_row_base / 64 + m, epoch);
+        if (hcount) red_add_release_gpu(hcount, 1);
     }
 }
 
@@ -758,7 +772,7 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
                 swapab_epilogue_chunk<EPI>(p, ctl, group, m, q, lane, c, v);
             }
             release(buf);
-            if (hflags) publish_h_tile(p, hflags, hcount, m);
+            if (hflags) publish_h_tile(p, hflags, hcount, m, p.hflag_epoch > 0 ? p.hflag_epoch : 1);
             continue;
         }
         // Clustered finish of two-part tiles (clusters of three CTAs covering two tiles
@@ -931,9 +945,21 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
             if (col1 > col0 && !finish_cols_smem<EPI>(p, ctl, reinterpret_cast<float *>(ring), ring_base, ring_bytes,
                                                        fix_round, nseg, col0, col1, group, m, tid, abort_flag))
                 return false;
+            if (hflags) {
+                // every epilogue thread's h stores precede this CTA's count below
+                fence_proxy_async_global();
+                named_barrier_sync(1, 128);
+            }
             if (threadIdx.x == 64) {
-                // every finisher is past its wait once all have counted themselves here
-                if (atomic_add_acq_rel_gpu(p.counters + ctile, 1) == nseg + n_fin - 1) p.counters[ctile] = 0;
+                // every finisher is past its wait once all have counted themselves here; the
+                // last one to count (acquiring every other finisher's slice) publishes the tile
+                if (atomic_add_acq_rel_gpu(p.counters + ctile, 1) == nseg + n_fin - 1) {
+                    p.counters[ctile] = 0;
+                    if (hflags) {
+                        st_release_gpu(hflags + p.a_row_base / 64 + m, p.hflag_epoch > 0 ? p.hflag_epoch : 1);
+                        if (hcount) red_add_release_gpu(hcount, 1);
+                    }
+                }
             }
             named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
             continue;
@@ -1004,7 +1030,7 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
             }
         }
         if (threadIdx.x == 64) p.counters[ctile] = 0;
-        if (hflags) publish_h_tile(p, hflags, hcount, m);
+        if (hflags) publish_h_tile(p, hflags, hcount, m, p.hflag_epoch > 0 ? p.hflag_epoch : 1);
         named_barrier_sync(1, 128);   // fin_flag is reused by the next tile
     }
     return true;
@@ -1031,6 +1057,7 @@ __device__ __forceinline__ void swapab_setup(Ctrl *ctl, int S, int tmem_cols, co
         mbar_init(bar_addr(&ctl->fixbar), 1);
         mbar_init(bar_addr(&ctl->go_bar), 1);
         mbar_init(bar_addr(&ctl->recv_bar), 1);
+        mbar_init(bar_addr(&ctl->hready_bar), 1);
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
@@ -1104,7 +1131,11 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
     swapab_setup<PAIR>(ctl, S, p.tmem_cols, maps, 2, clustered);
     const uint32_t tmem_base = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort_flag;
-    pdl_launch_dependents();
+    // gate_up that publishes h flags lets the down grid launch only once the previous grid on
+    // the stream (the previous call's down kernel, which clears the flags) is complete: no down
+    // CTA can see a flag that the previous call left behind
+    const bool late_trigger = EPI == EPI_SWIGLU && p.hflags != nullptr;
+    if (!late_trigger) pdl_launch_dependents();
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     int issued = 0;
@@ -1120,11 +1151,58 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
             (void)swapab_mma<PAIR>(p, ctl, sm, r, gseg, tmem_base, abort_flag);
         }
     } else {
+        if (EPI != EPI_SWIGLU && p.hflags) {
+            // the h blocks of every stage of this CTA: one flag per thread per round (an acquire
+            // load at most every 0.2 us), a CTA barrier once every flag is seen, then one arrival
+            // releases the producer's token loads
+            const int tid = threadIdx.x - 64;
+            Plan pl;
+            pl.init(p, worker_index<PAIR>(), worker_count<PAIR>());
+            const uint64_t t0 = global_timer_ns();
+            bool ok = true;
+            while (true) {
+                bool mine = true;
+                int base = 0;
+                for (int sg = 0; sg < pl.nseg; ++sg) {
+                    int64_t tile;
+                    int kb0, kb1;
+                    pl.seg_range(sg, tile, kb0, kb1);
+                    const int group = (int)(tile / p.n_mtiles);
+                    for (int kb = kb0 + ((tid - base) % 128 + 128) % 128; kb < kb1; kb += 128)
+                        mine &= ld_acquire_gpu(p.hflags + p.kb_first + group * p.kb_group_stride + kb) ==
+                                p.hflag_epoch;
+                    base += kb1 - kb0;
+                }
+                const bool timed_out = global_timer_ns() - t0 > p.wait_limit_ns || *abort_flag;
+                if (named_barrier_and(1, 128, mine)) break;
+                if (named_barrier_and(1, 128, !timed_out) == false) { ok = false; break; }
+                __nanosleep(200);
+            }
+            if (threadIdx.x == 64) {
+                if (ok) {
+                    mbar_arrive(bar_addr(&ctl->hready_bar));
+                    // Every flag is read by some CTA, so once all CTAs are past their polls the
+                    // gate_up grid has published every flag and no one reads them any more:
+                    // the last CTA here clears them (while the grid still runs, not at its end)
+                    if (atomic_add_acq_rel_gpu(p.exit_count, 1) == (int)gridDim.x - 1) {
+                        for (int t = 0; t < p.hflag_n; ++t) p.hflags[p.hflag_first + t] = 0;
+                        *p.exit_count = 0;
+                    }
+                } else if (!*abort_flag) {
+                    *abort_flag = 1;
+                    raise_device_error(p.err, DEV_ERR_TIMEOUT);
+                }
+            }
+        }
         pdl_wait();
+        if (late_trigger && threadIdx.x == 64) pdl_launch_dependents();
         int gseg = 0;
         uint32_t fix_round = 0;
+        // (the epilogue waits for the previous grid even where the producer does not: no output or
+        // split-K slot is written before the gate_up grid is complete)
         (void)swapab_epilogue<EPI, PAIR, COOP>(p, ctl, ring, base, (uint32_t)S * sm.stage_bytes, gseg, fix_round,
-                                               tmem_base, true, nullptr, nullptr, abort_flag);
+                                               tmem_base, true, EPI == EPI_SWIGLU ? p.hflags : nullptr, nullptr,
+                                               abort_flag);
     }
     swapab_teardown<PAIR>(ctl, S, issued, tmem_base, p.tmem_cols, p.wait_limit_ns, clustered);
 }
@@ -1697,7 +1775,7 @@ int swapab_stages_for(int bn, int kbs) {
 int std_stages() { return 4; }
 
 // Largest number of CTAs any tile of a single-CTA stream-K launch is split between.
-static int swapab_max_parts(const SwapAbParams &p, int grid) {
+int swapab_max_parts(const SwapAbParams &p, int grid) {
     const int64_t U = p.total_units, kbp = p.kb_per_tile;
     if (U <= 0 || kbp <= 0 || grid <= 0) return 1;
     const int64_t n_tiles = U / kbp;

@@ -54,6 +54,19 @@ struct SwapAbParams {
     uint16_t *out_rm; int64_t q_dim, kv_dim; int tp;   // EPI_MERGED
     float *slots;          // split-K partial tiles: 2 per CTA, 128 x bn fp32 each
     int *counters;         // one per tile; zero on entry, left zero on exit
+    // h handed between the two launches of a layer by per-block flags (null: not used).
+    // gate_up (EPI_SWIGLU): the flag of h column block a_row_base / 64 + m is set to
+    //   hflag_epoch once that tile is written; the launch lets its dependent grid start only
+    //   after waiting for the previous grid on the stream (the previous call's down kernel,
+    //   which clears the flags), so the down kernel never sees the previous call's flags.
+    // down: its epilogue warps poll, once, the flags of every h block the CTA reads until they
+    //   equal hflag_epoch, and then release the producer's token loads (instead of waiting for
+    //   the gate_up grid to complete); the last CTA past its poll (exit_count) clears the
+    //   flags [hflag_first, hflag_first + hflag_n) and exit_count.  The epoch also differs between
+    //   consecutive calls made outside graphs.
+    int *hflags;
+    int *exit_count;
+    int hflag_first, hflag_n, hflag_epoch;
     uint64_t wait_limit_ns;
     uint32_t *err;
 };
@@ -111,6 +124,9 @@ int std_stages();
 cudaError_t launch_swapab(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const SwapAbParams &p, int grid,
                           bool pdl, bool pair, cudaStream_t s);
 int swapab_pair_max_clusters(int bn, int stages, int kbs);
+// Largest number of CTAs any tile of a single-CTA stream-K launch of `grid` CTAs is split
+// between (the launch takes the joint-finish kernel from coop_finish parts on).
+int swapab_max_parts(const SwapAbParams &p, int grid);
 // clusters of three single CTAs of the swap-AB kernel resident at once (0 on failure)
 int swapab_trio_max_clusters(int bn, int stages, int kbs);
 // The one-launch decode layer (grid <= SMs, one CTA per SM).

@@ -1,8 +1,11 @@
-"""MSE_TUNE_X_EARLY: mlp_swiglu_forward reads x without waiting for the previous kernel on
-the stream when x overlaps neither the y nor the workspace of the previous call on that
-stream.  Independent calls streamed back to back, and layers chained through device memory
-(x of a call is the previous call's y: the library sees the overlap and waits), must give
-exactly what the default path gives."""
+"""The two options that relax the waits between kernels of consecutive decode layers:
+MSE_TUNE_X_EARLY (x read without waiting for the previous kernel when x overlaps nothing the
+previous call on the stream writes) and MSE_TUNE_DOWN_FLAGS (the down kernel waits for the
+flags of the h blocks it reads instead of the whole gate_up grid; the flags carry a per-call
+epoch and are cleared by the down kernel's last CTA).  Independent calls streamed back to
+back, layers chained through device memory (x of a call is the previous call's y: the
+library sees the overlap and waits) and CUDA-graph replays (the same epochs replayed) must
+give exactly what the default path gives."""
 import math
 
 import pytest
@@ -27,16 +30,19 @@ def _lib():
     assert mse.poll_device_error() == 0
 
 
-def with_x_early(v, fn):
-    old = mse.set_tuning(mse.TUNE_X_EARLY, v)
+def with_options(x_early, down_flags, fn):
+    o1 = mse.set_tuning(mse.TUNE_X_EARLY, x_early)
+    o2 = mse.set_tuning(mse.TUNE_DOWN_FLAGS, down_flags)
     try:
         return fn()
     finally:
-        mse.set_tuning(mse.TUNE_X_EARLY, old)
+        mse.set_tuning(mse.TUNE_X_EARLY, o1)
+        mse.set_tuning(mse.TUNE_DOWN_FLAGS, o2)
 
 
+@pytest.mark.parametrize("opts", [(1, 0), (0, 1), (1, 1)])
 @pytest.mark.parametrize("T", [64, 16])
-def test_x_early_independent_and_chained_calls(T):
+def test_options_independent_chained_and_replayed_calls(T, opts):
     w = W.DECODE_T64
     wgu, wd = W.make_mlp_weights(w)
     g0, d0 = to_dev(wgu), to_dev(wd)
@@ -59,10 +65,85 @@ def test_x_early_independent_and_chained_calls(T):
         torch.cuda.synchronize()
         return outs[1:]
 
-    ref_i, ref_c = with_x_early(0, independent), with_x_early(0, chained)
-    got_i, got_c = with_x_early(1, independent), with_x_early(1, chained)
+    def replayed():
+        side = torch.cuda.Stream()
+        outs = [torch.empty((T, w.H), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for k in range(3):
+                mse.mlp_swiglu_forward(xs[k], gus[k % 2], wds[k % 2], y=outs[k], workspace=ws, stream=side)
+        res = []
+        for _ in range(4):
+            for o in outs:
+                o.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            res.append([o.clone() for o in outs])
+        return res
+
+    ref_i, ref_c = with_options(0, 0, independent), with_options(0, 0, chained)
+    got_i, got_c = with_options(*opts, independent), with_options(*opts, chained)
+    got_r = with_options(*opts, replayed)
     for i, (a, b) in enumerate(zip(got_i, ref_i)):
         assert torch.equal(a, b), f"independent call {i}"
     for i, (a, b) in enumerate(zip(got_c, ref_c)):
         assert torch.equal(a, b), f"chained layer {i}"
+    for r in got_r:
+        for k in range(3):
+            assert torch.equal(r[k], ref_i[k]), f"graph call {k}"
     assert mse.poll_device_error() == 0
+    off, b = mse.mlp_swiglu_workspace_sync_range(T, w.H, w.I, ws.numel())
+    assert int(torch.count_nonzero(ws[off:off + b]).item()) == 0   # the flags were cleared
+
+
+@pytest.mark.parametrize("tp,rank_count", [(4, 1), (8, 1), (16, 1), (8, 2), (8, 8)])
+@pytest.mark.parametrize("T", [64, 16])
+def test_down_flags_shard_entry_points(T, tp, rank_count):
+    """One rank's (or a group of ranks') shard launches with the flag handover: narrow gate_up
+    slices whose tiles are finished jointly by several CTAs (each finisher one slice of token
+    columns) must publish their h blocks too.  Ranks cycled back to back, eagerly and in a
+    replayed graph, give exactly the results without flags; the sync words end zero."""
+    w = W.DECODE_T64
+    wgu, wd = W.make_mlp_weights(w)
+    g0, d0 = to_dev(wgu), to_dev(wd)
+    x = to_dev(W.make_custom(2100 + T, 0, (T, w.H)))
+    ws = mse.new_mlp_workspace(T, w.H, w.I)
+    firsts = list(range(0, tp - rank_count + 1, rank_count))
+
+    def eager():
+        outs = []
+        for _ in range(2):
+            for r in firsts:
+                outs.append(mse.mlp_swiglu_shard_partial(x, g0, d0, tp, r, rank_count, workspace=ws))
+                outs.append(mse.mlp_swiglu_shard_forward(x, g0, d0, tp, r, rank_count, workspace=ws))
+        torch.cuda.synchronize()
+        return outs
+
+    def replayed():
+        side = torch.cuda.Stream()
+        parts = [torch.empty((rank_count, T, w.H), dtype=torch.bfloat16, device="cuda") for _ in firsts]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for r, pt in zip(firsts, parts):
+                mse.mlp_swiglu_shard_partial(x, g0, d0, tp, r, rank_count, partials=pt, workspace=ws, stream=side)
+        res = []
+        for _ in range(3):
+            for pt in parts:
+                pt.zero_()
+            g.replay()
+            g.replay()
+            torch.cuda.synchronize()
+            res.append([pt.clone() for pt in parts])
+        return res
+
+    ref = with_options(0, 0, eager)
+    got = with_options(0, 1, eager)
+    got_r = with_options(0, 1, replayed)
+    for i, (a, b) in enumerate(zip(got, ref)):
+        assert torch.equal(a, b), f"eager call {i}"
+    for r in got_r:
+        for k in range(len(firsts)):
+            assert torch.equal(r[k], ref[2 * k]), f"graph rank group {k}"   # eager order: partial, forward
+    assert mse.poll_device_error() == 0
+    off, b = mse.mlp_swiglu_workspace_sync_range(T, w.H, w.I, ws.numel())
+    assert int(torch.count_nonzero(ws[off:off + b]).item()) == 0
