@@ -390,8 +390,9 @@ def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=No
     layer_ms = [e[0].elapsed_time(e[2]) for e in evs]
 
     # end to end through the public API with host buffers: mlp_swiglu_forward_host reads x
-    # from and writes y to page-locked host memory every step (a copy kernel and the
-    # layer's kernels, all chained by programmatic dependent launch)
+    # from and writes y to page-locked host memory every step (the gate_up kernel copies x
+    # from host memory itself, the down kernel writes y there; chained by programmatic
+    # dependent launch)
     # at least 200 steps, so that start-up and the final synchronisation do not dominate
     n_e2e = e2e_steps if e2e_steps is not None else min(max(K, 200), 2000)
     xh = torch.from_numpy(W.make_x(w).view(np.int16)).view(torch.bfloat16).pin_memory()

@@ -306,18 +306,24 @@ MSE_API mse_status mlp_swiglu_forward_static_scratch(const mse_bf16 *x, int64_t 
  *   y_host  [T x H] bf16, the same kind of memory, y_capacity >= T*H elements
  *   w_gate_up, w_down  device memory, as for mlp_swiglu_forward
  *   workspace  device memory of mlp_swiglu_host_workspace_bytes(T, H, I) bytes, 256-byte
- *           aligned, zero before first use: a device copy of x, then the workspace of
- *           mlp_swiglu_forward (same rules for reuse)
+ *           aligned, zero before first use: 256 bytes of copy counts, two device copies of
+ *           x, then the workspace of mlp_swiglu_forward (same rules for reuse)
  *
- * Three kernels on `stream`, each launched with programmatic dependent launch, so that
- * none of them cuts the overlap of consecutive calls: a copy of x into the workspace, and
- * the two kernels of the layer, the down projection writing y straight into y_host.  The
- * copy reads x while the previous work on the stream still runs, unless x overlaps the
- * y_host of the previous call of this entry point on the same stream (layers chained
- * through host memory): then it reads after that work is complete.  y_host holds the result once the stream has reached
- * the end of the call (e.g. after cudaStreamSynchronize); the host must not modify x or
- * read y before then.  MSE_ERR_INVALID_ARG if a host pointer is not mapped page-locked
- * memory or the two buffers overlap.
+ * The kernels are launched on `stream` with programmatic dependent launch, so that none of
+ * them cuts the overlap of consecutive calls; the down projection writes y straight into
+ * y_host.  On the decode-size (swap-AB) kernels the gate_up launch copies x itself: the
+ * CTAs that start first (on the SMs the previous layer's down projection leaves free; at
+ * most MSE_TUNE_HOST_X_COPIERS) copy one slice each into one of the two device copies, the
+ * other one than the previous call on this workspace, and every CTA's token loads wait for
+ * all slices.  Elsewhere a copy kernel into the first device copy runs before the layer.
+ * x is read while the previous work on the stream still runs, unless x overlaps the y_host
+ * of the previous call of this entry point on the same stream (layers chained through host
+ * memory), or the previous call on this workspace is unknown (the first, one with another T
+ * or H, one on another path, or one captured into a CUDA graph; calls during capture always
+ * wait): then it is read once that work is complete.  y_host holds the result once the
+ * stream has reached the end of the call (e.g. after cudaStreamSynchronize); the host must
+ * not modify x or read y before then.  MSE_ERR_INVALID_ARG if a host pointer is not mapped
+ * page-locked memory or the two buffers overlap.
  * ------------------------------------------------------------------------- */
 MSE_API size_t mlp_swiglu_host_workspace_bytes(int64_t T, int64_t H, int64_t I);
 MSE_API mse_status mlp_swiglu_forward_host(const mse_bf16 *x_host, int64_t T, int64_t H, int64_t I,
@@ -411,6 +417,10 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         kernel, instead of waiting for the gate_up grid to complete, waits
  *                         until the flags of every h block it reads are set (its epilogue still
  *                         waits for the gate_up grid before any store); 0 = off (default)
+ *   MSE_TUNE_HOST_X_COPIERS mlp_swiglu_forward_host on the decode-size kernels: the number of
+ *                         CTAs of the gate_up launch that copy a slice of x each from host memory
+ *                         (the first to start; 1 .. 1024, at most the launch's CTAs; default 16);
+ *                         0 = a separate copy kernel before the layer
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -428,7 +438,8 @@ typedef enum {
     MSE_TUNE_L2_PREFETCH = 14,
     MSE_TUNE_SWAPAB_MAX_T = 15,
     MSE_TUNE_X_EARLY = 16,
-    MSE_TUNE_DOWN_FLAGS = 17
+    MSE_TUNE_DOWN_FLAGS = 17,
+    MSE_TUNE_HOST_X_COPIERS = 18
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

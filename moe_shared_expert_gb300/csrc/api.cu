@@ -21,7 +21,8 @@ std::atomic<int> g_prefill{MSE_PREFILL_AUTO};
 std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1}, g_tune_grid{0},
     g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
     g_tune_coop_finish{6}, g_tune_pair_min_t{0}, g_tune_grid_down{0}, g_tune_cluster_finish{0},
-    g_tune_l2_prefetch{8}, g_tune_swapab_max_t{160}, g_tune_x_early{0}, g_tune_down_flags{0};
+    g_tune_l2_prefetch{8}, g_tune_swapab_max_t{160}, g_tune_x_early{0}, g_tune_down_flags{0},
+    g_tune_host_x_copiers{16};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -463,6 +464,16 @@ int std_grid(const DeviceInfo &d, int64_t n_tiles) {
     return (int)(g < n_tiles ? g : n_tiles);
 }
 
+// x of a replicated layer in host memory, copied by the gate_up launch itself
+// (mlp_swiglu_forward_host on the decode-size kernels): the device view of the caller's x,
+// the three copy-count words of this call's buffer, and whether the copy may run before
+// the previous grid on the stream is complete.
+struct HostX {
+    const void *x_host;
+    int *sync;
+    bool early;
+};
+
 // gate_up + SiluAndMul over intermediate columns [j_begin, j_begin + width) into h [T x I].
 // Whether the two swap-AB launches of a decode-size layer hand h over by per-block flags
 // (MSE_TUNE_DOWN_FLAGS): both launches single-CTA and the gate_up launch without cluster
@@ -473,7 +484,8 @@ int down_flags_epoch(const DeviceInfo &d, int64_t T, int64_t H, int64_t width, i
 
 mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t H, int64_t I,
                       const uint16_t *w_gate_up, int64_t j_begin, int64_t width, uint16_t *h, char *ws,
-                      const MlpWs &L, cudaStream_t s, bool x_early = false, int flags = 0) {
+                      const MlpWs &L, cudaStream_t s, bool x_early = false, int flags = 0,
+                      const HostX *hx = nullptr) {
     CUtensorMap ta, tb;
     mse_status st;
     if (use_swapab(T, 2 * width)) {
@@ -497,9 +509,23 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
             p.hflags = reinterpret_cast<int *>(ws + L.flags_off);
             p.hflag_epoch = flags;
         }
+        if (hx) {
+            if (sh.pair) return MSE_ERR_UNSUPPORTED_SHAPE;
+            p.x_host = static_cast<const uint4 *>(hx->x_host);
+            p.x_copy = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(x));
+            p.x_vecs = T * H * 2 / 16;
+            p.x_sync = hx->sync;
+            // the copiers should be CTAs that start while the previous layer's down kernel
+            // still runs: at most the SMs that launch leaves free (its shape is this layer's)
+            const SwapAbShape dn = swapab_shape(d, T, (int)((H + 127) / 128), 1, (int)(I / 64), true, true);
+            const int free_sms = std::max(1, d.sm_count - dn.grid * (dn.pair ? 2 : 1));
+            p.x_copiers = std::min({sh.grid, g_tune_host_x_copiers.load(), free_sms});
+            p.x_copy_early = hx->early ? 1 : 0;
+        }
         p.err = d.err;
         return from_cuda(tc::launch_swapab(tc::EPI_SWIGLU, ta, tb, p, sh.grid, use_pdl(), sh.pair, s));
     }
+    if (hx) return MSE_ERR_UNSUPPORTED_SHAPE;
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
         p.stages = tc::pair_stages();
@@ -683,6 +709,13 @@ mse_status tc_mlp_one_launch(const DeviceInfo &d, const uint16_t *x, int64_t T, 
 
 bool one_launch_enabled(int64_t T) { return T <= kSwapAbMaxT && g_tune_one_launch.load() != 0; }
 
+// Whether the gate_up launch of a replicated layer of T tokens copies x from host memory
+// itself: the single-CTA swap-AB kernels of the two-launch layer.
+bool hostx_supported(const DeviceInfo &d, int64_t T, int64_t H, int64_t I) {
+    if (one_launch_enabled(T) || !use_swapab(T, 2 * I)) return false;
+    return !swapab_shape(d, T, (int)(I / 64), 1, (int)(H / 64), false, true).pair;
+}
+
 std::atomic<uint32_t> g_epoch{0};
 
 int down_flags_epoch(const DeviceInfo &d, int64_t T, int64_t H, int64_t width, int64_t s_width, int groups) {
@@ -817,6 +850,119 @@ void record_host_output(void *stream, uintptr_t lo, uintptr_t hi) {
 }  // namespace
 }  // namespace mse
 
+// Workspace of mlp_swiglu_forward_host: the copy-count words of the two x buffers (fixed
+// place, whatever T), the two device copies of x, then the workspace of the layer.
+struct HostWs {
+    size_t sync_off, x_off[2], mlp_off;
+};
+HostWs host_ws_layout(int64_t T, int64_t H) {
+    const size_t act = align_up((size_t)T * (size_t)H * 2, 256);
+    HostWs w;
+    w.sync_off = 0;
+    w.x_off[0] = 256;
+    w.x_off[1] = 256 + act;
+    w.mlp_off = 256 + 2 * act;
+    return w;
+}
+
+// Which x buffer each host workspace used last (per workspace, in call order; a small table).
+// A call takes the other buffer, and may copy early, only when the previous call on that
+// workspace is known, had the same T and H, and was not captured into a graph.
+struct XBufState {
+    const void *ws;
+    int64_t T, H;
+    int buffer;
+};
+std::mutex g_xbuf_mu;
+XBufState g_xbuf[16];
+int g_xbuf_next = 0;
+
+int next_x_buffer(const void *ws, int64_t T, int64_t H, bool capturing, bool *alternate) {
+    std::lock_guard<std::mutex> lk(g_xbuf_mu);
+    *alternate = false;
+    XBufState *e = nullptr;
+    for (auto &x : g_xbuf)
+        if (x.ws == ws) e = &x;
+    if (capturing) {
+        if (e) e->ws = nullptr;
+        return 0;
+    }
+    if (e && e->T == T && e->H == H) {
+        e->buffer ^= 1;
+        *alternate = true;
+        return e->buffer;
+    }
+    if (!e) {
+        e = &g_xbuf[g_xbuf_next];
+        g_xbuf_next = (g_xbuf_next + 1) % 16;
+    }
+    *e = {ws, T, H, 0};
+    return 0;
+}
+
+void forget_x_buffer(const void *ws) {
+    std::lock_guard<std::mutex> lk(g_xbuf_mu);
+    for (auto &x : g_xbuf)
+        if (x.ws == ws) x.ws = nullptr;
+}
+
+// The replicated layer (mlp_swiglu_forward); hx: gate_up copies x from host memory into
+// the device buffer x (mlp_swiglu_forward_host, decode-size kernels only).
+mse_status forward_impl(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, const mse_bf16 *w_gate_up,
+                        const mse_bf16 *w_down, mse_bf16 *y, int64_t y_capacity, void *workspace,
+                        size_t workspace_bytes, void *stream, const HostX *hx) {
+    if (!x || !w_gate_up || !w_down || !y || T <= 0 || H <= 0 || I <= 0) return MSE_ERR_INVALID_ARG;
+    if (y_capacity < T * H) return MSE_ERR_GEOMETRY;
+    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes);
+    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MSE_ERR_WORKSPACE;
+    DeviceInfo *d = nullptr;
+    mse_status st = current_device(&d);
+    if (st != MSE_OK) return st;
+    Path path;
+    if ((st = choose(mlp_tc_ok(x, H, I, I, w_gate_up, w_down, y, workspace), &path)) != MSE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h_off);
+    // MSE_TUNE_X_EARLY: x overlaps nothing the previous call on this stream writes (nor this
+    // call's workspace); the record is forgotten until this call's launches succeed
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(workspace);
+    const bool x_early = !hx && g_tune_x_early.load() != 0 && !(xa < wa + workspace_bytes && wa < xa + T * H * 2) &&
+                         x_independent_of_last_forward(stream, xa, xa + (uintptr_t)(T * H * 2));
+    if (hx && (path != PATH_TC || !hostx_supported(*d, T, H, I))) return MSE_ERR_UNSUPPORTED_SHAPE;
+    forget_writes(stream);
+
+    record(g_ev_begin, s);
+    if (path == PATH_GENERIC) {
+        SimtGemmArgs a = {};
+        a.A = x; a.lda = H; a.B = w_gate_up; a.B2 = w_gate_up + I * H; a.ldb = H;
+        a.M = T; a.N = I; a.K = H; a.groups = 1; a.out = h; a.ldo = I; a.mode = SIMT_SWIGLU;
+        if ((st = from_cuda(launch_simt_gemm(a, s))) != MSE_OK) return st;
+        record(g_ev_mid, s);
+        SimtGemmArgs b = {};
+        b.A = h; b.lda = I; b.B = w_down; b.ldb = I;
+        b.M = T; b.N = H; b.K = I; b.groups = 1; b.out = y; b.ldo = H; b.mode = SIMT_BF16;
+        if ((st = from_cuda(launch_simt_gemm(b, s))) != MSE_OK) return st;
+    } else {
+        if (one_launch_enabled(T)) {
+            if ((st = tc_mlp_one_launch(*d, x, T, H, I, w_gate_up, w_down, 0, I, I, 1, y, tc::EPI_BF16, ws, L, s)) !=
+                MSE_OK)
+                return st;
+            record(g_ev_mid, s);   // one launch: no boundary between the passes
+        } else {
+            const int fl = down_flags_epoch(*d, T, H, I, I, 1);
+            if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, 0, I, h, ws, L, s, x_early, fl, hx)) != MSE_OK)
+                return st;
+            record(g_ev_mid, s);
+            if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s, fl)) != MSE_OK) return st;
+        }
+    }
+    record(g_ev_end, s);
+    const uintptr_t ya = reinterpret_cast<uintptr_t>(y);
+    record_forward_writes(stream, ya, ya + (uintptr_t)(T * H * 2), wa, wa + workspace_bytes);
+    return MSE_OK;
+}
+
 extern "C" {
 
 size_t mlp_swiglu_workspace_bytes(int64_t T, int64_t H, int64_t I) {
@@ -859,54 +1005,7 @@ mse_status merged_proj_workspace_sync_range(int64_t T, int64_t H, int64_t q_dim,
 mse_status mlp_swiglu_forward(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, const mse_bf16 *w_gate_up,
                               const mse_bf16 *w_down, mse_bf16 *y, int64_t y_capacity, void *workspace,
                               size_t workspace_bytes, void *stream) {
-    if (!x || !w_gate_up || !w_down || !y || T <= 0 || H <= 0 || I <= 0) return MSE_ERR_INVALID_ARG;
-    if (y_capacity < T * H) return MSE_ERR_GEOMETRY;
-    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes);
-    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return MSE_ERR_WORKSPACE;
-    DeviceInfo *d = nullptr;
-    mse_status st = current_device(&d);
-    if (st != MSE_OK) return st;
-    Path path;
-    if ((st = choose(mlp_tc_ok(x, H, I, I, w_gate_up, w_down, y, workspace), &path)) != MSE_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    char *ws = static_cast<char *>(workspace);
-    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h_off);
-    // MSE_TUNE_X_EARLY: x overlaps nothing the previous call on this stream writes (nor this
-    // call's workspace); the record is forgotten until this call's launches succeed
-    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(workspace);
-    const bool x_early = g_tune_x_early.load() != 0 && !(xa < wa + workspace_bytes && wa < xa + T * H * 2) &&
-                         x_independent_of_last_forward(stream, xa, xa + (uintptr_t)(T * H * 2));
-    forget_writes(stream);
-
-    record(g_ev_begin, s);
-    if (path == PATH_GENERIC) {
-        SimtGemmArgs a = {};
-        a.A = x; a.lda = H; a.B = w_gate_up; a.B2 = w_gate_up + I * H; a.ldb = H;
-        a.M = T; a.N = I; a.K = H; a.groups = 1; a.out = h; a.ldo = I; a.mode = SIMT_SWIGLU;
-        if ((st = from_cuda(launch_simt_gemm(a, s))) != MSE_OK) return st;
-        record(g_ev_mid, s);
-        SimtGemmArgs b = {};
-        b.A = h; b.lda = I; b.B = w_down; b.ldb = I;
-        b.M = T; b.N = H; b.K = I; b.groups = 1; b.out = y; b.ldo = H; b.mode = SIMT_BF16;
-        if ((st = from_cuda(launch_simt_gemm(b, s))) != MSE_OK) return st;
-    } else {
-        if (one_launch_enabled(T)) {
-            if ((st = tc_mlp_one_launch(*d, x, T, H, I, w_gate_up, w_down, 0, I, I, 1, y, tc::EPI_BF16, ws, L, s)) !=
-                MSE_OK)
-                return st;
-            record(g_ev_mid, s);   // one launch: no boundary between the passes
-        } else {
-            const int fl = down_flags_epoch(*d, T, H, I, I, 1);
-            if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, 0, I, h, ws, L, s, x_early, fl)) != MSE_OK) return st;
-            record(g_ev_mid, s);
-            if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s, fl)) != MSE_OK) return st;
-        }
-    }
-    record(g_ev_end, s);
-    const uintptr_t ya = reinterpret_cast<uintptr_t>(y);
-    record_forward_writes(stream, ya, ya + (uintptr_t)(T * H * 2), wa, wa + workspace_bytes);
-    return MSE_OK;
+    return forward_impl(x, T, H, I, w_gate_up, w_down, y, y_capacity, workspace, workspace_bytes, stream, nullptr);
 }
 
 mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, const mse_bf16 *w_gate_up,
@@ -1025,7 +1124,7 @@ mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int
 size_t mlp_swiglu_host_workspace_bytes(int64_t T, int64_t H, int64_t I) {
     const size_t n = mlp_swiglu_workspace_bytes(T, H, I);
     if (n == 0) return 0;
-    return align_up((size_t)T * (size_t)H * 2, 256) + n;
+    return host_ws_layout(T, H).mlp_off + n;
 }
 
 mse_status mlp_swiglu_forward_host(const mse_bf16 *x_host, int64_t T, int64_t H, int64_t I,
@@ -1033,11 +1132,11 @@ mse_status mlp_swiglu_forward_host(const mse_bf16 *x_host, int64_t T, int64_t H,
                                    int64_t y_capacity, void *workspace, size_t workspace_bytes, void *stream) {
     if (!x_host || !w_gate_up || !w_down || !y_host || T <= 0 || H <= 0 || I <= 0) return MSE_ERR_INVALID_ARG;
     if (y_capacity < T * H) return MSE_ERR_GEOMETRY;
-    const size_t act = align_up((size_t)T * (size_t)H * 2, 256);
-    if (!workspace || workspace_bytes < act || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    const HostWs hw = host_ws_layout(T, H);
+    if (!workspace || workspace_bytes < hw.mlp_off || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MSE_ERR_WORKSPACE;
-    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes - act);
-    if (workspace_bytes - act < L.total) return MSE_ERR_WORKSPACE;
+    const MlpWs L = mlp_ws_place(T, H, I, workspace_bytes - hw.mlp_off);
+    if (workspace_bytes - hw.mlp_off < L.total) return MSE_ERR_WORKSPACE;
     const uintptr_t xa = reinterpret_cast<uintptr_t>(x_host), ya = reinterpret_cast<uintptr_t>(y_host);
     const uintptr_t nb = (uintptr_t)(T * H * 2);
     if (xa < ya + nb && ya < xa + nb) return MSE_ERR_INVALID_ARG;   // x and y overlap
@@ -1052,17 +1151,42 @@ mse_status mlp_swiglu_forward_host(const mse_bf16 *x_host, int64_t T, int64_t H,
         return MSE_ERR_INVALID_ARG;
     }
     char *ws = static_cast<char *>(workspace);
-    mse_bf16 *xd = reinterpret_cast<mse_bf16 *>(ws);
+    char *wsm = ws + hw.mlp_off;
+    const size_t wsm_bytes = workspace_bytes - hw.mlp_off;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // x may be read before the previous work on the stream is done unless the previous call
     // of this entry point on the stream writes it
-    const bool early = !host_range_overlaps_last_output(stream, xa, xa + nb);
+    const bool read_early = !host_range_overlaps_last_output(stream, xa, xa + nb);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        cap = cudaStreamCaptureStatusActive;   // unknown: take the waiting copy
+    }
+    const bool hostx = g_tune_host_x_copiers.load() > 0 && g_path.load() != MSE_PATH_GENERIC && aligned16(xh) &&
+                       mlp_tc_ok(ws + hw.x_off[0], H, I, I, w_gate_up, w_down, yh, wsm) &&
+                       hostx_supported(*d, T, H, I);
     record_host_output(stream, ya, ya + nb);
+    forget_writes(stream);
+    if (hostx) {
+        // the gate_up launch copies x into one of two buffers, the other one than the
+        // previous call on this workspace: the copy may then run before the previous grid
+        // is complete, since every reader of this buffer is an earlier call's gate_up
+        bool alternate = false;
+        const int b = next_x_buffer(workspace, T, H, cap != cudaStreamCaptureStatusNone, &alternate);
+        const HostX hx = {xh, reinterpret_cast<int *>(ws + hw.sync_off) + 4 * b, alternate && read_early};
+        st = forward_impl(reinterpret_cast<const mse_bf16 *>(ws + hw.x_off[b]), T, H, I, w_gate_up, w_down,
+                          static_cast<mse_bf16 *>(yh), y_capacity, wsm, wsm_bytes, stream, &hx);
+        if (st != MSE_OK) forget_x_buffer(workspace);
+        return st;
+    }
+    // otherwise a copy kernel into buffer 0, which writes once the previous work is complete
+    forget_x_buffer(workspace);
+    mse_bf16 *xd = reinterpret_cast<mse_bf16 *>(ws + hw.x_off[0]);
     forget_writes(stream);   // the copy kernel writes this call's x
-    if ((st = from_cuda(launch_copy_in(xh, xd, T * H * 2, early, d->sm_count, s))) != MSE_OK) return st;
+    if ((st = from_cuda(launch_copy_in(xh, xd, T * H * 2, read_early, d->sm_count, s))) != MSE_OK) return st;
     // the down projection writes y straight into the caller's host buffer
-    return mlp_swiglu_forward(xd, T, H, I, w_gate_up, w_down, static_cast<mse_bf16 *>(yh), y_capacity, ws + act,
-                              workspace_bytes - act, stream);
+    return forward_impl(xd, T, H, I, w_gate_up, w_down, static_cast<mse_bf16 *>(yh), y_capacity, wsm, wsm_bytes,
+                        stream, nullptr);
 }
 
 int mse_shard_sequence_parallel_mlp(int enabled, int use_sequence_parallel, int eligible, int tp_size,
@@ -1234,6 +1358,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_SWAPAB_MAX_T: slot = &g_tune_swapab_max_t; ok = value >= 0 && value <= kSwapAbMaxT; break;
         case MSE_TUNE_X_EARLY: slot = &g_tune_x_early; ok = value == 0 || value == 1; break;
         case MSE_TUNE_DOWN_FLAGS: slot = &g_tune_down_flags; ok = value == 0 || value == 1; break;
+        case MSE_TUNE_HOST_X_COPIERS: slot = &g_tune_host_x_copiers; ok = value >= 0 && value <= 1024; break;
         default: return -1;
     }
     if (!ok) return -1;

@@ -42,6 +42,7 @@ struct Ctrl {
     uint32_t tmem_base;
     int abort_flag;
     int fin_flag;
+    int x_ticket;            // swap-AB gate_up with x in host memory: this CTA's copy ticket
     int seg_slot[128];       // swap-AB split-K finisher: slot index of each part of the tile
 };
 
@@ -428,11 +429,12 @@ __device__ bool swapab_produce(const SwapAbParams &p, const CUtensorMap *tmA, co
             }
         }
         bool flags_ok = true;
-        if (EPI != EPI_SWIGLU && p.hflags) {
+        if ((EPI != EPI_SWIGLU && p.hflags) || (EPI == EPI_SWIGLU && p.x_host)) {
             // the epilogue warps poll the flags of every h block this CTA reads (no wait for
-            // the gate_up grid to complete) and arrive here once all are published
+            // the gate_up grid to complete), or the count of copied slices of x, and arrive
+            // here once the token operand is complete
             flags_ok = mbar_wait_bounded(bar_addr(&ctl->hready_bar), 0u, abort_flag, p.wait_limit_ns, p.err);
-            fence_proxy_async_global();   // h was written through the generic proxy
+            fence_proxy_async_global();   // written through the generic proxy
         } else {
             pdl_wait();
         }
@@ -1036,6 +1038,57 @@ __device__ bool swapab_epilogue(const SwapAbParams &p, Ctrl *ctl, uint8_t *ring,
     return true;
 }
 
+// ---- gate_up with x in host memory (epilogue warps, before their first tile) ----
+// Each CTA takes a ticket; the first x_copiers tickets copy one slice of x each (16-byte
+// words, sixteen loads in flight per thread), make the stores visible to the tensor-memory
+// copies' proxy and count the slice (release).  One thread per CTA then waits for every
+// slice (acquire), releases the producer's token loads, and counts itself past the wait;
+// the last CTA past it zeroes the three words.  Without x_copy_early every CTA first waits
+// for the previous grid (then every earlier user of the buffer and of the words is done).
+// Every wait is bounded.
+__device__ __noinline__ void swapab_copy_x(const SwapAbParams &p, Ctrl *ctl, volatile int *abort_flag) {
+    const int tid = threadIdx.x - 64;
+    if (!p.x_copy_early) pdl_wait();
+    if (tid == 0) ctl->x_ticket = atomicAdd(p.x_sync, 1);
+    named_barrier_sync(1, 128);
+    const int ticket = ctl->x_ticket;
+    if (ticket < p.x_copiers) {
+        const int64_t v0 = p.x_vecs * ticket / p.x_copiers, v1 = p.x_vecs * (ticket + 1) / p.x_copiers;
+        constexpr int kIn = 16;   // 32 KB of host reads in flight per CTA
+        for (int64_t v = v0 + tid; v < v1; v += 128 * kIn) {
+            uint4 r[kIn];
+#pragma unroll
+            for (int k = 0; k < kIn; ++k)
+                if (v + k * 128 < v1) r[k] = p.x_host[v + k * 128];
+#pragma unroll
+            for (int k = 0; k < kIn; ++k)
+                if (v + k * 128 < v1) p.x_copy[v + k * 128] = r[k];
+        }
+        fence_proxy_async_global();
+        named_barrier_sync(1, 128);
+        if (tid == 0) red_add_release_gpu(p.x_sync + 1, 1);
+    }
+    if (tid == 0) {
+        const uint64_t t0 = global_timer_ns();
+        bool ok = true;
+        while (ld_acquire_gpu(p.x_sync + 1) < p.x_copiers) {
+            if (*abort_flag || global_timer_ns() - t0 > p.wait_limit_ns) { ok = false; break; }
+            __nanosleep(100);
+        }
+        if (ok) {
+            mbar_arrive(bar_addr(&ctl->hready_bar));
+            if (atomic_add_acq_rel_gpu(p.x_sync + 2, 1) == (int)gridDim.x - 1) {
+                p.x_sync[0] = 0;
+                p.x_sync[1] = 0;
+                p.x_sync[2] = 0;
+            }
+        } else if (!*abort_flag) {
+            *abort_flag = 1;
+            raise_device_error(p.err, DEV_ERR_TIMEOUT);
+        }
+    }
+}
+
 // ---- set-up and teardown shared by the swap-AB kernels ----
 // PAIR: the second CTA's full barriers are unused (its copies signal the first CTA's),
 // the first CTA's tempty barriers count one arrival per epilogue warp of both CTAs, and
@@ -1133,8 +1186,10 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
     volatile int *abort_flag = &ctl->abort_flag;
     // gate_up that publishes h flags lets the down grid launch only once the previous grid on
     // the stream (the previous call's down kernel, which clears the flags) is complete: no down
-    // CTA can see a flag that the previous call left behind
-    const bool late_trigger = EPI == EPI_SWIGLU && p.hflags != nullptr;
+    // CTA can see a flag that the previous call left behind.  gate_up that copies x from host
+    // memory does the same, so that every grid before it is complete once the next call's
+    // gate_up starts (that one may write the other x buffer, which this call's predecessors read)
+    const bool late_trigger = EPI == EPI_SWIGLU && (p.hflags != nullptr || p.x_host != nullptr);
     if (!late_trigger) pdl_launch_dependents();
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -1151,6 +1206,7 @@ __global__ void __launch_bounds__(kSwapAbThreads, 1)
             (void)swapab_mma<PAIR>(p, ctl, sm, r, gseg, tmem_base, abort_flag);
         }
     } else {
+        if (EPI == EPI_SWIGLU && p.x_host) swapab_copy_x(p, ctl, abort_flag);
         if (EPI != EPI_SWIGLU && p.hflags) {
             // the h blocks of every stage of this CTA: one flag per thread per round (an acquire
             // load at most every 0.2 us), a CTA barrier once every flag is seen, then one arrival

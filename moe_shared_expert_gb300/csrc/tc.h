@@ -67,6 +67,18 @@ struct SwapAbParams {
     int *hflags;
     int *exit_count;
     int hflag_first, hflag_n, hflag_epoch;
+    // gate_up with x in host memory (null: x is already in device memory).  The first
+    // x_copiers CTAs to start (those on SMs the previous kernel leaves free) copy one slice
+    // of x each from x_host into x_copy, the buffer the token operand's tensor map reads, and
+    // count it in x_sync[1]; every CTA's token loads wait until all slices are counted.
+    // x_sync = [tickets taken, slices copied, CTAs past the wait]: the last CTA past the wait
+    // zeroes all three.  x_copy_early = 0: the copiers wait for the previous grid first.
+    const uint4 *x_host;
+    uint4 *x_copy;
+    int64_t x_vecs;        // 16-byte words of x
+    int *x_sync;
+    int x_copiers;
+    int x_copy_early;
     uint64_t wait_limit_ns;
     uint32_t *err;
 };

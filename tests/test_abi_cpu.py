@@ -126,7 +126,8 @@ def test_forward_validation(L):
 def test_forward_host_validation(L):
     f = L.mlp_swiglu_forward_host
     n = L.mlp_swiglu_host_workspace_bytes(64, 7168, 6144)
-    assert n == L.mlp_swiglu_workspace_bytes(64, 7168, 6144) + 64 * 7168 * 2   # + the device copy of x
+    # + the copy counts (256 bytes) and the two device copies of x
+    assert n == L.mlp_swiglu_workspace_bytes(64, 7168, 6144) + 256 + 2 * 64 * 7168 * 2
     assert f(None, 64, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168, FAKE, n, None) == code("MSE_ERR_INVALID_ARG")
     assert f(FAKE, 64, 7168, 6144, FAKE, FAKE, FAKE, 64 * 7168 - 1, FAKE, n, None) == code("MSE_ERR_GEOMETRY")
     assert f(FAKE, 64, 7168, 6144, FAKE, FAKE, FAKE * 16, 64 * 7168, FAKE, n - 256, None) == code("MSE_ERR_WORKSPACE")
