@@ -421,6 +421,10 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         CTAs of the gate_up launch that copy a slice of x each from host memory
  *                         (the first to start; 1 .. 1024, at most the launch's CTAs; default 16);
  *                         0 = a separate copy kernel before the layer
+ *   MSE_TUNE_PAIR_SPLIT   1 = CTA-pair kernel launches of an MLP call at 129-256 tokens with at
+ *                         most half as many tiles as clusters split the k-blocks of their tiles
+ *                         over more clusters, at most two parts per tile (default); 0 = whole
+ *                         tiles only
  * Returns the previous value, or -1 for an unknown key or out-of-range value.
  * Results do not depend on these settings beyond floating-point summation order. */
 typedef enum {
@@ -439,7 +443,8 @@ typedef enum {
     MSE_TUNE_SWAPAB_MAX_T = 15,
     MSE_TUNE_X_EARLY = 16,
     MSE_TUNE_DOWN_FLAGS = 17,
-    MSE_TUNE_HOST_X_COPIERS = 18
+    MSE_TUNE_HOST_X_COPIERS = 18,
+    MSE_TUNE_PAIR_SPLIT = 19
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 

@@ -35,7 +35,7 @@ TUNE_ISSUE_GROUP, TUNE_STAGES, TUNE_CACHE_HINTS, TUNE_GRID, TUNE_SPIN_WAIT, TUNE
     1, 2, 3, 4, 6, 7, 8
 TUNE_COOP_FINISH, TUNE_PAIR_MIN_T, TUNE_GRID_DOWN, TUNE_CLUSTER_FINISH = 9, 10, 11, 12
 TUNE_L2_PREFETCH, TUNE_SWAPAB_MAX_T, TUNE_X_EARLY, TUNE_DOWN_FLAGS = 14, 15, 16, 17
-TUNE_HOST_X_COPIERS = 18
+TUNE_HOST_X_COPIERS, TUNE_PAIR_SPLIT = 18, 19
 STATUS = {
     0: "MSE_OK", 1: "MSE_ERR_INVALID_ARG", 2: "MSE_ERR_NOT_DIVISIBLE", 3: "MSE_ERR_GEOMETRY",
     4: "MSE_ERR_WORKSPACE", 5: "MSE_ERR_UNSUPPORTED_DEVICE", 6: "MSE_ERR_CUDA", 7: "MSE_ERR_TIMEOUT",

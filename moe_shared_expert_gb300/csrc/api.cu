@@ -22,7 +22,7 @@ std::atomic<int> g_tune_issue_group{2}, g_tune_stages{0}, g_tune_cache_hints{1},
     g_tune_spin_wait{0}, g_tune_one_launch{0}, g_tune_pdl{1},
     g_tune_coop_finish{6}, g_tune_pair_min_t{0}, g_tune_grid_down{0}, g_tune_cluster_finish{0},
     g_tune_l2_prefetch{8}, g_tune_swapab_max_t{160}, g_tune_x_early{0}, g_tune_down_flags{0},
-    g_tune_host_x_copiers{16};
+    g_tune_host_x_copiers{16}, g_tune_pair_split{1};
 std::atomic<void *> g_ev_begin{nullptr}, g_ev_mid{nullptr}, g_ev_end{nullptr};
 
 struct DeviceInfo {
@@ -115,7 +115,9 @@ MlpWs mlp_ws_layout(int64_t T, int64_t H, int64_t I) {
     w.h_off = off;
     off = align_up(off + (size_t)T * (size_t)I * 2, 256);
     if (T <= kSwapAbMaxT) {
-        const int bn = round_up16(T);
+        // 2 slots per CTA of 128 rows x bn tokens (swap-AB), or of 128 tokens x 256 columns
+        // (the CTA-pair kernel's split tiles, from 129 tokens on)
+        const int bn = T > 128 ? 256 : round_up16(T);
         const size_t slot_region = (size_t)tc::kMaxGrid * 2 * 128 * (size_t)bn * 4;
         w.slots_off = off;
         off = align_up(off + slot_region, 256);
@@ -454,6 +456,27 @@ bool use_pair(int64_t T) {
     return T <= 256 || T >= 512;
 }
 
+// Split-K for the CTA-pair kernel (MSE_TUNE_PAIR_SPLIT): when a launch has at most half as
+// many tiles as clusters (up to 256 tokens: one token tile), the largest cluster count that
+// splits no tile into more than two parts (the finisher then adds one other part); 0
+// otherwise.  At 256 tokens the down projection's 28 tiles of 96 k-blocks run on 56 clusters
+// (34.8 against 38.9 us alone); gate_up's 48 tiles stay whole: on 72 clusters it measured
+// 47.1 against 43.3 us (the launch's operand stream does not grow with more SMs).
+int pair_split_clusters(const DeviceInfo &d, int64_t n_tiles, int kbp) {
+    const int64_t max_c = (d.sm_count < tc::kMaxPersistentGrid ? d.sm_count : tc::kMaxPersistentGrid) / 2;
+    if (g_tune_pair_split.load() == 0 || 2 * n_tiles > max_c || kbp < 2) return 0;
+    const int64_t U = n_tiles * kbp;
+    for (int64_t C = max_c; C > n_tiles; --C) {
+        int worst = 1;
+        for (int64_t t = 0; t < n_tiles && worst <= 2; ++t) {
+            const int64_t c0 = ((t * kbp + 1) * C - 1) / U, c1 = ((t * kbp + kbp) * C - 1) / U;
+            worst = std::max(worst, (int)(c1 - c0 + 1));
+        }
+        if (worst <= 2) return (int)C;
+    }
+    return 0;
+}
+
 int pair_clusters(const DeviceInfo &d, int64_t n_tiles) {
     int64_t c = (d.sm_count < tc::kMaxPersistentGrid ? d.sm_count : tc::kMaxPersistentGrid) / 2;
     return (int)(c < n_tiles ? c : n_tiles);
@@ -543,8 +566,18 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         p.out = h;
         p.ldo = I;
         p.err = d.err;
-        return from_cuda(tc::launch_pair(tc::EPI_SWIGLU, ta, tb, p,
-                                         pair_clusters(d, (int64_t)p.n_mtiles * p.n_ntiles), use_pdl(), s));
+        int clusters = pair_clusters(d, (int64_t)p.n_mtiles * p.n_ntiles);
+        p.cache_hints = T <= 256 ? g_tune_cache_hints.load() : 0;   // weights streamed once
+        if (T <= kSwapAbMaxT && T > 128) {
+            const int c = pair_split_clusters(d, (int64_t)p.n_mtiles * p.n_ntiles, p.kb_per_tile);
+            if (c > 0) {
+                p.split_k = 1;
+                p.slots = reinterpret_cast<float *>(ws + L.slots_off);
+                p.counters = reinterpret_cast<int *>(ws + L.cnt_gu_off);
+                clusters = c;
+            }
+        }
+        return from_cuda(tc::launch_pair(tc::EPI_SWIGLU, ta, tb, p, clusters, use_pdl(), s));
     }
     if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
     if ((st = map_gate_up_halves(&tb, w_gate_up, H, I, 128)) != MSE_OK) return st;
@@ -614,8 +647,19 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
         p.ldo = H;
         p.o_group_stride = T * H;
         p.err = d.err;
-        return from_cuda(tc::launch_pair(epi, ta, tb, p,
-                                         pair_clusters(d, (int64_t)groups * p.n_mtiles * p.n_ntiles), use_pdl(), s));
+        const int64_t n_tiles = (int64_t)groups * p.n_mtiles * p.n_ntiles;
+        int clusters = pair_clusters(d, n_tiles);
+        p.cache_hints = T <= 256 ? g_tune_cache_hints.load() : 0;   // weights streamed once
+        if (T <= kSwapAbMaxT && T > 128) {
+            const int c = pair_split_clusters(d, n_tiles, p.kb_per_tile);
+            if (c > 0) {
+                p.split_k = 1;
+                p.slots = reinterpret_cast<float *>(ws + L.slots_dn_off);
+                p.counters = reinterpret_cast<int *>(ws + L.cnt_dn_off);
+                clusters = c;
+            }
+        }
+        return from_cuda(tc::launch_pair(epi, ta, tb, p, clusters, use_pdl(), s));
     }
     if ((st = map_2d(&ta, h, T, I, I, 128)) != MSE_OK) return st;
     if ((st = map_2d(&tb, w_down, H, I, I, 256)) != MSE_OK) return st;
@@ -1359,6 +1403,7 @@ int mse_set_tuning(int key, int value) {
         case MSE_TUNE_X_EARLY: slot = &g_tune_x_early; ok = value == 0 || value == 1; break;
         case MSE_TUNE_DOWN_FLAGS: slot = &g_tune_down_flags; ok = value == 0 || value == 1; break;
         case MSE_TUNE_HOST_X_COPIERS: slot = &g_tune_host_x_copiers; ok = value >= 0 && value <= 1024; break;
+        case MSE_TUNE_PAIR_SPLIT: slot = &g_tune_pair_split; ok = value == 0 || value == 1; break;
         default: return -1;
     }
     if (!ok) return -1;

@@ -1575,6 +1575,79 @@ __global__ void __launch_bounds__(kStdThreads, 1)
 constexpr uint32_t kPairBTileBytes = 128 * 64 * 2;
 constexpr int kPairBandM = 8;
 
+// Epilogue stores of the pair kernel for one CTA's token row `tok`: SwiGLU chunk c (gate
+// columns 16c .., up columns 128 + 16c ..) or 16 output columns 16c .. of the tile.
+__device__ __forceinline__ void pair_store_swiglu(const StdParams &p, const StdTile &t, int64_t tok, bool tok_ok,
+                                                  int c, const float (&g)[16], const float (&u)[16]) {
+    uint16_t *h = static_cast<uint16_t *>(p.out);
+    const int64_t j = (int64_t)p.n_base + (int64_t)t.n * 128 + c * 16;
+    if (!tok_ok || j >= p.n_valid) return;
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = (uint32_t)f32_to_bf16_bits(silu_f32(g[2 * i]) * u[2 * i]) |
+               ((uint32_t)f32_to_bf16_bits(silu_f32(g[2 * i + 1]) * u[2 * i + 1]) << 16);
+    uint4 *dst = reinterpret_cast<uint4 *>(h + tok * p.ldo + j);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+template <int EPI>
+__device__ __forceinline__ void pair_store_cols(const StdParams &p, const StdTile &t, int64_t tok, bool tok_ok, int c,
+                                                const float (&v)[16]) {
+    const int64_t n = (int64_t)t.n * 256 + c * 16;
+    if (!tok_ok || n >= p.n_valid) return;
+    if constexpr (EPI == EPI_F32) {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + t.group * p.o_group_stride +
+                                                 tok * p.ldo + n);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else if constexpr (EPI == EPI_BF16) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = (uint32_t)f32_to_bf16_bits(v[2 * i]) | ((uint32_t)f32_to_bf16_bits(v[2 * i + 1]) << 16);
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + t.group * p.o_group_stride +
+                                               tok * p.ldo + n);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {  // EPI_MERGED
+        uint16_t *lo = static_cast<uint16_t *>(p.out);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int64_t col = n + i;
+            if (col >= p.n_valid) break;
+            const uint16_t b = f32_to_bf16_bits(v[i]);
+            if (lo) lo[tok * p.ldo + col] = b;
+            if (p.out_rm) p.out_rm[tok * p.ldo + logical_to_gathered(col, p.q_dim, p.kv_dim, p.tp)] = b;
+        }
+    }
+}
+
+constexpr int kPairSlotFloats = 128 * 256;
+
+// The units of one cluster of the pair kernel, as segments (tile, k-blocks [kb0, kb1)):
+// whole tiles cluster, cluster + n_clusters, ..., or with split_k the cluster's share
+// [ub, ue) of the (tile, k-block) units.
+struct PairWork {
+    int64_t cluster, n_clusters, n_tiles, ub, ue;
+    int kbp;
+    bool split;
+    __device__ bool seg(int64_t i, int64_t &tile, int &kb0, int &kb1) const {
+        if (!split) {
+            tile = cluster + i * n_clusters;
+            kb0 = 0;
+            kb1 = kbp;
+            return tile < n_tiles;
+        }
+        tile = ub / kbp + i;
+        if (tile * kbp >= ue) return false;
+        kb0 = (int)(ub > tile * kbp ? ub - tile * kbp : 0);
+        kb1 = (int)(ue < (tile + 1) * kbp ? ue - tile * kbp : kbp);
+        return true;
+    }
+};
+
 template <int EPI>
 __global__ void __launch_bounds__(kStdThreads, 1)
     pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const StdParams p) {
@@ -1584,7 +1657,9 @@ __global__ void __launch_bounds__(kStdThreads, 1)
     const int S = p.stages;
     const uint32_t sA = base;
     const uint32_t sB = base + (uint32_t)S * kATileBytes;
-    Ctrl *ctl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + (uint32_t)S * (kATileBytes + kPairBTileBytes));
+    uint8_t *ring = smem_raw + (base - raw);
+    const uint32_t ring_bytes = (uint32_t)S * (kATileBytes + kPairBTileBytes);
+    Ctrl *ctl = reinterpret_cast<Ctrl *>(ring + ring_bytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
@@ -1592,6 +1667,8 @@ __global__ void __launch_bounds__(kStdThreads, 1)
     const int64_t n_tiles = (int64_t)p.n_groups * p.n_mtiles * p.n_ntiles;
     const int kbp = p.kb_per_tile;
     constexpr uint32_t kTmemCols = 512;
+    const StreamK sk{n_tiles * kbp, n_clusters};
+    const PairWork work{cluster, n_clusters, n_tiles, sk.begin(cluster), sk.begin(cluster + 1), kbp, p.split_k != 0};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -1603,6 +1680,7 @@ __global__ void __launch_bounds__(kStdThreads, 1)
             mbar_init(bar_addr(&ctl->tempty[b]), 8);   // 4 epilogue warps x 2 CTAs
         }
         mbar_init(bar_addr(&ctl->drain), 1);
+        mbar_init(bar_addr(&ctl->fixbar), 1);
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
@@ -1640,13 +1718,18 @@ __global__ void __launch_bounds__(kStdThreads, 1)
     int64_t issued = 0;
     if (warp == 0) {
         if (lane == 0) {
+            // (token tiles are read by every tile of a column band, weight tiles once when the
+            // launch has one token tile)
+            const uint64_t pol_a = l2_policy_evict_last(), pol_b = l2_policy_evict_first();
             pdl_wait();
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int64_t id = cluster; id < n_tiles && ok; id += n_clusters) {
+            int64_t id;
+            int kb0, kb1;
+            for (int64_t i = 0; ok && work.seg(i, id, kb0, kb1); ++i) {
                 const StdTile t = tile_of(id);
-                for (int kb = 0; kb < kbp; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_bounded(bar_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns,
                                            p.err)) {
                         ok = false;
@@ -1656,9 +1739,15 @@ __global__ void __launch_bounds__(kStdThreads, 1)
                     if (leader)
                         mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), 2u * (kATileBytes + kPairBTileBytes));
                     const int k = (p.kb_first + t.group * p.kb_group_stride + kb) * 64;
-                    tma_load_2d_pair(sA + stage * kATileBytes, &tmA, fb, k, t.m * 256 + (int)rank * 128);
-                    tma_load_2d_pair(sB + stage * kPairBTileBytes, &tmB, fb, k,
-                                     p.b_base + t.n * p.b_n_stride + (int)rank * p.b_rank_stride);
+                    const int a_row = t.m * 256 + (int)rank * 128;
+                    const int b_row = p.b_base + t.n * p.b_n_stride + (int)rank * p.b_rank_stride;
+                    if (p.cache_hints) {
+                        tma_load_2d_pair_hint(sA + stage * kATileBytes, &tmA, fb, k, a_row, pol_a);
+                        tma_load_2d_pair_hint(sB + stage * kPairBTileBytes, &tmB, fb, k, b_row, pol_b);
+                    } else {
+                        tma_load_2d_pair(sA + stage * kATileBytes, &tmA, fb, k, a_row);
+                        tma_load_2d_pair(sB + stage * kPairBTileBytes, &tmB, fb, k, b_row);
+                    }
                     ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
@@ -1669,17 +1758,18 @@ __global__ void __launch_bounds__(kStdThreads, 1)
             const uint32_t idesc = idesc_bf16_f32(256, 256);
             int stage = 0;
             uint32_t phase = 0;
-            int it = 0;
             bool ok = true;
-            for (int64_t id = cluster; id < n_tiles && ok; id += n_clusters, ++it) {
-                const int buf = it & 1;
-                const uint32_t use = (uint32_t)(it >> 1);
+            int64_t id;
+            int kb0, kb1;
+            for (int64_t i = 0; ok && work.seg(i, id, kb0, kb1); ++i) {
+                const int buf = (int)(i & 1);
+                const uint32_t use = (uint32_t)(i >> 1);
                 if (!mbar_wait_bounded(bar_addr(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, p.wait_limit_ns,
                                        p.err))
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * 256);
-                for (int kb = 0; kb < kbp; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_bounded(bar_addr(&ctl->full[stage]), phase, abort_flag, p.wait_limit_ns, p.err)) {
                         ok = false;
                         break;
@@ -1690,7 +1780,7 @@ __global__ void __launch_bounds__(kStdThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_bf16_pair(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
-                                         (kb > 0 || kk > 0) ? 1u : 0u);
+                                         (kb > kb0 || kk > 0) ? 1u : 0u);
                     tc_commit_pair_multicast(bar_addr(&ctl->empty[stage]), (uint16_t)0x3);
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
@@ -1702,12 +1792,19 @@ __global__ void __launch_bounds__(kStdThreads, 1)
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        auto release = [&](int buf) {   // hand the accumulator back to the MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(bar_addr(&ctl->tempty[buf]), 0));
+        };
         pdl_wait();
-        int it = 0;
-        for (int64_t id = cluster; id < n_tiles; id += n_clusters, ++it) {
+        uint32_t fix_round = 0;
+        int64_t id;
+        int kb0, kb1;
+        for (int64_t i = 0; work.seg(i, id, kb0, kb1); ++i) {
             const StdTile t = tile_of(id);
-            const int buf = it & 1;
-            const uint32_t use = (uint32_t)(it >> 1);
+            const int buf = (int)(i & 1);
+            const uint32_t use = (uint32_t)(i >> 1);
             const bool got =
                 mbar_wait_bounded(bar_addr(&ctl->tfull[buf]), use & 1u, abort_flag, p.wait_limit_ns, p.err);
             if (!named_barrier_and(1, 128, got)) break;
@@ -1715,65 +1812,134 @@ __global__ void __launch_bounds__(kStdThreads, 1)
             const uint32_t tacc = tmem_base + (uint32_t)(buf * 256) + lane_off;
             const int64_t tok = (int64_t)t.m * 256 + rank * 128 + row;
             const bool tok_ok = tok < p.T;
-            if constexpr (EPI == EPI_SWIGLU) {
-                uint16_t *h = static_cast<uint16_t *>(p.out);
-                const int64_t j0 = (int64_t)p.n_base + (int64_t)t.n * 128;
+            if (kb0 == 0 && kb1 == kbp) {   // the whole tile: straight from tensor memory
+                if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
-                    float g[16], u[16];
-                    load_tmem_chunk(tacc + (uint32_t)(c * 16), g);
-                    load_tmem_chunk(tacc + (uint32_t)(128 + c * 16), u);
-                    const int64_t j = j0 + c * 16;
-                    if (tok_ok && j < p.n_valid) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            w[i] = (uint32_t)f32_to_bf16_bits(silu_f32(g[2 * i]) * u[2 * i]) |
-                                   ((uint32_t)f32_to_bf16_bits(silu_f32(g[2 * i + 1]) * u[2 * i + 1]) << 16);
-                        uint4 *dst = reinterpret_cast<uint4 *>(h + tok * p.ldo + j);
-                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int c = 0; c < 8; ++c) {
+                        float g[16], u[16];
+                        load_tmem_chunk(tacc + (uint32_t)(c * 16), g);
+                        load_tmem_chunk(tacc + (uint32_t)(128 + c * 16), u);
+                        pair_store_swiglu(p, t, tok, tok_ok, c, g, u);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < 16; ++c) {
+                        float v[16];
+                        load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
+                        pair_store_cols<EPI>(p, t, tok, tok_ok, c, v);
                     }
                 }
-            } else {
+                release(buf);
+                continue;
+            }
+            // A part of a split tile (at most two parts: the host's choice of clusters).  Park
+            // it in this CTA's slot (0 for the cluster's first segment, 1 for its last), count
+            // it, and if it arrived last, sum both parts in part order and finish the tile.
+            int64_t id_next;
+            int nb0, nb1;
+            const bool final_seg = !work.seg(i + 1, id_next, nb0, nb1);
+            float *slot = p.slots + ((size_t)blockIdx.x * 2 + (work.ub >= id * kbp ? 0 : 1)) * kPairSlotFloats;
 #pragma unroll 1
-                for (int c = 0; c < 16; ++c) {
-                    float v[16];
-                    load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
-                    const int64_t n = (int64_t)t.n * 256 + c * 16;
-                    if (!tok_ok || n >= p.n_valid) continue;
-                    if constexpr (EPI == EPI_F32) {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
-                                                                 t.group * p.o_group_stride + tok * p.ldo + n);
+            for (int c = 0; c < 16; ++c) {
+                float v[16];
+                load_tmem_chunk(tacc + (uint32_t)(c * 16), v);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    } else if constexpr (EPI == EPI_BF16) {
-                        uint32_t w[8];
+                for (int k = 0; k < 16; ++k) __stcg(slot + (size_t)(c * 16 + k) * 128 + row, v[k]);
+            }
+            fence_proxy_async_global();   // a finisher may fetch this slot with a bulk copy
+            named_barrier_sync(1, 128);
+            const int64_t c_first = sk.owner(id * kbp), c_last = sk.owner(id * kbp + kbp - 1);
+            const int nparts = (int)(c_last - c_first + 1);
+            int *ctr = p.counters + id * 2 + rank;
+            if (threadIdx.x == 64) ctl->fin_flag = atomic_add_acq_rel_gpu(ctr, 1) == nparts - 1 ? 1 : 0;
+            named_barrier_sync(1, 128);
+            const bool finisher = ctl->fin_flag != 0;
+            auto part = [&](int64_t cc) -> const float * {   // part of cluster cc (this CTA's rank)
+                return p.slots + ((size_t)(cc * 2 + rank) * 2 + (sk.begin(cc) >= id * kbp ? 0 : 1)) * kPairSlotFloats;
+            };
+            if (finisher && nparts == 2 && final_seg && ring_bytes >= kPairSlotFloats * 4u) {
+                // the ring is idle after this cluster's last MMA: the other part goes into it
+                // with one bulk copy; this CTA's own part is still in tensor memory
+                const bool own_first = c_first == cluster;
+                bool ok = true;
+                if (threadIdx.x == 64) {
+                    fence_proxy_async_global();
+                    mbar_arrive_expect_tx(bar_addr(&ctl->fixbar), kPairSlotFloats * 4u);
+                    bulk_load(base, part(own_first ? c_last : c_first), kPairSlotFloats * 4u, bar_addr(&ctl->fixbar));
+                    ok = mbar_wait_bounded(bar_addr(&ctl->fixbar), fix_round & 1u, abort_flag, p.wait_limit_ns, p.err);
+                }
+                ++fix_round;
+                if (!named_barrier_and(1, 128, ok)) {
+                    if (threadIdx.x == 64)
+                        (void)mbar_wait_drain(bar_addr(&ctl->fixbar), (fix_round - 1) & 1u,
+                                              drain_limit_ns(p.wait_limit_ns));
+                    release(buf);
+                    break;
+                }
+                const float *other = reinterpret_cast<const float *>(ring);
+                auto sum2 = [&](int col0, float (&v)[16]) {   // (0 + first part) + second part
+                    float own[16];
+                    load_tmem_chunk(tacc + (uint32_t)col0, own);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            w[i] = (uint32_t)f32_to_bf16_bits(v[2 * i]) |
-                                   ((uint32_t)f32_to_bf16_bits(v[2 * i + 1]) << 16);
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
-                                                               t.group * p.o_group_stride + tok * p.ldo + n);
-                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    } else {  // EPI_MERGED
-                        uint16_t *lo = static_cast<uint16_t *>(p.out);
+                    for (int k = 0; k < 16; ++k) {
+                        const float o = other[(col0 + k) * 128 + row];
+                        v[k] = own_first ? (0.f + own[k]) + o : (0.f + o) + own[k];
+                    }
+                };
+                if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        float g[16], u[16];
+                        sum2(c * 16, g);
+                        sum2(128 + c * 16, u);
+                        pair_store_swiglu(p, t, tok, tok_ok, c, g, u);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < 16; ++c) {
+                        float v[16];
+                        sum2(c * 16, v);
+                        pair_store_cols<EPI>(p, t, tok, tok_ok, c, v);
+                    }
+                }
+                release(buf);
+            } else {
+                release(buf);
+                if (finisher) {
+                    // from L2, every part in cluster order (first to arrive finishing early, or
+                    // more than two parts)
+                    auto sumk = [&](int col0, float (&v)[16]) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int64_t col = n + i;
-                            if (col >= p.n_valid) break;
-                            const uint16_t b = f32_to_bf16_bits(v[i]);
-                            if (lo) lo[tok * p.ldo + col] = b;
-                            if (p.out_rm) p.out_rm[tok * p.ldo + logical_to_gathered(col, p.q_dim, p.kv_dim, p.tp)] = b;
+                        for (int k = 0; k < 16; ++k) v[k] = 0.f;
+                        for (int64_t cc = c_first; cc <= c_last; ++cc) {
+                            const float *src = part(cc) + row;
+                            float w[16];
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) w[k] = __ldcg(src + (size_t)(col0 + k) * 128);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) v[k] += w[k];
+                        }
+                    };
+                    if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+                        for (int c = 0; c < 8; ++c) {
+                            float g[16], u[16];
+                            sumk(c * 16, g);
+                            sumk(128 + c * 16, u);
+                            pair_store_swiglu(p, t, tok, tok_ok, c, g, u);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int c = 0; c < 16; ++c) {
+                            float v[16];
+                            sumk(c * 16, v);
+                            pair_store_cols<EPI>(p, t, tok, tok_ok, c, v);
                         }
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(map_to_rank(bar_addr(&ctl->tempty[buf]), 0));
+            if (finisher && threadIdx.x == 64) *ctr = 0;
+            named_barrier_sync(1, 128);   // fin_flag is reused by the next segment
         }
     }
 

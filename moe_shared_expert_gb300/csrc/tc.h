@@ -113,6 +113,15 @@ struct StdParams {
     uint16_t *out_rm; int64_t q_dim, kv_dim; int tp;
     // CTA-pair kernel only: B row coordinate = b_base + n * b_n_stride + rank * b_rank_stride
     int b_base, b_n_stride, b_rank_stride;
+    // CTA-pair kernel only: split_k = 1 splits the (tile, k-block) units evenly over the
+    // clusters (stream-K; the host picks a cluster count that splits no tile into more than
+    // two parts).  A split tile's parts are parked in slots (2 per CTA, 128 rows x 256
+    // columns fp32, [column][row]) and counted in counters[tile * 2 + rank] (zero on entry,
+    // left zero); the CTA arriving last sums them in part order and runs the epilogue.
+    int split_k;
+    float *slots;
+    int *counters;
+    int cache_hints;       // CTA-pair kernel: 1 = B (weights) evict_first, A (tokens) evict_last in L2
     uint64_t wait_limit_ns;
     uint32_t *err;
 };

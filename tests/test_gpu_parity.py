@@ -267,6 +267,43 @@ def test_near_ridge_tokens_decode_weights(T, swapab_max_t):
     print(f"T={T} swap-AB up to {swapab_max_t}: max err/tol {r:.3f}")
 
 
+@pytest.mark.parametrize("T", [161, 200, 256])
+def test_pair_kernel_split_k(T):
+    # 161-256 tokens over at least 4096 weight rows take the CTA-pair kernel, whose tiles are
+    # then split over more clusters (at most two parts each; the CTA arriving last adds the
+    # other part, from its idle ring or from L2).  On a workspace that is 0xFF except the
+    # sync range: every row within tolerance of the oracle, bit-identical to a fresh
+    # workspace and to a second run (parts summed in part order), the counters left zero;
+    # and within tolerance with the split switched off.
+    H, I = 1024, 2048
+    x, wgu, wd = small_case(T, H, I, 5100 + T)
+    dx, dgu, dwd = to_dev(x), to_dev(wgu), to_dev(wd)
+    n = mse.mlp_swiglu_workspace_bytes(T, H, I)
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")
+    off, b = mse.mlp_swiglu_workspace_sync_range(T, H, I, n)
+    ws[off:off + b].zero_()
+    with kernel_path(mse.PATH_TENSORCORE), prefill_kernel(mse.PREFILL_PAIR):
+        old = mse.set_tuning(mse.TUNE_PAIR_SPLIT, 1)
+        try:
+            y = mse.mlp_swiglu_forward(dx, dgu, dwd, workspace=ws)
+            torch.cuda.synchronize()
+            h = ws[: T * I * 2].view(torch.int16).view(T, I).cpu().numpy().view(np.uint16).copy()
+            y_fresh = mse.mlp_swiglu_forward(dx, dgu, dwd)
+            y_again = mse.mlp_swiglu_forward(dx, dgu, dwd, workspace=ws)
+            mse.set_tuning(mse.TUNE_PAIR_SPLIT, 0)
+            y_whole = mse.mlp_swiglu_forward(dx, dgu, dwd)
+        finally:
+            mse.set_tuning(mse.TUNE_PAIR_SPLIT, old)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_fresh) and torch.equal(y, y_again)
+    assert int(torch.count_nonzero(ws[off:off + b]).item()) == 0
+    y_ref, _, h_ref = oracle.mlp_forward(x, wgu, wd)
+    assert_close(bits_f64(h), bits_f64(h_ref), f"h T={T}")
+    assert_close(bits_f64(to_bits(y)), bits_f64(y_ref), f"y T={T} split")
+    assert_close(bits_f64(to_bits(y_whole)), bits_f64(y_ref), f"y T={T} whole tiles")
+    assert mse.poll_device_error() == 0
+
+
 @pytest.mark.parametrize("T", [257, 300, 512, 700, 1000])
 @pytest.mark.parametrize("kind", [mse.PREFILL_SINGLE, mse.PREFILL_PAIR])
 def test_prefill_kernels_ragged(T, kind):
