@@ -1721,36 +1721,76 @@ __global__ void __launch_bounds__(kStdThreads, 1)
             // (token tiles are read by every tile of a column band, weight tiles once when the
             // launch has one token tile)
             const uint64_t pol_a = l2_policy_evict_last(), pol_b = l2_policy_evict_first();
+            auto rows = [&](const StdTile &t, int kb, int &k, int &a_row, int &b_row) {
+                k = (p.kb_first + t.group * p.kb_group_stride + kb) * 64;
+                a_row = t.m * 256 + (int)rank * 128;
+                b_row = p.b_base + t.n * p.b_n_stride + (int)rank * p.b_rank_stride;
+            };
+            int64_t id;
+            int kb0, kb1;
+            // Launches with one token tile stream their weights once: the weight tiles of the
+            // first stages (a fresh ring) are requested before the wait for the previous
+            // kernel, whose results only the token tiles can depend on.
+            int pre = 0;
+            if (p.cache_hints) {
+                for (int64_t i = 0; pre < S && work.seg(i, id, kb0, kb1); ++i) {
+                    const StdTile t = tile_of(id);
+                    for (int kb = kb0; kb < kb1 && pre < S; ++kb, ++pre) {
+                        int k, a_row, b_row;
+                        rows(t, kb, k, a_row, b_row);
+                        if (leader)
+                            mbar_arrive_expect_tx(bar_addr(&ctl->full[pre]), 2u * (kATileBytes + kPairBTileBytes));
+                        tma_load_2d_pair_hint(sB + pre * kPairBTileBytes, &tmB,
+                                              map_to_rank(bar_addr(&ctl->full[pre]), 0), k, b_row, pol_b);
+                    }
+                }
+            }
             pdl_wait();
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int64_t id;
-            int kb0, kb1;
             for (int64_t i = 0; ok && work.seg(i, id, kb0, kb1); ++i) {
                 const StdTile t = tile_of(id);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_bounded(bar_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.wait_limit_ns,
-                                           p.err)) {
-                        ok = false;
-                        break;
-                    }
                     const uint32_t fb = map_to_rank(bar_addr(&ctl->full[stage]), 0);
-                    if (leader)
-                        mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), 2u * (kATileBytes + kPairBTileBytes));
-                    const int k = (p.kb_first + t.group * p.kb_group_stride + kb) * 64;
-                    const int a_row = t.m * 256 + (int)rank * 128;
-                    const int b_row = p.b_base + t.n * p.b_n_stride + (int)rank * p.b_rank_stride;
-                    if (p.cache_hints) {
+                    int k, a_row, b_row;
+                    rows(t, kb, k, a_row, b_row);
+                    if (issued < pre) {   // its weight tile is requested already
                         tma_load_2d_pair_hint(sA + stage * kATileBytes, &tmA, fb, k, a_row, pol_a);
-                        tma_load_2d_pair_hint(sB + stage * kPairBTileBytes, &tmB, fb, k, b_row, pol_b);
                     } else {
-                        tma_load_2d_pair(sA + stage * kATileBytes, &tmA, fb, k, a_row);
-                        tma_load_2d_pair(sB + stage * kPairBTileBytes, &tmB, fb, k, b_row);
+                        if (!mbar_wait_bounded(bar_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag,
+                                               p.wait_limit_ns, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        if (leader)
+                            mbar_arrive_expect_tx(bar_addr(&ctl->full[stage]), 2u * (kATileBytes + kPairBTileBytes));
+                        if (p.cache_hints) {
+                            tma_load_2d_pair_hint(sA + stage * kATileBytes, &tmA, fb, k, a_row, pol_a);
+                            tma_load_2d_pair_hint(sB + stage * kPairBTileBytes, &tmB, fb, k, b_row, pol_b);
+                        } else {
+                            tma_load_2d_pair(sA + stage * kATileBytes, &tmA, fb, k, a_row);
+                            tma_load_2d_pair(sB + stage * kPairBTileBytes, &tmB, fb, k, b_row);
+                        }
                     }
                     ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
+            }
+            if (issued < pre) {
+                // (only after an abort: the token tiles of the stages whose weight tiles were
+                // requested, so that every expected byte lands before the teardown drains)
+                for (int64_t i = 0, u = 0; work.seg(i, id, kb0, kb1); ++i) {
+                    const StdTile t = tile_of(id);
+                    for (int kb = kb0; kb < kb1; ++kb, ++u) {
+                        if (u < issued || u >= pre) continue;
+                        int k, a_row, b_row;
+                        rows(t, kb, k, a_row, b_row);
+                        tma_load_2d_pair_hint(sA + (int)u * kATileBytes, &tmA, map_to_rank(bar_addr(&ctl->full[u]), 0),
+                                              k, a_row, pol_a);
+                    }
+                }
+                issued = pre;
             }
         }
     } else if (warp == 1) {
