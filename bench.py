@@ -874,17 +874,26 @@ def gpu_arm(args):
         per_rank = {}
         for tp in (4, 8, 16):
             t = rs.rank_partial(64, tp, K=args.aux_steps, Wm=args.warmup)
+            # the same steps with early token loads (the steps are independent: x is a buffer
+            # no kernel writes), as in the decode leg
+            old = mse.set_tuning(mse.TUNE_X_EARLY, 1)
+            te = rs.rank_partial(64, tp, K=args.aux_steps, Wm=args.warmup)
+            mse.set_tuning(mse.TUNE_X_EARLY, old)
             b = mlp_bytes(64, w.H, w.I // tp)
-            per_rank[f"tp{tp}"] = {"us": t * 1e6, "slice": w.I // tp, "tbps_algorithmic": b / t / 1e12,
-                                   "frac_of_hbm": b / t / 1e9 / peaks["hbm_gbs"], "timing": "CUDA graph replay"}
+            per_rank[f"tp{tp}"] = {"us": t * 1e6, "us_x_early": te * 1e6, "slice": w.I // tp,
+                                   "tbps_algorithmic": b / t / 1e12, "frac_of_hbm": b / t / 1e9 / peaks["hbm_gbs"],
+                                   "timing": "CUDA graph replay; us: library defaults, us_x_early: x_early=1"}
         extra["one_rank_partial_t64"] = per_rank
         del rs
         torch.cuda.empty_cache()
         w4 = W.MLA_MERGED
         s4 = bench_mla(w4, args.aux_steps, args.warmup)
+        old = mse.set_tuning(mse.TUNE_X_EARLY, 1)
+        s4e = bench_mla(w4, args.aux_steps, args.warmup)
+        mse.set_tuning(mse.TUNE_X_EARLY, old)
         C = w4.q_dim + w4.kv_dim
         b4 = C * w4.H * 2 + w4.T * w4.H * 2 + w4.T * C * 2
-        extra["mla_merged_tp16_t128"] = {"us": s4 * 1e6, "tbps_algorithmic": b4 / s4 / 1e12,
+        extra["mla_merged_tp16_t128"] = {"us": s4 * 1e6, "us_x_early": s4e * 1e6, "tbps_algorithmic": b4 / s4 / 1e12,
                                          "frac_of_hbm": b4 / s4 / 1e9 / peaks["hbm_gbs"],
                                          "outputs": "logical + rank-major", "weight_copies_cycled": 24}
     if clocks:

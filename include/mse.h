@@ -403,15 +403,17 @@ MSE_API int mse_set_prefill_kernel(int kind);
  *                         kernels above it (0 .. 256, default 160: at 176-256 tokens the full
  *                         layer measured 73 us on the CTA-pair kernel against 80-93 us); narrower
  *                         launches take the swap-AB kernels up to 256 tokens
- *   MSE_TUNE_X_EARLY      1 = mlp_swiglu_forward (decode-size kernels) reads its x without waiting
- *                         for the previous kernel on the stream when x overlaps neither the y nor
- *                         the workspace of the previous mlp_swiglu_forward call on that stream
- *                         and no other call of this library came between (independent layers or
- *                         requests streamed back to back): the gate_up weight stream then runs
- *                         during the previous layer's split-K tail.  Only for callers whose x is
- *                         not written by a kernel of their own that lets its dependents start
- *                         early (programmatic dependent launch) while still writing x.  0 =
- *                         always wait (default).
+ *   MSE_TUNE_X_EARLY      1 = mlp_swiglu_forward, mlp_swiglu_shard_partial, mlp_swiglu_shard_forward
+ *                         and merged_proj_forward (decode-size kernels) read their x without
+ *                         waiting for the previous kernel on the stream when x overlaps neither
+ *                         this call's workspace nor anything the previous call on that stream
+ *                         writes (its outputs and workspace), the previous call being one of
+ *                         these four (independent layers, ranks or requests streamed back to
+ *                         back): the first kernel's weight stream then runs during the previous
+ *                         call's split-K tail.  Only for callers whose x is not written by a
+ *                         kernel of their own that lets its dependents start early
+ *                         (programmatic dependent launch) while still writing x.  0 = always
+ *                         wait (default).
  *   MSE_TUNE_DOWN_FLAGS   decode token counts, two launches per layer: 1 = the gate_up kernel sets
  *                         a flag per finished 64-column block of h, and each CTA of the down
  *                         kernel, instead of waiting for the gate_up grid to complete, waits

@@ -840,7 +840,7 @@ int g_hostout_n = 0;
 // stream forgets the record (its kernels write other ranges).
 struct StreamWrites {
     void *stream;
-    uintptr_t lo[2], hi[2];
+    uintptr_t lo[3], hi[3];
     bool known;
 };
 StreamWrites g_writes[64];
@@ -860,16 +860,27 @@ bool x_independent_of_last_forward(void *stream, uintptr_t lo, uintptr_t hi) {
     std::lock_guard<std::mutex> lk(g_hostout_mu);
     const StreamWrites *w = stream_writes(stream);
     if (!w->known) return false;
-    for (int k = 0; k < 2; ++k)
+    for (int k = 0; k < 3; ++k)
         if (lo < w->hi[k] && w->lo[k] < hi) return false;
     return true;
 }
 
-void record_forward_writes(void *stream, uintptr_t y_lo, uintptr_t y_hi, uintptr_t ws_lo, uintptr_t ws_hi) {
+// The device ranges a call's kernels write (outputs and workspace; empty ranges allowed).
+void record_forward_writes(void *stream, uintptr_t y_lo, uintptr_t y_hi, uintptr_t ws_lo, uintptr_t ws_hi,
+                           uintptr_t z_lo = 0, uintptr_t z_hi = 0) {
     std::lock_guard<std::mutex> lk(g_hostout_mu);
     StreamWrites *w = stream_writes(stream);
-    w->lo[0] = y_lo; w->hi[0] = y_hi; w->lo[1] = ws_lo; w->hi[1] = ws_hi;
+    w->lo[0] = y_lo; w->hi[0] = y_hi; w->lo[1] = ws_lo; w->hi[1] = ws_hi; w->lo[2] = z_lo; w->hi[2] = z_hi;
     w->known = true;
+}
+
+// MSE_TUNE_X_EARLY for a call reading x [x, x + x_bytes) with workspace [ws, ws + ws_bytes):
+// x overlaps neither this call's workspace nor anything the previous call on the stream
+// writes (recorded in call order; no other call of this library came between).
+bool x_early_for(void *stream, const void *x, size_t x_bytes, const void *ws, size_t ws_bytes) {
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(ws);
+    return g_tune_x_early.load() != 0 && !(xa < wa + ws_bytes && wa < xa + x_bytes) &&
+           x_independent_of_last_forward(stream, xa, xa + x_bytes);
 }
 
 void forget_writes(void *stream) {
@@ -970,9 +981,8 @@ mse_status forward_impl(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, cons
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h_off);
     // MSE_TUNE_X_EARLY: x overlaps nothing the previous call on this stream writes (nor this
     // call's workspace); the record is forgotten until this call's launches succeed
-    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(workspace);
-    const bool x_early = !hx && g_tune_x_early.load() != 0 && !(xa < wa + workspace_bytes && wa < xa + T * H * 2) &&
-                         x_independent_of_last_forward(stream, xa, xa + (uintptr_t)(T * H * 2));
+    const uintptr_t wa = reinterpret_cast<uintptr_t>(workspace);
+    const bool x_early = !hx && x_early_for(stream, x, (size_t)(T * H * 2), workspace, workspace_bytes);
     if (hx && (path != PATH_TC || !hostx_supported(*d, T, H, I))) return MSE_ERR_UNSUPPORTED_SHAPE;
     forget_writes(stream);
 
@@ -1068,6 +1078,8 @@ mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int
     DeviceInfo *d = nullptr;
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
+    const size_t out_bytes = (size_t)rank_count * T * H * (partial_dtype == MSE_F32 ? 4 : 2);
+    const bool x_early = x_early_for(stream, x, (size_t)(T * H * 2), workspace, workspace_bytes);
     forget_writes(stream);
     const int64_t sw = I / tp;
     Path path;
@@ -1100,12 +1112,14 @@ mse_status mlp_swiglu_shard_partial(const mse_bf16 *x, int64_t T, int64_t H, int
         record(g_ev_mid, s);
     } else {
         const int fl = down_flags_epoch(*d, T, H, width, sw, rank_count);
-        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s, false, fl)) != MSE_OK) return st;
+        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s, x_early, fl)) != MSE_OK) return st;
         record(g_ev_mid, s);
         if ((st = tc_down(*d, h, T, H, I, w_down, j0, sw, rank_count, partials, epi, ws, L, s, fl)) != MSE_OK)
             return st;
     }
     record(g_ev_end, s);
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(partials), wa = reinterpret_cast<uintptr_t>(workspace);
+    record_forward_writes(stream, pa, pa + out_bytes, wa, wa + workspace_bytes);
     return MSE_OK;
 }
 
@@ -1125,6 +1139,8 @@ mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int
     DeviceInfo *d = nullptr;
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
+    const size_t out_bytes = (size_t)T * H * (out_dtype == MSE_F32 ? 4 : 2);
+    const bool x_early = x_early_for(stream, x, (size_t)(T * H * 2), workspace, workspace_bytes);
     forget_writes(stream);
     const int64_t sw = I / tp;
     Path path;
@@ -1157,11 +1173,13 @@ mse_status mlp_swiglu_shard_forward(const mse_bf16 *x, int64_t T, int64_t H, int
         record(g_ev_mid, s);
     } else {
         const int fl = down_flags_epoch(*d, T, H, width, width, 1);
-        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s, false, fl)) != MSE_OK) return st;
+        if ((st = tc_gate_up(*d, x, T, H, I, w_gate_up, j0, width, h, ws, L, s, x_early, fl)) != MSE_OK) return st;
         record(g_ev_mid, s);
         if ((st = tc_down(*d, h, T, H, I, w_down, j0, width, 1, out, epi, ws, L, s, fl)) != MSE_OK) return st;
     }
     record(g_ev_end, s);
+    const uintptr_t oa = reinterpret_cast<uintptr_t>(out), wa = reinterpret_cast<uintptr_t>(workspace);
+    record_forward_writes(stream, oa, oa + out_bytes, wa, wa + workspace_bytes);
     return MSE_OK;
 }
 
@@ -1267,6 +1285,7 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
     DeviceInfo *d = nullptr;
     mse_status st = current_device(&d);
     if (st != MSE_OK) return st;
+    const bool x_early = x_early_for(stream, x, (size_t)(T * H * 2), workspace, workspace_bytes);
     forget_writes(stream);
     const bool tc_ok = H % 64 == 0 && aligned16(x) && aligned16(w) && aligned16(workspace);
     Path path;
@@ -1296,8 +1315,16 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
         p.q_dim = q_dim; p.kv_dim = kv_dim; p.tp = tp;
         p.slots = reinterpret_cast<float *>(ws + L.slots_off);
         p.counters = reinterpret_cast<int *>(ws + L.cnt_off);
+        p.x_early = x_early ? 1 : 0;
         p.err = d->err;
-        return from_cuda(tc::launch_swapab(tc::EPI_MERGED, ta, tb, p, sh.grid, use_pdl(), sh.pair, s));
+        if ((st = from_cuda(tc::launch_swapab(tc::EPI_MERGED, ta, tb, p, sh.grid, use_pdl(), sh.pair, s))) !=
+            MSE_OK)
+            return st;
+        // what this call writes, for the next call's MSE_TUNE_X_EARLY
+        const uintptr_t la = reinterpret_cast<uintptr_t>(out_logical), ra = reinterpret_cast<uintptr_t>(out_rank_major);
+        const uintptr_t wa = reinterpret_cast<uintptr_t>(workspace), ob = (uintptr_t)(T * C * 2);
+        record_forward_writes(stream, la, la ? la + ob : 0, wa, wa + workspace_bytes, ra, ra ? ra + ob : 0);
+        return MSE_OK;
     }
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {

@@ -96,13 +96,15 @@ def test_options_independent_chained_and_replayed_calls(T, opts):
     assert int(torch.count_nonzero(ws[off:off + b]).item()) == 0   # the flags were cleared
 
 
+@pytest.mark.parametrize("opts", [(0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("tp,rank_count", [(4, 1), (8, 1), (16, 1), (8, 2), (8, 8)])
 @pytest.mark.parametrize("T", [64, 16])
-def test_down_flags_shard_entry_points(T, tp, rank_count):
-    """One rank's (or a group of ranks') shard launches with the flag handover: narrow gate_up
-    slices whose tiles are finished jointly by several CTAs (each finisher one slice of token
-    columns) must publish their h blocks too.  Ranks cycled back to back, eagerly and in a
-    replayed graph, give exactly the results without flags; the sync words end zero."""
+def test_options_shard_entry_points(T, tp, rank_count, opts):
+    """One rank's (or a group of ranks') shard launches with early token loads and/or the flag
+    handover: narrow gate_up slices whose tiles are finished jointly by several CTAs (each
+    finisher one slice of token columns) must publish their h blocks too.  Ranks cycled back
+    to back, eagerly and in a replayed graph, give exactly the results without the options;
+    the sync words end zero."""
     w = W.DECODE_T64
     wgu, wd = W.make_mlp_weights(w)
     g0, d0 = to_dev(wgu), to_dev(wd)
@@ -137,8 +139,8 @@ def test_down_flags_shard_entry_points(T, tp, rank_count):
         return res
 
     ref = with_options(0, 0, eager)
-    got = with_options(0, 1, eager)
-    got_r = with_options(0, 1, replayed)
+    got = with_options(*opts, eager)
+    got_r = with_options(*opts, replayed)
     for i, (a, b) in enumerate(zip(got, ref)):
         assert torch.equal(a, b), f"eager call {i}"
     for r in got_r:
@@ -147,3 +149,50 @@ def test_down_flags_shard_entry_points(T, tp, rank_count):
     assert mse.poll_device_error() == 0
     off, b = mse.mlp_swiglu_workspace_sync_range(T, w.H, w.I, ws.numel())
     assert int(torch.count_nonzero(ws[off:off + b]).item()) == 0
+
+
+@pytest.mark.parametrize("T", [128, 16])
+def test_x_early_merged_projection(T):
+    """merged_proj_forward with early token loads: independent calls with cycled weights, a
+    call whose x overlaps the previous call's output (the library sees it and waits), and a
+    replayed graph give exactly the results without the option."""
+    w = W.MLA_MERGED
+    H, q, kv, tp = w.H, w.q_dim, w.kv_dim, w.tp
+    C = q + kv
+    w0 = to_dev(W.make_merged_weight(w))
+    wts = [w0, torch.roll(w0, 13, 0).contiguous(), torch.roll(w0, 29, 0).contiguous()]
+    xs = [to_dev(W.make_custom(2300 + k, 0, (T, H))) for k in range(3)]
+    ws = mse.new_merged_workspace(T, H, q, kv)
+    big = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")   # an output that a later x reads
+
+    def run():
+        outs = []
+        for i in range(9):
+            lo, rm = mse.merged_proj_forward(xs[i % 3], wts[i % 3], q, kv, tp, workspace=ws)
+            outs += [lo, rm]
+        # the previous call writes into big; the next call reads big as its x
+        lo_big = big.view(-1)[: T * C].view(T, C)
+        mse.merged_proj_forward(xs[0], wts[1], q, kv, tp, out_logical=lo_big, workspace=ws)
+        lo2, rm2 = mse.merged_proj_forward(big, wts[2], q, kv, tp, workspace=ws)
+        outs += [lo2, rm2]
+        side = torch.cuda.Stream()
+        gl = [torch.empty((T, C), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for k in range(3):
+                mse.merged_proj_forward(xs[k], wts[(k + 1) % 3], q, kv, tp, out_logical=gl[k], workspace=ws,
+                                        stream=side)
+        for _ in range(2):
+            for t in gl:
+                t.zero_()
+            g.replay()
+            g.replay()
+        torch.cuda.synchronize()
+        return [t.clone() for t in outs + gl]
+
+    ref = with_options(0, 0, run)
+    big.zero_()
+    got = with_options(1, 0, run)
+    for i, (a, b) in enumerate(zip(got, ref)):
+        assert torch.equal(a, b), f"output {i}"
+    assert mse.poll_device_error() == 0
