@@ -354,7 +354,8 @@ MSE_API int mse_set_prefill_kernel(int kind);
 
 /* Tuning of the decode-size (swap-AB) kernels, process-wide, for later launches.
  *   MSE_TUNE_ISSUE_GROUP  consecutive 64-wide k-blocks per pipeline stage, i.e. each weight row
- *                         is fetched in runs of 128 x value contiguous bytes (1..4, default 2)
+ *                         is fetched in runs of 128 x value contiguous bytes (1..4); 0 (default)
+ *                         = 3 for launches of at most 64 tokens, 2 above
  *   MSE_TUNE_STAGES       shared-memory pipeline depth (0 = as many as fit, default)
  *   MSE_TUNE_CACHE_HINTS  1 = weights evict-first / tokens evict-last in L2 (default), 0 = none
  *   MSE_TUNE_GRID         CTAs of the stream-K grid (at most 160).  0 (default) = chosen per shape:

@@ -218,7 +218,7 @@ def test_product_path_does_not_import_oracle():
 
 # key: (default, accepted values, rejected values)
 TUNING = {
-    mse.TUNE_ISSUE_GROUP: (2, [1, 4], [0, 5]),
+    mse.TUNE_ISSUE_GROUP: (0, [0, 1, 4], [-1, 5]),
     mse.TUNE_STAGES: (0, [2, 12], [1, 13]),
     mse.TUNE_CACHE_HINTS: (1, [0, 1], [2, -1]),
     mse.TUNE_GRID: (0, [1, 160], [161, -1]),
@@ -229,6 +229,12 @@ TUNING = {
     mse.TUNE_PAIR_MIN_T: (0, [1, 256], [-1]),
     mse.TUNE_GRID_DOWN: (0, [1, 160], [161]),
     mse.TUNE_CLUSTER_FINISH: (0, [0, 1], [2]),
+    mse.TUNE_L2_PREFETCH: (8, [0, 256], [-1, 257]),
+    mse.TUNE_SWAPAB_MAX_T: (160, [0, 256], [-1, 257]),
+    mse.TUNE_X_EARLY: (0, [0, 1], [2, -1]),
+    mse.TUNE_DOWN_FLAGS: (0, [0, 1], [2, -1]),
+    mse.TUNE_HOST_X_COPIERS: (16, [0, 1, 1024], [-1, 1025]),
+    mse.TUNE_PAIR_SPLIT: (1, [0, 1], [2, -1]),
 }
 
 
