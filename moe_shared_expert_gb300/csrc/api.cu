@@ -555,7 +555,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
     if (hx) return MSE_ERR_UNSUPPORTED_SHAPE;
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
-        p.stages = tc::pair_stages();
+        p.stages = tc::pair_stages(T <= 256);
         if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
         if ((st = map_2d(&tb, w_gate_up, 2 * I, H, H, 128)) != MSE_OK) return st;
         p.n_mtiles = (int)((T + 255) / 256);
@@ -634,7 +634,7 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
     }
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
-        p.stages = tc::pair_stages();
+        p.stages = tc::pair_stages(T <= 256);
         if ((st = map_2d(&ta, h, T, I, I, 128)) != MSE_OK) return st;
         if ((st = map_2d(&tb, w_down, H, I, I, 128)) != MSE_OK) return st;
         p.n_mtiles = (int)((T + 255) / 256);
@@ -1332,7 +1332,7 @@ mse_status merged_proj_forward(const mse_bf16 *x, int64_t T, int64_t H, const ms
     }
     tc::StdParams p = std_base(T);
     if (use_pair(T)) {
-        p.stages = tc::pair_stages();
+        p.stages = tc::pair_stages(T <= 256);
         if ((st = map_2d(&ta, x, T, H, H, 128)) != MSE_OK) return st;
         if ((st = map_2d(&tb, w, C, H, H, 128)) != MSE_OK) return st;
         p.n_mtiles = (int)((T + 255) / 256);

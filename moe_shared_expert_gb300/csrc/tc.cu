@@ -2239,7 +2239,10 @@ cudaError_t launch_std(int epi, const CUtensorMap &ta, const CUtensorMap &tb, co
 
 
 size_t pair_smem_bytes(int stages) { return (size_t)stages * (kATileBytes + kPairBTileBytes) + 1024 + sizeof(Ctrl); }
-int pair_stages() { return 6; }
+// one token tile (up to 256 tokens, weights streamed once): seven stages of 32 KB (the
+// 256-token layer 65.1 against 66.3 us with six); prefill keeps six (1,939 against
+// 1,946-1,972 TFLOP/s with seven)
+int pair_stages(bool one_token_tile) { return one_token_tile ? 7 : 6; }
 
 cudaError_t launch_pair(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const StdParams &p, int clusters,
                         bool pdl, cudaStream_t s) {

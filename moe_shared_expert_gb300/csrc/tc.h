@@ -137,7 +137,7 @@ constexpr int kMaxPersistentGrid = 160; // cap on the persistent prefill grids
 size_t swapab_smem_bytes(int bn, int stages, int kbs);
 size_t std_smem_bytes(int stages);
 size_t pair_smem_bytes(int stages);
-int pair_stages();
+int pair_stages(bool one_token_tile);
 int swapab_stages_for(int bn, int kbs);
 int std_stages();
 
