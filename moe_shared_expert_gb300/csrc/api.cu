@@ -420,7 +420,16 @@ SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups,
     // a grid is set through the tuning keys.
     if (narrow && g_tune_grid.load() == 0 && (!down || g_tune_grid_down.load() == 0)) {
         const int cap = std::max((r.p.total_units + 15) / 16, std::min(d.sm_count, tc::kMaxGrid) / 2);
-        if (cap < r.grid) r.grid = cap;
+        if (cap < r.grid) {
+            r.grid = cap;
+            // gate_up slices: every tile in the same number of parts, one part per CTA, on
+            // about two thirds of the SMs (TP8's 12 tiles and TP16's 6 on 96 CTAs: one rank's
+            // step 19.5 against 20.2 us and 16.0 against 17.4, with early token loads 15.9
+            // against 16.4 and 13.8 against 15.6)
+            const int n_tiles = groups * n_real;
+            const int target = std::min(d.sm_count, tc::kMaxGrid) * 2 / 3;
+            if (!down && n_tiles <= target && kbp >= 2 * (target / n_tiles)) r.grid = n_tiles * (target / n_tiles);
+        }
     }
     // Down projections of a narrow slice (at most 24 k-blocks per tile, one shard's or a few
     // shards' columns): one CTA per whole tile when every tile has an SM, so no tile is split
