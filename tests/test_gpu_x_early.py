@@ -103,8 +103,8 @@ def test_options_shard_entry_points(T, tp, rank_count, opts):
     """One rank's (or a group of ranks') shard launches with early token loads and/or the flag
     handover: narrow gate_up slices whose tiles are finished jointly by several CTAs (each
     finisher one slice of token columns) must publish their h blocks too.  Ranks cycled back
-    to back, eagerly and in a replayed graph, give exactly the results without the options;
-    the sync words end zero."""
+    to back, eagerly and in a replayed graph, match the results without the options; the sync
+    words end zero."""
     w = W.DECODE_T64
     wgu, wd = W.make_mlp_weights(w)
     g0, d0 = to_dev(wgu), to_dev(wd)
@@ -140,12 +140,22 @@ def test_options_shard_entry_points(T, tp, rank_count, opts):
 
     ref = with_options(0, 0, eager)
     got = with_options(*opts, eager)
+    again = with_options(*opts, eager)
     got_r = with_options(*opts, replayed)
+    # With early token loads a shard's gate_up grid may differ (it is sized to run beside the
+    # previous call's down kernel), so the fp32 split-K sums may run in another order: the
+    # results are compared with the default path within the bf16 tolerance of the layer, and
+    # bit for bit between identical runs and between the replays of a graph.
+    def close(a, b):
+        return torch.allclose(a.float(), b.float(), rtol=0.02, atol=0.02)
     for i, (a, b) in enumerate(zip(got, ref)):
-        assert torch.equal(a, b), f"eager call {i}"
+        assert close(a, b), f"eager call {i}"
+    for i, (a, b) in enumerate(zip(got, again)):
+        assert torch.equal(a, b), f"eager call {i}, second run"
     for r in got_r:
         for k in range(len(firsts)):
-            assert torch.equal(r[k], ref[2 * k]), f"graph rank group {k}"   # eager order: partial, forward
+            assert close(r[k], ref[2 * k]), f"graph rank group {k}"   # eager order: partial, forward
+            assert torch.equal(r[k], got_r[0][k]), f"graph rank group {k}, replays differ"
     assert mse.poll_device_error() == 0
     off, b = mse.mlp_swiglu_workspace_sync_range(T, w.H, w.I, ws.numel())
     assert int(torch.count_nonzero(ws[off:off + b]).item()) == 0
