@@ -355,9 +355,16 @@ int stream_k_grid(int units, int kbp, int g_max) {
             best = G;
         }
     }
-    // fewer CTAs pay only where tiles end up split in at most three parts (the merged
-    // projection's tiles are split about nine ways: 138 CTAs measured slower than 152)
-    if (best_parts > 3) best = g_max;
+    // Fewer CTAs pay where tiles end up split in at most three parts.  Tiles split more ways
+    // (the merged projection's 17 tiles of 112 k-blocks) take the grid that puts every tile in
+    // the same number of parts, one part per CTA, when it keeps at least 80% of the SMs: 136
+    // CTAs measured 14.8 against 16.3 us (13.9 against 16.1 with early token loads), where 138
+    // or 152 CTAs leave parts straddling tiles.
+    if (best_parts > 3) {
+        const int64_t per = n_tiles > 0 ? g_max / n_tiles : 0;
+        const int64_t aligned = n_tiles * per;
+        best = (per >= 2 && kbp >= per && 5 * aligned >= 4LL * g_max) ? (int)aligned : g_max;
+    }
     std::lock_guard<std::mutex> lk(mu);
     if (cache.size() > 4096) cache.clear();
     cache.emplace(key, best);
