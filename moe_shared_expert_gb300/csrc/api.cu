@@ -438,6 +438,16 @@ SwapAbShape swapab_shape(const DeviceInfo &d, int64_t T, int n_real, int groups,
             if (!down && n_tiles <= target && kbp >= 2 * (target / n_tiles)) r.grid = n_tiles * (target / n_tiles);
         }
     }
+    // gate_up launches of at least 128 tokens over at least half as many tiles as SMs (the
+    // full layer's 96): one CTA per whole tile, no split-K finish (the layer at 128 / 160
+    // tokens 62.3 / 66.5 against 63.1 / 68.7 us, 59.3 / 61.6 against 60.8 / 66.4 with early
+    // token loads and h flags; TP8 as partials at 128 tokens 65.9 against 68.0); at 80-96
+    // tokens the stream-K split stays ahead by 0.3-1 us.
+    {
+        const int n_tiles = groups * n_real, g_cap = std::min(d.sm_count, tc::kMaxGrid);
+        if (!down && g_tune_grid.load() == 0 && r.p.bn >= 128 && 2 * n_tiles >= g_cap && n_tiles <= g_cap)
+            r.grid = n_tiles;
+    }
     // Down projections of a narrow slice (at most 24 k-blocks per tile, one shard's or a few
     // shards' columns): one CTA per whole tile when every tile has an SM, so no tile is split
     // and no split-K finish runs (one rank's step at 64 tokens: TP8 20.3 against 27.1 us,
