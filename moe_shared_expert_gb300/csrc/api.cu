@@ -620,6 +620,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         p.err = d.err;
         int clusters = pair_clusters(d, (int64_t)p.n_mtiles * p.n_ntiles);
         p.cache_hints = T <= 256 ? g_tune_cache_hints.load() : 0;   // weights streamed once
+        p.x_early = x_early && T <= 256 ? 1 : 0;
         if (T <= kSwapAbMaxT && T > 128) {
             const int c = pair_split_clusters(d, (int64_t)p.n_mtiles * p.n_ntiles, p.kb_per_tile);
             if (c > 0) {
@@ -650,7 +651,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
 // intermediate columns starting at column kcol0 + g * s_width.
 mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H, int64_t I, const uint16_t *w_down,
                    int64_t kcol0, int64_t s_width, int groups, void *out, int epi, char *ws, const MlpWs &L,
-                   cudaStream_t s, int flags = 0) {
+                   cudaStream_t s, int flags = 0, bool coreside = false) {
     CUtensorMap ta, tb;
     mse_status st;
     // the same choice as the layer's gate_up launch (its rows: 2 x the intermediate columns)
@@ -702,7 +703,9 @@ mse_status tc_down(const DeviceInfo &d, const uint16_t *h, int64_t T, int64_t H,
         const int64_t n_tiles = (int64_t)groups * p.n_mtiles * p.n_ntiles;
         int clusters = pair_clusters(d, n_tiles);
         p.cache_hints = T <= 256 ? g_tune_cache_hints.load() : 0;   // weights streamed once
-        if (T <= kSwapAbMaxT && T > 128) {
+        // coreside (calls streamed with early token loads): whole tiles, so that the next
+        // call's gate_up grid fits on the SMs this launch leaves free and streams beside it
+        if (T <= kSwapAbMaxT && T > 128 && !coreside) {
             const int c = pair_split_clusters(d, n_tiles, p.kb_per_tile);
             if (c > 0) {
                 p.split_k = 1;
@@ -1068,7 +1071,8 @@ mse_status forward_impl(const mse_bf16 *x, int64_t T, int64_t H, int64_t I, cons
                                  x_early ? swapab_down_grid(*d, T, H, I, 1) : 0)) != MSE_OK)
                 return st;
             record(g_ev_mid, s);
-            if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s, fl)) != MSE_OK) return st;
+            if ((st = tc_down(*d, h, T, H, I, w_down, 0, I, 1, y, tc::EPI_BF16, ws, L, s, fl, x_early)) != MSE_OK)
+                return st;
         }
     }
     record(g_ev_end, s);

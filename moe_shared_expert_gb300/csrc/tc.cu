@@ -1745,7 +1745,7 @@ __global__ void __launch_bounds__(kStdThreads, 1)
                     }
                 }
             }
-            pdl_wait();
+            if (!p.x_early) pdl_wait();
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;

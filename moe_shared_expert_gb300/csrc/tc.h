@@ -122,6 +122,9 @@ struct StdParams {
     float *slots;
     int *counters;
     int cache_hints;       // CTA-pair kernel: 1 = B (weights) evict_first, A (tokens) evict_last in L2
+    int x_early;           // CTA-pair kernel: the A operand (tokens) is not written by the previous
+                           // kernel on the stream, so the producer does not wait for that kernel
+                           // (the epilogue still waits before any store)
     uint64_t wait_limit_ns;
     uint32_t *err;
 };

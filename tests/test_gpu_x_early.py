@@ -41,7 +41,7 @@ def with_options(x_early, down_flags, fn):
 
 
 @pytest.mark.parametrize("opts", [(1, 0), (0, 1), (1, 1)])
-@pytest.mark.parametrize("T", [64, 16])
+@pytest.mark.parametrize("T", [64, 16, 256, 192])
 def test_options_independent_chained_and_replayed_calls(T, opts):
     w = W.DECODE_T64
     wgu, wd = W.make_mlp_weights(w)
@@ -83,14 +83,26 @@ def test_options_independent_chained_and_replayed_calls(T, opts):
 
     ref_i, ref_c = with_options(0, 0, independent), with_options(0, 0, chained)
     got_i, got_c = with_options(*opts, independent), with_options(*opts, chained)
+    again_i = with_options(*opts, independent)
     got_r = with_options(*opts, replayed)
+    # With early token loads the 129-256-token layer runs its down projection on whole tiles
+    # (so that the next call's gate_up streams beside it), which sums in another order than
+    # the split tiles: the results match the default path within the layer's bf16 tolerance
+    # there, and bit for bit elsewhere, between identical runs and between graph replays.
+    exact = T <= 128 or opts[0] == 0
+
+    def same(a, b):
+        return torch.equal(a, b) if exact else torch.allclose(a.float(), b.float(), rtol=0.02, atol=0.02)
     for i, (a, b) in enumerate(zip(got_i, ref_i)):
-        assert torch.equal(a, b), f"independent call {i}"
+        assert same(a, b), f"independent call {i}"
+    for i, (a, b) in enumerate(zip(got_i, again_i)):
+        assert torch.equal(a, b), f"independent call {i}, second run"
     for i, (a, b) in enumerate(zip(got_c, ref_c)):
-        assert torch.equal(a, b), f"chained layer {i}"
+        assert same(a, b), f"chained layer {i}"
     for r in got_r:
         for k in range(3):
-            assert torch.equal(r[k], ref_i[k]), f"graph call {k}"
+            assert same(r[k], ref_i[k]), f"graph call {k}"
+            assert torch.equal(r[k], got_r[0][k]), f"graph call {k}, replays differ"
     assert mse.poll_device_error() == 0
     off, b = mse.mlp_swiglu_workspace_sync_range(T, w.H, w.I, ws.numel())
     assert int(torch.count_nonzero(ws[off:off + b]).item()) == 0   # the flags were cleared
