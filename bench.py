@@ -644,6 +644,28 @@ def rank_bench(args):
                       "tbps_algorithmic": b / t / 1e12, "gpu_launches": 2 * args.steps}), flush=True)
 
 
+def mla_bench(args):
+    """The merged MLA projection alone (logical + rank-major outputs, T = 128, TP16 layout),
+    eager launches cycling 24 weight copies: the small command that profiles of its kernel
+    are taken on."""
+    import torch
+    torch.cuda.set_device(0)
+    from moe_shared_expert_gb300 import _build
+    _build.build()
+    import moe_shared_expert_gb300 as mse
+    mse.lib()
+    tuning = apply_tuning(args.tune)
+    w = W.MLA_MERGED
+    t = bench_mla(w, args.steps, args.warmup)
+    C = w.q_dim + w.kv_dim
+    b = C * w.H * 2 + w.T * w.H * 2 + w.T * C * 2
+    print(json.dumps({"metric": "merged MLA projection", "value": t * 1e6, "unit": "us", "n_gpus": 1,
+                      "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": w.name, "T": w.T, "H": w.H, "q_dim": w.q_dim, "kv_dim": w.kv_dim,
+                                 "tp": w.tp, "timing": "eager launches", "tuning": tuning},
+                      "tbps_algorithmic": b / t / 1e12, "gpu_launches": args.steps}), flush=True)
+
+
 def collectives_model_s(T, H, tp, alpha_s, beta_Bps):
     """Modelled time of the block's two collectives (all-gather of the tokens, reduce-scatter
     of the bf16 partials): each alpha + (tp-1)/tp * T*H*2 bytes / beta."""
@@ -1038,7 +1060,7 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--aux-steps", type=int, default=2000)
     ap.add_argument("--decode-only", action="store_true", help="same as --only decode")
-    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill", "tp-sweep", "rank"])
+    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill", "tp-sweep", "rank", "mla"])
     ap.add_argument("--sweep-tokens", default="16,32,64,128,256,512,1024,2048")
     ap.add_argument("--sweep-tp", default="4,8,16")
     ap.add_argument("--coll-alpha-us", type=float, default=10.0,
@@ -1067,6 +1089,8 @@ def main():
         tp_sweep(args)
     elif args.only == "rank":
         rank_bench(args)
+    elif args.only == "mla":
+        mla_bench(args)
     else:
         gpu_arm(args)
 
