@@ -304,10 +304,15 @@ def one_launch_active() -> bool:
 # the previous step writes: MSE_TUNE_X_EARLY lets each layer's gate_up weight stream start
 # during the previous layer's split-K tail; with it, 12 k-blocks of L2 prefetch measured best,
 # and MSE_TUNE_DOWN_FLAGS (the down kernel starts on each h block as soon as the gate_up
-# kernel publishes it) took the layer from 53.6 to 50.2 us.  The time with the library's
-# default settings is reported beside the headline.
-DECODE_TUNING = "x_early=1,l2_prefetch=12,down_flags=1"
-LIBRARY_DEFAULTS = (("x_early", 0), ("l2_prefetch", 8), ("down_flags", 0))
+# kernel publishes it) took the layer from 53.6 to 50.2 us.  With these, the down projection
+# on 128 CTAs (the library's rule takes 140, the largest grid near all SMs whose tiles are
+# split at most three ways) measured 48.6 against 50.1 us, three alternating rounds on one
+# box (144 and 152 CTAs: 48.3 and 48.5, but 144 also read 53.4 once).  It leaves 24 SMs to
+# the next layer's first CTAs, which copy x in the host-buffer (e2e) step: 52.9 us there
+# against 53.0-53.1 with 144.  The time with the library's default settings is reported
+# beside the headline.
+DECODE_TUNING = "x_early=1,l2_prefetch=12,down_flags=1,grid_down=128"
+LIBRARY_DEFAULTS = (("x_early", 0), ("l2_prefetch", 8), ("down_flags", 0), ("grid_down", 0))
 
 
 def bench_mlp(w, K, Wm, layers, dist, clocks=None, phase_steps=200, e2e_steps=None, spread_steps=2000,

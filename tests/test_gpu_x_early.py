@@ -218,3 +218,50 @@ def test_x_early_merged_projection(T):
     for i, (a, b) in enumerate(zip(got, ref)):
         assert torch.equal(a, b), f"output {i}"
     assert mse.poll_device_error() == 0
+
+
+def test_bench_decode_tuning_matches_oracle():
+    """The settings the bench's decode leg runs with (early token loads, the h flag handover,
+    L2 prefetch, the down projection's grid), on the 64-token decode workload: calls streamed
+    back to back over two weight copies give every row within tolerance of the oracle, and the
+    same bits on a second run."""
+    import numpy as np
+
+    import bench
+    import oracle
+    from tests.helpers import assert_close, bits_f64, to_bits
+
+    w = W.DECODE_T64
+    wgu, wd = W.make_mlp_weights(w)
+    x = W.make_x(w)
+    dx, g0, d0 = to_dev(x), to_dev(wgu), to_dev(wd)
+    gus = [g0, torch.roll(g0, 977, 0).contiguous()]
+    wds = [d0, torch.roll(d0, 331, 0).contiguous()]
+    ws = mse.new_mlp_workspace(w.T, w.H, w.I)
+    olds = []
+    try:
+        for item in bench.DECODE_TUNING.split(","):
+            name, v = item.split("=")
+            olds.append((getattr(mse, "TUNE_" + name.upper()), mse.set_tuning(getattr(mse, "TUNE_" + name.upper()),
+                                                                               int(v))))
+            assert olds[-1][1] >= 0, item
+
+        def run():
+            ys = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+            for i, y in enumerate(ys):
+                mse.mlp_swiglu_forward(dx, gus[i % 2], wds[i % 2], y=y, workspace=ws)
+            torch.cuda.synchronize()
+            return ys
+        ys, again = run(), run()
+    finally:
+        for key, o in reversed(olds):
+            mse.set_tuning(key, o)
+    refs = [oracle.mlp_forward(x, wgu, wd)[0],
+            oracle.mlp_forward(x, np.roll(wgu, 977, 0), np.roll(wd, 331, 0))[0]]
+    for i in range(8):
+        assert_close(bits_f64(to_bits(ys[i])), bits_f64(refs[i % 2]), f"call {i}")
+    for i, (a, b) in enumerate(zip(ys, again)):
+        assert torch.equal(a, b), f"call {i}, second run"
+    assert mse.poll_device_error() == 0
+    off, b = mse.mlp_swiglu_workspace_sync_range(w.T, w.H, w.I, ws.numel())
+    assert int(torch.count_nonzero(ws[off:off + b]).item()) == 0
