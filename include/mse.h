@@ -451,6 +451,25 @@ typedef enum {
 } mse_tune_key;
 MSE_API int mse_set_tuning(int key, int value);
 
+/* Launch plan of the decode-size (swap-AB) kernels of an MLP call, computed on the host
+ * without a GPU: the CTA counts that mlp_swiglu_forward (tp = 1, rank_count = 1) or a
+ * group of rank_count consecutive ranks of a tp-way split (mlp_swiglu_shard_partial /
+ * mlp_swiglu_shard_forward, slices of I / tp intermediate columns; pages P1 "Change",
+ * P2 "关键源码片段") would launch for T tokens on a device with sm_count SMs, with the
+ * tuning keys as currently set; x_early = 1 when the call's early token loads apply (a
+ * streamed call whose x the previous call does not write, MSE_TUNE_X_EARLY).
+ * out[8] (host memory, written): [0] 1 when the call takes the swap-AB kernels, 0 when it
+ * takes the prefill or the generic kernels (shapes off the 64-column grid, or
+ * mse_set_kernel_path(MSE_PATH_GENERIC); then [1..7] are 0); [1] gate_up CTAs; [2] down
+ * CTAs; [3] / [4] the largest number of CTAs a gate_up / down tile is split between;
+ * [5] token tile width (T rounded up to 16); [6] k-blocks per pipeline stage; [7] stages.
+ * Returns MSE_OK; MSE_ERR_INVALID_ARG (null out, non-positive size, rank_count outside
+ * [1, tp]); MSE_ERR_NOT_DIVISIBLE (I by tp); MSE_ERR_UNSUPPORTED_SHAPE when a tuning key
+ * makes the shape depend on the device's occupancy (MSE_TUNE_ONE_LAUNCH,
+ * MSE_TUNE_PAIR_MIN_T, MSE_TUNE_CLUSTER_FINISH). */
+MSE_API int mse_mlp_launch_plan(int64_t T, int64_t H, int64_t I, int tp, int rank_count, int x_early,
+                                int sm_count, int32_t *out);
+
 /* Failure-detection self test: launches one CTA that waits on a barrier no one
  * arrives on, bounded by `limit_ns`.  The wait runs out by design; the kernel
  * records MSE_ERR_TIMEOUT in the device error word and returns, leaving the

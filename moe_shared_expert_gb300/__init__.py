@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
                 "mse_set_kernel_path": (ci, [ci]),
                 "mse_set_prefill_kernel": (ci, [ci]),
                 "mse_set_tuning": (ci, [ci, ci]),
+                "mse_mlp_launch_plan": (ci, [i64, i64, i64, ci, ci, ci, ci, P]),
                 "mse_selftest_wait_timeout": (ci, [u64, P]),
                 "mse_set_phase_events": (None, [P, P, P]),
                 "mse_status_string": (ctypes.c_char_p, [ci]),
@@ -377,6 +378,17 @@ def set_kernel_path(path: int) -> int:
 
 def set_tuning(key: int, value: int) -> int:
     return int(lib().mse_set_tuning(int(key), int(value)))
+
+
+def mlp_launch_plan(T: int, H: int, I: int, tp: int = 1, rank_count: int = 1, x_early: bool = False,
+                    sm_count: int = 152) -> dict:
+    """CTA counts of the decode-size kernels of an MLP call (host-side, no GPU): see
+    mse_mlp_launch_plan in include/mse.h."""
+    out = (ctypes.c_int32 * 8)()
+    _check("mse_mlp_launch_plan", lib().mse_mlp_launch_plan(int(T), int(H), int(I), int(tp), int(rank_count),
+                                                             int(bool(x_early)), int(sm_count), out))
+    keys = ("swapab", "gate_up_ctas", "down_ctas", "gate_up_parts", "down_parts", "bn", "kbs", "stages")
+    return {k: int(v) for k, v in zip(keys, out)}
 
 
 def set_prefill_kernel(kind: int) -> int:

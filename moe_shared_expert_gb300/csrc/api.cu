@@ -544,6 +544,22 @@ struct HostX {
 // epoch the flags of this call carry, or 0 for no flags.
 int down_flags_epoch(const DeviceInfo &d, int64_t T, int64_t H, int64_t width, int64_t s_width, int groups);
 
+// Early token loads: a gate_up grid streams while the previous call's down kernel (of the
+// same shape as this call's, down_grid CTAs) finishes.  When that kernel leaves at least a
+// third of the SMs free, as a shard's narrow down projection does, the grid takes those SMs,
+// every tile in the same number of parts and one part per CTA, so that the two kernels run
+// side by side (one rank's step at 64 tokens, TP4: 19.8 against 25.4 us).  n_gt: gate_up
+// tiles; kbp: their k-blocks.
+void coreside_gate_up_grid(const DeviceInfo &d, int n_gt, int kbp, int down_grid, SwapAbShape &sh) {
+    const int free_sms = std::min(d.sm_count, tc::kMaxGrid) - down_grid;
+    if (down_grid > 0 && !sh.pair && g_tune_grid.load() == 0 && 3 * free_sms >= d.sm_count && n_gt <= free_sms &&
+        kbp >= 2 * (free_sms / n_gt)) {
+        sh.grid = n_gt * (free_sms / n_gt);
+        if (sh.p.total_units < 32LL * sh.grid) sh.p.l2_prefetch_kb = 0;
+        sh.p.l2_prefetch_from = std::max(0, d.sm_count - sh.grid);
+    }
+}
+
 mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t H, int64_t I,
                       const uint16_t *w_gate_up, int64_t j_begin, int64_t width, uint16_t *h, char *ws,
                       const MlpWs &L, cudaStream_t s, bool x_early = false, int flags = 0,
@@ -554,19 +570,7 @@ mse_status tc_gate_up(const DeviceInfo &d, const uint16_t *x, int64_t T, int64_t
         const int kbp = (int)(H / 64);
         SwapAbShape sh = swapab_shape(d, T, (int)(width / 64), 1, kbp, false, true);
         tc::SwapAbParams &p = sh.p;
-        // Early token loads: this grid streams while the previous call's down kernel finishes.
-        // When that kernel (of the same shape as this call's, down_grid CTAs) leaves at least a
-        // third of the SMs free, as a shard's narrow down projection does, the grid takes those
-        // SMs, every tile in the same number of parts and one part per CTA, so that the two
-        // kernels run side by side (one rank's step at 64 tokens, TP4: 19.8 against 25.4 us).
-        const int free_sms = std::min(d.sm_count, tc::kMaxGrid) - down_grid;
-        const int n_gt = (int)(width / 64);
-        if (x_early && down_grid > 0 && !sh.pair && g_tune_grid.load() == 0 && 3 * free_sms >= d.sm_count &&
-            n_gt <= free_sms && kbp >= 2 * (free_sms / n_gt)) {
-            sh.grid = n_gt * (free_sms / n_gt);
-            if (p.total_units < 32LL * sh.grid) p.l2_prefetch_kb = 0;
-            p.l2_prefetch_from = std::max(0, d.sm_count - sh.grid);
-        }
+        if (x_early) coreside_gate_up_grid(d, (int)(width / 64), kbp, down_grid, sh);
         if ((st = map_gate_up_interleaved(&ta, w_gate_up, H, I)) != MSE_OK) return st;
         if ((st = map_2d(&tb, x, T, H, H, sh.b_box_rows)) != MSE_OK) return st;
         p.n_groups = 1;
@@ -1476,6 +1480,40 @@ int mse_set_kernel_path(int path) {
 int mse_set_prefill_kernel(int kind) {
     if (kind < MSE_PREFILL_AUTO || kind > MSE_PREFILL_PAIR) return g_prefill.load();
     return g_prefill.exchange(kind);
+}
+
+int mse_mlp_launch_plan(int64_t T, int64_t H, int64_t I, int tp, int rank_count, int x_early, int sm_count,
+                        int32_t *out) {
+    if (!out || T < 1 || H < 1 || I < 1 || tp < 1 || rank_count < 1 || rank_count > tp || sm_count < 1)
+        return MSE_ERR_INVALID_ARG;
+    for (int i = 0; i < 8; ++i) out[i] = 0;
+    if (I % tp != 0) return MSE_ERR_NOT_DIVISIBLE;
+    const int64_t sw = I / tp, width = (int64_t)rank_count * sw;
+    // the generic kernels (shapes off the 64-column grid, or that path forced)
+    if (H % 64 != 0 || sw % 64 != 0 || g_path.load() == MSE_PATH_GENERIC) return MSE_OK;
+    // options whose shapes depend on occupancy queries of a device
+    if (one_launch_enabled(T) || g_tune_pair_min_t.load() > 0 || g_tune_cluster_finish.load() != 0)
+        return MSE_ERR_UNSUPPORTED_SHAPE;
+    if (!use_swapab(T, 2 * width)) return MSE_OK;    // the prefill kernels
+    DeviceInfo d;
+    d.init = true;
+    d.supported = true;
+    d.sm_count = sm_count;
+    const int kbp = (int)(H / 64);
+    SwapAbShape gu = swapab_shape(d, T, (int)(width / 64), 1, kbp, false, true);
+    gu.p.kb_per_tile = kbp;
+    if (x_early) coreside_gate_up_grid(d, (int)(width / 64), kbp, swapab_down_grid(d, T, H, sw, rank_count), gu);
+    SwapAbShape dn = swapab_shape(d, T, (int)((H + 127) / 128), rank_count, (int)(sw / 64), true, true);
+    dn.p.kb_per_tile = (int)(sw / 64);
+    out[0] = 1;
+    out[1] = gu.grid;
+    out[2] = dn.grid;
+    out[3] = tc::swapab_max_parts(gu.p, gu.grid);
+    out[4] = tc::swapab_max_parts(dn.p, dn.grid);
+    out[5] = gu.p.bn;
+    out[6] = gu.p.kbs;
+    out[7] = gu.p.stages;
+    return MSE_OK;
 }
 
 int mse_set_tuning(int key, int value) {
