@@ -470,6 +470,16 @@ MSE_API int mse_set_tuning(int key, int value);
 MSE_API int mse_mlp_launch_plan(int64_t T, int64_t H, int64_t I, int tp, int rank_count, int x_early,
                                 int sm_count, int32_t *out);
 
+/* The same for merged_proj_forward (page P4 "Behavior": the 2112 x 7168 merged q_a / kv_a
+ * projection).  out[8]: [0] 1 when the call takes the swap-AB kernel (0: the prefill or the
+ * generic kernels, then [1..7] are 0); [1] CTAs; [2] the largest number of CTAs a 128-row
+ * weight tile is split between; [3] 1 when the tiles' parts are finished jointly (every part's
+ * CTA sums a slice of the token columns, MSE_TUNE_COOP_FINISH); [4] token tile width;
+ * [5] k-blocks per pipeline stage; [6] stages; [7] 0.  Errors as mse_mlp_launch_plan (q_dim
+ * and kv_dim by tp for MSE_ERR_NOT_DIVISIBLE). */
+MSE_API int mse_merged_launch_plan(int64_t T, int64_t H, int64_t q_dim, int64_t kv_dim, int tp, int sm_count,
+                                   int32_t *out);
+
 /* Failure-detection self test: launches one CTA that waits on a barrier no one
  * arrives on, bounded by `limit_ns`.  The wait runs out by design; the kernel
  * records MSE_ERR_TIMEOUT in the device error word and returns, leaving the

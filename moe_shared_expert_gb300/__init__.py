@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
                 "mse_set_prefill_kernel": (ci, [ci]),
                 "mse_set_tuning": (ci, [ci, ci]),
                 "mse_mlp_launch_plan": (ci, [i64, i64, i64, ci, ci, ci, ci, P]),
+                "mse_merged_launch_plan": (ci, [i64, i64, i64, i64, ci, ci, P]),
                 "mse_selftest_wait_timeout": (ci, [u64, P]),
                 "mse_set_phase_events": (None, [P, P, P]),
                 "mse_status_string": (ctypes.c_char_p, [ci]),
@@ -388,6 +389,16 @@ def mlp_launch_plan(T: int, H: int, I: int, tp: int = 1, rank_count: int = 1, x_
     _check("mse_mlp_launch_plan", lib().mse_mlp_launch_plan(int(T), int(H), int(I), int(tp), int(rank_count),
                                                              int(bool(x_early)), int(sm_count), out))
     keys = ("swapab", "gate_up_ctas", "down_ctas", "gate_up_parts", "down_parts", "bn", "kbs", "stages")
+    return {k: int(v) for k, v in zip(keys, out)}
+
+
+def merged_launch_plan(T: int, H: int, q_dim: int, kv_dim: int, tp: int, sm_count: int = 152) -> dict:
+    """CTA count and split of the merged projection's kernel (host-side, no GPU): see
+    mse_merged_launch_plan in include/mse.h."""
+    out = (ctypes.c_int32 * 8)()
+    _check("mse_merged_launch_plan", lib().mse_merged_launch_plan(int(T), int(H), int(q_dim), int(kv_dim), int(tp),
+                                                                   int(sm_count), out))
+    keys = ("swapab", "ctas", "parts", "joint_finish", "bn", "kbs", "stages")
     return {k: int(v) for k, v in zip(keys, out)}
 
 

@@ -1516,6 +1516,32 @@ int mse_mlp_launch_plan(int64_t T, int64_t H, int64_t I, int tp, int rank_count,
     return MSE_OK;
 }
 
+int mse_merged_launch_plan(int64_t T, int64_t H, int64_t q_dim, int64_t kv_dim, int tp, int sm_count, int32_t *out) {
+    if (!out || T < 1 || H < 1 || q_dim < 1 || kv_dim < 1 || tp < 1 || sm_count < 1) return MSE_ERR_INVALID_ARG;
+    for (int i = 0; i < 8; ++i) out[i] = 0;
+    if (q_dim % tp != 0 || kv_dim % tp != 0) return MSE_ERR_NOT_DIVISIBLE;
+    if (H % 64 != 0 || g_path.load() == MSE_PATH_GENERIC) return MSE_OK;   // the generic kernels
+    const int64_t C = q_dim + kv_dim;
+    if (!use_swapab(T, C)) return MSE_OK;   // the prefill kernels
+    if (g_tune_pair_min_t.load() > 0 || g_tune_cluster_finish.load() != 0) return MSE_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo d;
+    d.init = true;
+    d.supported = true;
+    d.sm_count = sm_count;
+    const int kbp = (int)(H / 64);
+    SwapAbShape sh = swapab_shape(d, T, (int)((C + 127) / 128), 1, kbp);
+    sh.p.kb_per_tile = kbp;
+    const int parts = tc::swapab_max_parts(sh.p, sh.grid);
+    out[0] = 1;
+    out[1] = sh.grid;
+    out[2] = parts;
+    out[3] = sh.p.coop_finish > 0 && parts >= sh.p.coop_finish ? 1 : 0;
+    out[4] = sh.p.bn;
+    out[5] = sh.p.kbs;
+    out[6] = sh.p.stages;
+    return MSE_OK;
+}
+
 int mse_set_tuning(int key, int value) {
     std::atomic<int> *slot = nullptr;
     bool ok = false;

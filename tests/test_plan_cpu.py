@@ -157,3 +157,38 @@ def test_plan_errors_and_unsupported_options():
         finally:
             mse.set_tuning(key, old)
     assert plan(64)["swapab"] == 1
+
+
+# -------------------------------------------------------------------- merged projection
+Q, KV, TP16 = 1536, 576, 16   # q_a and kv_a rows of the merged projection, TP16 layout
+
+
+def test_merged_projection_aligned_grid():
+    # 17 weight tiles of 128 rows (2112 rows) and 112 k-blocks: every grid near all SMs splits
+    # some tile more than three ways, so the launch takes the grid that puts every tile in the
+    # same number of parts (136 CTAs, 8 parts each), finished jointly
+    for T in (1, 64, 128, 160):
+        p = mse.merged_launch_plan(T, H, Q, KV, TP16)
+        assert (p["swapab"], p["ctas"], p["parts"], p["joint_finish"]) == (1, 136, 8, 1)
+        assert p["bn"] == -(-T // 16) * 16
+
+
+@pytest.mark.parametrize("sm", range(40, 161, 7))
+def test_merged_projection_grid_rule_over_sm_counts(sm):
+    p = mse.merged_launch_plan(128, H, Q, KV, TP16, sm)
+    g_max, n_tiles, kbp = min(sm, 160), 17, H // 64
+    assert p["parts"] == stream_k_parts(n_tiles * kbp, kbp, p["ctas"])
+    per = g_max // n_tiles
+    if p["ctas"] != g_max:
+        # the aligned grid: a multiple of the tile count, at least 80% of the SMs
+        assert p["ctas"] == n_tiles * per and 5 * p["ctas"] >= 4 * g_max and p["parts"] == per
+    assert p["joint_finish"] == (1 if p["parts"] >= 6 else 0)
+
+
+def test_merged_plan_errors():
+    with pytest.raises(mse.MSEError):
+        mse.merged_launch_plan(128, H, 1536, 577, 16)   # kv_dim not divisible by tp
+    with pytest.raises(mse.MSEError):
+        mse.merged_launch_plan(0, H, Q, KV, TP16)
+    assert mse.merged_launch_plan(300, H, Q, KV, TP16)["swapab"] == 0   # the prefill kernels
+    assert mse.merged_launch_plan(128, 7200, Q, KV, TP16)["swapab"] == 0   # the generic kernels
