@@ -23,6 +23,17 @@ int main(void) {
                                                  128 * 7168, dummy, (size_t)1 << 30, NULL);
         if (st != MSE_ERR_NOT_DIVISIBLE) bad |= 32;
     }
+    /* launch plans are host arithmetic: the replicated decode layer's gate_up on 144 CTAs in two
+     * parts per tile, the merged projection on 136 CTAs in eight */
+    {
+        int32_t plan[8];
+        if (mse_mlp_launch_plan(64, 7168, 6144, 1, 1, 0, 152, plan) != MSE_OK || plan[0] != 1 || plan[1] != 144 ||
+            plan[3] != 2)
+            bad |= 64;
+        if (mse_merged_launch_plan(128, 7168, 1536, 576, 16, 152, plan) != MSE_OK || plan[1] != 136 || plan[2] != 8)
+            bad |= 128;
+        if (mse_mlp_launch_plan(64, 7168, 6144, 8, 9, 0, 152, plan) != MSE_ERR_INVALID_ARG) bad |= 256;
+    }
     printf("%s %d\n", mse_version(), bad);
     return bad;
 }
